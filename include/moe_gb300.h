@@ -1,0 +1,161 @@
+/* moe_gb300.h - C ABI of the single-GPU mixture-of-experts layer (GB300, sm_103a).
+ *
+ * The operation is the expert layer described in "X-Stage: An Overlooked
+ * Pipeline Stage for Communication-Computation Overlap in DiT Inference",
+ * MegaMoE background paragraph: a router selects the top-k experts of every
+ * token; Dispatch moves each token to its experts; each expert applies
+ * Linear-1 (hidden H -> intermediate I), the SwiGLU activation (Shazeer 2020,
+ * cited there) and Linear-2 (I -> H); Combine brings the k expert outputs
+ * back to the token and sums them weighted by the router weights.  On one
+ * GPU, Dispatch and Combine are permutations inside device memory.
+ *
+ * Numerics (fixed by this library; the page leaves them open):
+ *   - logits[t,e] = sum_h x[t,h]*Wr[h,e] (+bias[e]) in fp32 in one canonical
+ *     order: 32 partial sums, partial j over h = j, j+32, ... with fused
+ *     multiply-adds, then pairwise (j, j+16), (j, j+8), (j, j+4), (j, j+2),
+ *     (j, j+1) additions;
+ *   - top-k by descending logit, ties to the lower expert id, NaN below -inf;
+ *     weights = softmax over the k selected logits;
+ *   - Linear-1 / Linear-2: bf16 inputs, fp32 accumulation on the tensor cores;
+ *     the SwiGLU intermediate silu(g)*u is rounded to bf16; Linear-2's output
+ *     is scaled by the router weight in fp32;
+ *   - Combine: fp32 sum over the k slots in slot order j = 0..k-1, rounded to
+ *     bf16.  Results are bitwise reproducible run to run and across schedules.
+ *
+ * Memory: every tensor argument is a DEVICE pointer owned by the caller,
+ * 16-byte aligned, row-major and densely packed.  The plan owns only its
+ * workspace (sized for T_max at plan time) and never frees caller memory.
+ *
+ * Errors: arguments are validated on the host before anything is launched
+ * (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED, nothing enqueued).  Launch
+ * failures return MOE_ERR_CUDA.  Problems detected on the device (a wait that
+ * ran past timeout_ns, an index out of range) set a sticky error word in the
+ * plan that moe_get_status() reports (MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK);
+ * no kernel of this library traps or spins without a time limit.
+ *
+ * Threading: a plan may be used by one stream at a time.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, T out of range, bad config value   */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape outside the supported set (see moe_config_t)          */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                           */
+  MOE_ERR_OOM = 4,          /* workspace allocation failed                                 */
+  MOE_ERR_TIMEOUT = 5,      /* a device-side wait ran past timeout_ns (reported by status) */
+  MOE_ERR_DEVICE_CHECK = 6  /* a device-side consistency check failed (reported by status) */
+} moe_status_t;
+
+/* Tile schedules of the grouped GEMMs.  An expert wave is a run of
+ * consecutive experts (the X-Stage paper's MegaMoE discussion: waves group
+ * local experts; the original schedule runs a wave's Linear-1 and then its
+ * Linear-2 before the next wave; the cross-wave interleave places later
+ * waves' Linear-1 tiles between the current wave's Linear-2 tiles). */
+#define MOE_SCHED_WAVE_SERIAL 0 /* L1(w0) L2(w0) L1(w1) L2(w1) ... in one persistent launch      */
+#define MOE_SCHED_INTERLEAVED 1 /* L1(w0..wD-1), then L2(w) merged with L1(w+D), D = lead_waves  */
+#define MOE_SCHED_PHASED 2      /* all Linear-1 tiles in one launch, then all Linear-2 tiles     */
+
+/* flags */
+#define MOE_FLAG_ACT_BILINEAR (1u << 0) /* activation g*u instead of silu(g)*u (GLU "bilinear"
+                                           variant, same paper as SwiGLU); used by exactness tests */
+#define MOE_FLAG_STAGE_TIMING (1u << 1) /* record CUDA events between stages (moe_stage_times)    */
+#define MOE_FLAG_TEST_STALL (1u << 8)   /* test only: Linear-2 tiles wait for a readiness count that
+                                           is never reached, so the bounded wait expires and
+                                           moe_get_status reports MOE_ERR_TIMEOUT (no GPU fault)   */
+
+#define MOE_NUM_STAGES 5 /* router+top-k, dispatch sort+schedule, gather, grouped GEMMs, combine */
+
+typedef struct {
+  int32_t T_max;        /* largest token count a forward may use (>= 1)                         */
+  int32_t H;            /* hidden size: multiple of 256                                         */
+  int32_t I;            /* intermediate size per expert: multiple of 128                        */
+  int32_t E;            /* experts: 1 <= E <= 256                                               */
+  int32_t top_k;        /* 1 <= top_k <= min(E, 8)                                              */
+  int32_t schedule;     /* MOE_SCHED_*                                                          */
+  int32_t wave_experts; /* experts per wave; 0 = smallest run whose Linear-1 tiles fill the SMs */
+  int32_t lead_waves;   /* interleave lead D >= 1 (0 = default 1)                               */
+  uint32_t flags;       /* MOE_FLAG_*                                                           */
+  int64_t timeout_ns;   /* limit of any device-side wait; 0 = 1 s                               */
+  const float* router_bias; /* optional HOST pointer to E fp32 values added to every logit,
+                               copied at plan time; NULL = no bias                               */
+} moe_config_t;
+
+typedef struct moe_plan_s* moe_plan_t;
+
+/* Validate cfg, allocate the workspace for T_max on `device`, copy the bias.
+ * On success *out receives a plan to pass to the calls below. */
+MOE_API moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out);
+
+/* Bytes of device workspace moe_plan allocates for cfg (no allocation). */
+MOE_API moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
+
+/* One forward of the layer for T tokens (0 <= T <= T_max; T = 0 enqueues nothing), enqueued
+ * on `stream` (a cudaStream_t; NULL = the legacy default stream).  Never synchronises.
+ *   x             bf16 [T, H]            input tokens
+ *   router_logits fp32 [T, E]            OUTPUT when W_router != NULL, else INPUT
+ *   W_router      bf16 [H, E] or NULL    router weight
+ *   W1_gate_up    bf16 [E, H, 2I]        Linear-1; columns [0,I) gate, [I,2I) up
+ *   W2            bf16 [E, I, H]         Linear-2
+ *   y             bf16 [T, H]            output
+ * Device pointers, 16-byte aligned. */
+MOE_API moe_status_t moe_forward(moe_plan_t plan, int32_t T, const void* x, float* router_logits,
+                         const void* W_router, const void* W1_gate_up, const void* W2, void* y,
+                         void* stream);
+
+/* Synchronise `stream`, then read and clear the plan's device error word.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_get_status(moe_plan_t plan, void* stream);
+
+/* Copy the routing of the last forward (T tokens) into caller DEVICE buffers, stream-ordered
+ * (any pointer may be NULL to skip it):
+ *   ids int32 [T,k], w fp32 [T,k], counts int32 [E], offsets int32 [E+1],
+ *   row_pair int32 [T*k] (row -> t*k+j, rows grouped by expert, ascending t within an expert),
+ *   row_of int32 [T*k] ((t,j) -> row). */
+MOE_API moe_status_t moe_debug_routing(moe_plan_t plan, int32_t T, int32_t* ids, float* w, int32_t* counts,
+                               int32_t* offsets, int32_t* row_pair, int32_t* row_of, void* stream);
+
+/* Copy the intermediates of the last forward into caller DEVICE buffers (NULL skips):
+ *   h   bf16 [T*k, I]   activation rows in dispatch (row) order
+ *   P   fp32 [T*k, H]   router-weighted expert outputs, indexed by t*k+j */
+MOE_API moe_status_t moe_debug_intermediates(moe_plan_t plan, int32_t T, void* h, float* P, void* stream);
+
+/* Durations (ms) of the MOE_NUM_STAGES stages of the last forward; needs MOE_FLAG_STAGE_TIMING.
+ * Synchronises on the recorded events.  ms[3] is the grouped-GEMM launch(es). */
+MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
+
+/* Number of kernels the last moe_forward launched. */
+MOE_API moe_status_t moe_last_launch_count(moe_plan_t plan, int32_t* n);
+
+/* Free the plan and its workspace (synchronises the device first). */
+MOE_API moe_status_t moe_plan_destroy(moe_plan_t plan);
+
+/* Static description of a status code. */
+MOE_API const char* moe_status_string(moe_status_t s);
+
+/* Host-side evaluation of the tile schedule the device builds (for tests; no GPU needed).
+ * counts[E] rows per expert; writes up to cap tiles as 4 ints each
+ * {phase | n_block << 1, expert, m_block, global m-tile index} into tiles_out and the
+ * tile counts {linear-1 tiles, total tiles} into n_out[2]. */
+MOE_API moe_status_t moe_schedule_host(const int32_t* counts, int32_t E, int32_t H, int32_t I,
+                               int32_t num_sms, int32_t schedule, int32_t wave_experts,
+                               int32_t lead_waves, int32_t* tiles_out, int64_t cap, int64_t* n_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,386 @@
+// C ABI of the MoE layer (include/moe_gb300.h): plan, forward, status, debug
+// hooks.  Host code only; every step of the layer runs in this library's
+// kernels (router.cu, dispatch.cu, gemm.cu, combine.cu).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+struct moe_plan_s {
+  moe_config_t cfg;
+  int device;
+  int num_sms;
+  int64_t R_max, max_mt, max_tiles;
+  void* base;
+  size_t bytes;
+  float* bias;
+  Workspace ws;
+  cudaEvent_t ev[MOE_NUM_STAGES + 1];
+  bool timing;
+  int last_launches;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor [outer, inner] (row pitch = inner*2 bytes), box {64, box_outer}, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t validate_cfg(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T_max < 1 || c->H < 1 || c->I < 1 || c->E < 1 || c->top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (c->schedule < 0 || c->schedule > 2 || c->wave_experts < 0 || c->lead_waves < 0 || c->timeout_ns < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->H % L2_COLS != 0 || c->I % L1_COLS != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->E > MAX_E || c->top_k > MAX_K || c->top_k > c->E) return MOE_ERR_UNSUPPORTED;
+  const int64_t R = (int64_t)c->T_max * c->top_k;
+  if (R >= (1ll << 30) || (int64_t)c->E * c->H >= (1ll << 31) || (int64_t)c->E * c->I >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+struct Layout {
+  size_t off[14];
+  size_t total;
+};
+
+Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_tiles) {
+  const size_t sizes[14] = {
+      (size_t)R * 4,                       // ids
+      (size_t)R * 4,                       // w
+      (size_t)c.E * 4,                     // counts
+      (size_t)(c.E + 1) * 4,               // offsets
+      (size_t)R * 4,                       // row_pair
+      (size_t)R * 4,                       // row_of
+      (size_t)R * 4,                       // row_w
+      (size_t)R * c.H * 2,                 // x_perm
+      (size_t)R * c.I * 2,                 // h
+      (size_t)R * c.H * 4,                 // P
+      (size_t)max_tiles * 16,              // tiles
+      16,                                  // sched
+      (size_t)max_mt * 4,                  // ready
+      16,                                  // err
+  };
+  Layout L;
+  size_t o = 0;
+  for (int i = 0; i < 14; ++i) {
+    L.off[i] = o;
+    o += (sizes[i] + 255) & ~(size_t)255;
+  }
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const int64_t R = (int64_t)cfg->T_max * cfg->top_k;
+  const int64_t max_mt = max_mtiles(R, cfg->E);
+  const int64_t max_tiles = max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  *bytes = layout_of(*cfg, R, max_mt, max_tiles).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status_t st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!get_encode()) return MOE_ERR_CUDA;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_INVALID_ARG;
+  moe_plan_s* p = new (std::nothrow) moe_plan_s();
+  if (!p) return MOE_ERR_OOM;
+  p->cfg = *cfg;
+  p->cfg.router_bias = nullptr;
+  if (p->cfg.timeout_ns == 0) p->cfg.timeout_ns = 1000000000ll;
+  if (p->cfg.lead_waves == 0) p->cfg.lead_waves = 1;
+  p->device = device;
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device);
+  p->R_max = (int64_t)cfg->T_max * cfg->top_k;
+  p->max_mt = max_mtiles(p->R_max, cfg->E);
+  p->max_tiles = p->max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  Layout L = layout_of(*cfg, p->R_max, p->max_mt, p->max_tiles);
+  p->bytes = L.total;
+  auto fail = [&](moe_status_t s) {
+    if (p->base) cudaFree(p->base);
+    if (p->bias) cudaFree(p->bias);
+    delete p;
+    cudaSetDevice(cur);
+    return s;
+  };
+  if (cudaMalloc(&p->base, L.total) != cudaSuccess) {
+    cudaGetLastError();
+    p->base = nullptr;
+    return fail(MOE_ERR_OOM);
+  }
+  char* b = static_cast<char*>(p->base);
+  p->ws.ids = reinterpret_cast<int32_t*>(b + L.off[0]);
+  p->ws.w = reinterpret_cast<float*>(b + L.off[1]);
+  p->ws.counts = reinterpret_cast<int32_t*>(b + L.off[2]);
+  p->ws.offsets = reinterpret_cast<int32_t*>(b + L.off[3]);
+  p->ws.row_pair = reinterpret_cast<int32_t*>(b + L.off[4]);
+  p->ws.row_of = reinterpret_cast<int32_t*>(b + L.off[5]);
+  p->ws.row_w = reinterpret_cast<float*>(b + L.off[6]);
+  p->ws.x_perm = reinterpret_cast<uint16_t*>(b + L.off[7]);
+  p->ws.h = reinterpret_cast<uint16_t*>(b + L.off[8]);
+  p->ws.P = reinterpret_cast<float*>(b + L.off[9]);
+  p->ws.tiles = reinterpret_cast<int32_t*>(b + L.off[10]);
+  p->ws.sched = reinterpret_cast<int32_t*>(b + L.off[11]);
+  p->ws.ready = reinterpret_cast<int32_t*>(b + L.off[12]);
+  p->ws.err = reinterpret_cast<uint32_t*>(b + L.off[13]);
+  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (cfg->router_bias) {
+    if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
+      cudaGetLastError();
+      p->bias = nullptr;
+      return fail(MOE_ERR_OOM);
+    }
+    if (cudaMemcpy(p->bias, cfg->router_bias, sizeof(float) * cfg->E, cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(MOE_ERR_CUDA);
+  }
+  if (gemm_prepare(device) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
+  if (p->timing)
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i)
+      if (cudaEventCreate(&p->ev[i]) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  cudaSetDevice(cur);
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_logits, const void* W_router,
+                         const void* W1, const void* W2, void* y, void* stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  const moe_config_t& c = p->cfg;
+  if (T < 0 || T > c.T_max) return MOE_ERR_INVALID_ARG;
+  if (!x || !router_logits || !W1 || !W2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_logits) || !aligned16(W1) || !aligned16(W2) || !aligned16(y) ||
+      (W_router && !aligned16(W_router)))
+    return MOE_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cur != p->device) return MOE_ERR_INVALID_ARG;
+  p->last_launches = 0;
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int k = c.top_k, E = c.E, H = c.H, I = c.I;
+  const int R = T * k;
+  int nl = 0;
+  auto rec = [&](int i) {
+    if (p->timing) cudaEventRecord(p->ev[i], st);
+  };
+#define MOE_CK(x)                                   \
+  do {                                              \
+    if ((x) != cudaSuccess) {                       \
+      p->last_launches = nl;                        \
+      return MOE_ERR_CUDA;                          \
+    }                                               \
+  } while (0)
+  rec(0);
+  MOE_CK(cudaMemsetAsync(p->ws.counts, 0, sizeof(int32_t) * E, st));
+  if (W_router) {
+    MOE_CK(launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router), p->bias,
+                                router_logits, T, H, E, st));
+    ++nl;
+  }
+  MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, st));
+  ++nl;
+  rec(1);
+  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->num_sms, c.schedule, c.wave_experts, c.lead_waves, st));
+  ++nl;
+  rec(2);
+  MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.row_pair, R, H, k, p->ws.x_perm, st));
+  ++nl;
+  rec(3);
+  CUtensorMap tA1, tB1, tA2, tB2;
+  if (!make_tmap(&tA1, p->ws.x_perm, H, R, BM) || !make_tmap(&tB1, W1, 2 * I, (uint64_t)E * H, BK) ||
+      !make_tmap(&tA2, p->ws.h, I, R, BM) || !make_tmap(&tB2, W2, H, (uint64_t)E * I, BK)) {
+    p->last_launches = nl;
+    return MOE_ERR_CUDA;
+  }
+  GemmArgs ga;
+  ga.tiles = reinterpret_cast<const int4*>(p->ws.tiles);
+  ga.sched = p->ws.sched;
+  ga.counts = p->ws.counts;
+  ga.offsets = p->ws.offsets;
+  ga.row_w = p->ws.row_w;
+  ga.row_pair = p->ws.row_pair;
+  ga.h = p->ws.h;
+  ga.P = p->ws.P;
+  ga.ready = p->ws.ready;
+  ga.err = p->ws.err;
+  ga.H = H;
+  ga.I = I;
+  ga.E = E;
+  ga.R = R;
+  ga.nL1 = I / L1_COLS;
+  ga.flags = c.flags;
+  ga.timeout_ns = c.timeout_ns;
+  if (c.schedule == MOE_SCHED_PHASED) {
+    ga.range_sel = 0;
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->num_sms, st));
+    ga.range_sel = 1;
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->num_sms, st));
+    nl += 2;
+  } else {
+    ga.range_sel = 2;
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->num_sms, st));
+    ++nl;
+  }
+  rec(4);
+  MOE_CK(launch_combine(p->ws.P, T, H, k, static_cast<uint16_t*>(y), p->num_sms, st));
+  ++nl;
+  rec(5);
+#undef MOE_CK
+  p->last_launches = nl;
+  return MOE_OK;
+}
+
+moe_status_t moe_get_status(moe_plan_t p, void* stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t e = 0;
+  if (cudaMemcpy(&e, p->ws.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != 0 && cudaMemset(p->ws.err, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (e & ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (e & ERR_CHECK) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_routing(moe_plan_t p, int32_t T, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                               int32_t* row_pair, int32_t* row_of, void* stream) {
+  if (!p || T < 0 || T > p->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t R = (size_t)T * p->cfg.top_k;
+  const size_t E = p->cfg.E;
+  auto cp = [&](void* dst, const void* src, size_t n) {
+    return (dst && n) ? cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, st) : cudaSuccess;
+  };
+  if (cp(ids, p->ws.ids, R * 4) || cp(w, p->ws.w, R * 4) || cp(counts, p->ws.counts, E * 4) ||
+      cp(offsets, p->ws.offsets, (E + 1) * 4) || cp(row_pair, p->ws.row_pair, R * 4) ||
+      cp(row_of, p->ws.row_of, R * 4))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_intermediates(moe_plan_t p, int32_t T, void* h, float* P, void* stream) {
+  if (!p || T < 0 || T > p->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t R = (size_t)T * p->cfg.top_k;
+  if (h && R && cudaMemcpyAsync(h, p->ws.h, R * p->cfg.I * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (P && R && cudaMemcpyAsync(P, p->ws.P, R * p->cfg.H * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_stage_times(moe_plan_t p, float* ms) {
+  if (!p || !ms || !p->timing) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_NUM_STAGES; ++i) {
+    if (cudaEventSynchronize(p->ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms[i], p->ev[i], p->ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_last_launch_count(moe_plan_t p, int32_t* n) {
+  if (!p || !n) return MOE_ERR_INVALID_ARG;
+  *n = p->last_launches;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan_destroy(moe_plan_t p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  if (p->timing)
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i) cudaEventDestroy(p->ev[i]);
+  if (p->base) cudaFree(p->base);
+  if (p->bias) cudaFree(p->bias);
+  cudaSetDevice(cur);
+  delete p;
+  return MOE_OK;
+}
+
+moe_status_t moe_schedule_host(const int32_t* counts, int32_t E, int32_t H, int32_t I, int32_t num_sms,
+                               int32_t schedule, int32_t wave_experts, int32_t lead_waves, int32_t* tiles_out,
+                               int64_t cap, int64_t* n_out) {
+  if (!counts || !n_out || E < 1 || E > MAX_E || H % L2_COLS || I % L1_COLS || num_sms < 1 || schedule < 0 ||
+      schedule > 2)
+    return MOE_ERR_INVALID_ARG;
+  SchedTables* s = new (std::nothrow) SchedTables();
+  if (!s) return MOE_ERR_OOM;
+  sched_build(*s, counts, E, I / L1_COLS, H / L2_COLS, num_sms, schedule, wave_experts,
+              lead_waves == 0 ? 1 : lead_waves);
+  n_out[0] = s->n1_total;
+  n_out[1] = s->total;
+  if (tiles_out) {
+    if (cap < s->total) {
+      delete s;
+      return MOE_ERR_INVALID_ARG;
+    }
+    for (int g = 0; g < s->total_mt; ++g) sched_emit_mtile(*s, g, tiles_out);
+  }
+  delete s;
+  return MOE_OK;
+}
+
+}  // extern "C"

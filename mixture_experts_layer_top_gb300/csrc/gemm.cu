@@ -1,0 +1,336 @@
+// Persistent grouped GEMM for both expert projections of the MoE layer.
+//
+// Linear-1 tile (phase 0): rows [offsets[e] + 128 m, +128) of x_perm times
+//   W1[e][:, 128 n .. +128] (gate) and W1[e][:, I + 128 n .. +128] (up), one
+//   M=128 x N=256 tcgen05 accumulator; epilogue h = bf16(silu(g) * u).
+// Linear-2 tile (phase 1): the same rows of h times W2[e][:, 256 n .. +256];
+//   epilogue P[t*k + j] = w[t,j] * acc (fp32), the router-weight scale.
+// (X-Stage paper, MegaMoE background: Linear-1 projects hidden to
+// intermediate, SwiGLU is applied, Linear-2 projects back; the kernel design -
+// persistent, warp-specialised, TMA producer, tensor-core issuer, epilogue
+// roles coupled through finite accumulator staging - follows the fused-kernel
+// description there, rebuilt here for tcgen05/TMEM on sm_103a.)
+//
+// Roles (192 threads):  warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer (one thread), warps 2..5 = epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31, i.e. tile rows).  Tiles come from a ticket list built by
+// the dispatch kernel; CTA b takes tickets b, b+grid, ... in order.  A
+// Linear-2 tile first waits until the ready counter of its m-tile shows all
+// Linear-1 tiles of those rows stored; tickets are in a topological order and
+// every CTA is resident (grid <= SMs, 1 CTA/SM), so the waits always finish.
+// Every wait is bounded by timeout_ns; on expiry the CTA records
+// ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+//
+// Shared-memory operand layouts (128-byte swizzle, as written by TMA):
+//   A (K-major): 128 rows x 128 B per stage; descriptor SBO = 1024 B (8-row
+//     group), K step of 16 elements = +32 B on the start address.
+//   B (N-major): four 64-column boxes of 64 K-rows x 128 B (8 KB each);
+//     descriptor LBO = 8 KB (next 64 columns), SBO = 1024 B (next 8 K-rows),
+//     K step of 16 rows = +2048 B.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int GEMM_THREADS = 192;
+constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
+constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
+constexpr int GEMM_SMEM = SMEM_BAR_OFF + 256 + 1024;   // + barriers/flags + alignment slack
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N, true);
+
+struct SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int ep_ok[2];   // epilogue go/stop decision of the waiting thread, by tile parity
+};
+
+__device__ __forceinline__ void set_abort(SmemCtl* ctl, uint32_t* err, uint32_t code) {
+  atomicOr(err, code);
+  *(volatile int*)&ctl->abort_flag = 1;
+}
+
+__device__ __forceinline__ void tile_range(const GemmArgs& a, int& begin, int& end) {
+  const int n1 = a.sched[0], tot = a.sched[1];
+  begin = (a.range_sel == 1) ? n1 : 0;
+  end = (a.range_sel == 0) ? n1 : tot;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_BAR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&ctl->full[s], 1);
+      ptx::mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl->tfull[b], 1);
+      ptx::mbar_init(&ctl->tempty[b], 4 * 32);
+    }
+    ptx::mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmA1);
+    ptx::tma_prefetch_desc(&tmB1);
+    ptx::tma_prefetch_desc(&tmA2);
+    ptx::tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc<TMEM_COLS>(&ctl->tmem_base);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  int t_begin, t_end;
+  tile_range(args, t_begin, t_end);
+  const int64_t tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_normal();
+      const uint64_t pol_a = ptx::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_par = 0;   // per stage: issued at least once / parity of last issue
+      for (int i = t_begin + blockIdx.x; i < t_end && !*abort_flag; i += gridDim.x) {
+        const int4 tl = args.tiles[i];
+        const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, m = tl.z, g = tl.w;
+        const int row0 = args.offsets[e] + m * BM;
+        if (ph == 1) {
+          // wait for every Linear-1 tile of this m-tile (bounded)
+          const int* rp = args.ready + g;
+          const int need = args.nL1 + ((args.flags & MOE_FLAG_TEST_STALL) ? 1 : 0);
+          if (ptx::ld_acquire_gpu(rp) < need) {
+            const uint64_t t0 = ptx::globaltimer();
+            bool ok = false;
+            while (true) {
+              if (ptx::ld_acquire_gpu(rp) >= need) { ok = true; break; }
+              if (*abort_flag) break;
+              if ((int64_t)(ptx::globaltimer() - t0) > tmo) break;
+              __nanosleep(64);
+            }
+            if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
+          }
+          ptx::fence_proxy_async_global();
+        }
+        const int nk = (ph == 0 ? args.H : args.I) / BK;
+        const CUtensorMap* tA = ph == 0 ? &tmA1 : &tmA2;
+        const CUtensorMap* tB = ph == 0 ? &tmB1 : &tmB2;
+        const int brow0 = e * (ph == 0 ? args.H : args.I);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, tmo, abort_flag)) { ok = false; break; }
+          uint8_t* sA = smem + stage * STAGE_BYTES;
+          uint8_t* sB = sA + A_STAGE_BYTES;
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          ptx::tma_load_2d(tA, &ctl->full[stage], sA, kb * BK, row0, pol_a);
+          if (ph == 0) {
+            const int c0 = nb * L1_COLS;
+            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 0 * B_BOX_BYTES, c0, brow0 + kb * BK, pol_w);
+            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 1 * B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
+            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 2 * B_BOX_BYTES, args.I + c0, brow0 + kb * BK, pol_w);
+            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 3 * B_BOX_BYTES, args.I + c0 + 64, brow0 + kb * BK,
+                             pol_w);
+          } else {
+            const int c0 = nb * L2_COLS;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              ptx::tma_load_2d(tB, &ctl->full[stage], sB + q * B_BOX_BYTES, c0 + 64 * q, brow0 + kb * BK, pol_w);
+          }
+          issued_mask |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
+      }
+      if (*abort_flag) {
+        // let every issued copy land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask & (1u << s)) {
+            int dummy = 0;
+            ptx::mbar_wait(&ctl->full[s], (last_par >> s) & 1u, tmo, &dummy);
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool issued_any = false;
+      for (int i = t_begin + blockIdx.x; i < t_end && !*abort_flag; i += gridDim.x, ++local) {
+        const int4 tl = args.tiles[i];
+        const int ph = tl.x & 1;
+        const int as = local & 1;
+        const uint32_t aphase = (local >> 1) & 1;
+        if (!ptx::mbar_wait(&ctl->tempty[as], aphase ^ 1u, tmo, abort_flag)) {
+          set_abort(ctl, args.err, ERR_TIMEOUT);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(as * MMA_N);
+        const int nk = (ph == 0 ? args.H : args.I) / BK;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, tmo, abort_flag)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b0 = a0 + A_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 2048, B_BOX_BYTES, 1024);
+            ptx::mma_bf16(d, ad, bd, IDESC, (kb | kk) != 0);
+          }
+          issued_any = true;
+          ptx::mma_commit(&ctl->empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
+        ptx::mma_commit(&ctl->tfull[as]);
+      }
+      if (*abort_flag && issued_any) {
+        // make sure no MMA still reads shared memory or writes TMEM
+        ptx::mma_commit(&ctl->drain);
+        int dummy = 0;
+        ptx::mbar_wait(&ctl->drain, 0, tmo, &dummy);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;               // TMEM lane quadrant
+    const int r = q * 32 + lane;          // tile row
+    const int ep_tid = threadIdx.x - 64;  // 0..127
+    int local = 0;
+    const bool bilinear = (args.flags & MOE_FLAG_ACT_BILINEAR) != 0;
+    for (int i = t_begin + blockIdx.x; i < t_end; i += gridDim.x, ++local) {
+      const int4 tl = args.tiles[i];
+      const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, m = tl.z, g = tl.w;
+      const int as = local & 1;
+      const uint32_t aphase = (local >> 1) & 1;
+      // one thread waits, the named barrier broadcasts its decision to all 128
+      if (ep_tid == 0) {
+        const bool okw = ptx::mbar_wait(&ctl->tfull[as], aphase, tmo, abort_flag);
+        if (!okw) set_abort(ctl, args.err, ERR_TIMEOUT);
+        *(volatile int*)&ctl->ep_ok[local & 1] = okw ? 1 : 0;
+      }
+      ptx::named_bar_sync(1, 128);
+      if (!*(volatile int*)&ctl->ep_ok[local & 1]) break;
+      ptx::tc_fence_after();
+      const int rows_valid = args.counts[e] - m * BM;
+      const int grow = args.offsets[e] + m * BM + r;
+      bool valid = r < rows_valid;
+      if (valid && (grow < 0 || grow >= args.R)) {
+        atomicOr(args.err, ERR_CHECK);
+        valid = false;
+      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * MMA_N);
+      if (ph == 0) {
+        uint16_t* hrow = args.h + (size_t)grow * args.I + nb * L1_COLS;
+#pragma unroll 1
+        for (int c = 0; c < L1_COLS / 32; ++c) {
+          uint32_t gv[32], uv[32];
+          ptx::tmem_ld32(taddr + c * 32, gv);
+          ptx::tmem_ld32(taddr + L1_COLS + c * 32, uv);
+          ptx::tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+            const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
+            const float v0 = bilinear ? g0 * u0 : silu_mul(g0, u0);
+            const float v1 = bilinear ? g1 * u1 : silu_mul(g1, u1);
+            pk[j] = pack_bf16x2(v0, v1);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+        }
+      } else {
+        const float wgt = valid ? args.row_w[grow] : 0.0f;
+        const int pair = valid ? args.row_pair[grow] : 0;
+        float* prow = args.P + (size_t)pair * args.H + nb * L2_COLS;
+#pragma unroll 1
+        for (int c = 0; c < L2_COLS / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(taddr + c * 32, v);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(wgt * __uint_as_float(v[4 * j]), wgt * __uint_as_float(v[4 * j + 1]),
+                                   wgt * __uint_as_float(v[4 * j + 2]), wgt * __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ctl->tempty[as]);
+      if (ph == 0) {
+        // publish: these rows' h columns are stored (visible to TMA readers)
+        ptx::fence_proxy_async_global();
+        ptx::named_bar_sync(1, 128);
+        if (ep_tid == 0) {
+          __threadfence();
+          ptx::red_release_add_gpu(args.ready + g, 1);
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc<TMEM_COLS>(tmem_base);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_prepare(int device) {
+  (void)device;
+  return cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+}
+
+cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
+                                const CUtensorMap& tB2, const GemmArgs& a, int grid, cudaStream_t st) {
+  grouped_gemm_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(tA1, tB1, tA2, tB2, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

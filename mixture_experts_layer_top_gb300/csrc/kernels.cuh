@@ -1,0 +1,58 @@
+// Host-side launchers of the MoE layer kernels (internal to libmoe_gb300.so).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct Workspace {
+  int32_t* ids;       // [T_max*k]
+  float* w;           // [T_max*k]
+  int32_t* counts;    // [E]
+  int32_t* offsets;   // [E+1]
+  int32_t* row_pair;  // [R_max]
+  int32_t* row_of;    // [R_max]
+  float* row_w;       // [R_max]
+  uint16_t* x_perm;   // [R_max, H] bf16
+  uint16_t* h;        // [R_max, I] bf16
+  float* P;           // [R_max, H] fp32, indexed by t*k+j
+  int32_t* tiles;     // [max_tiles*4]
+  int32_t* sched;     // [4]: linear-1 tiles, total tiles, m-tiles
+  int32_t* ready;     // [max_mt]
+  uint32_t* err;      // [1]
+};
+
+struct GemmArgs {
+  const int4* tiles;
+  const int32_t* sched;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const float* row_w;
+  const int32_t* row_pair;
+  uint16_t* h;
+  float* P;
+  int32_t* ready;
+  uint32_t* err;
+  int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all
+  int H, I, E, R, nL1;
+  uint32_t flags;
+  int64_t timeout_ns;
+};
+
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
+                                 int H, int E, cudaStream_t st);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                        cudaStream_t st);
+cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
+                            int wave_experts, int lead, cudaStream_t st);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, int R, int H, int k, uint16_t* x_perm,
+                          cudaStream_t st);
+cudaError_t gemm_prepare(int device);
+cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
+                                const CUtensorMap& tB2, const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_combine(const float* P, int T, int H, int k, uint16_t* y, int num_sms, cudaStream_t st);
+
+}  // namespace moe

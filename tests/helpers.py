@@ -1,0 +1,73 @@
+"""Shared helpers of the GPU tests: inputs (seeded, from synth), the oracle's
+expectations, and the output tolerance.
+
+Tolerance on y (bf16): max |y - y_ref| <= 2e-2 * RMS(y_ref), and |y - y_ref| <=
+3e-2 * |y_ref| wherever |y_ref| > 0.1 * RMS(y_ref).  Routing (logits, ids,
+counts, offsets, row_pair, row_of) must be bit-exact; router weights within
+1e-6 relative (the GPU's exp is not the host's)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 bit patterns (host)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def from_bits(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def f64(b: np.ndarray) -> np.ndarray:
+    return oracle.bf16_to_f32(b).astype(np.float64)
+
+
+def check_y(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: str = "y"):
+    yg, yr = f64(y_gpu_bits), f64(y_ref_bits)
+    assert yg.shape == yr.shape
+    rms = float(np.sqrt(np.mean(yr ** 2)))
+    d = np.abs(yg - yr)
+    assert np.all(np.isfinite(yg)), f"{what}: non-finite outputs"
+    assert d.max() <= 2e-2 * rms, f"{what}: max abs err {d.max():.3e} > 2e-2 * rms {rms:.3e}"
+    big = np.abs(yr) > 0.1 * rms
+    rel = d[big] / np.abs(yr[big])
+    assert rel.size == 0 or rel.max() <= 3e-2, f"{what}: max rel err {rel.max():.3e} > 3e-2"
+    return dict(max_abs=float(d.max()), rms=rms, max_rel=float(rel.max()) if rel.size else 0.0)
+
+
+def routing_equal(gpu: dict, ref: dict, T: int):
+    ids = gpu["ids"].cpu().numpy()
+    assert np.array_equal(ids, ref["ids"]), "ids differ"
+    assert np.array_equal(gpu["counts"].cpu().numpy(), ref["counts"]), "counts differ"
+    assert np.array_equal(gpu["offsets"].cpu().numpy(), ref["offsets"]), "offsets differ"
+    assert np.array_equal(gpu["row_pair"].cpu().numpy(), ref["row_pair"]), "row_pair differs"
+    assert np.array_equal(gpu["row_of"].cpu().numpy(), ref["row_of"]), "row_of differs"
+    w = gpu["w"].cpu().numpy()
+    assert np.allclose(w, ref["w"], rtol=1e-6, atol=1e-30, equal_nan=True), "router weights differ"
+
+
+def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
+    if n >= T:
+        return np.arange(T, dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    s = rng.choice(T, size=n, replace=False)
+    s[0], s[-1] = 0, T - 1
+    return np.sort(s).astype(np.int64)
+
+
+def oracle_for(wl: synth.Workload, x_bits: np.ndarray, Wr_bits: np.ndarray, bias, tokens, act=0,
+               full_weights=None, want_intermediates=False):
+    """Oracle on a workload: routing for all tokens, y for ``tokens``.  Expert weights
+    come from the host generator (per expert slice) unless ``full_weights`` is given."""
+    if full_weights is not None:
+        W1, W2 = full_weights
+    else:
+        W1 = lambda e: synth.expert_slice_host(wl, "W1", e)   # noqa: E731
+        W2 = lambda e: synth.expert_slice_host(wl, "W2", e)   # noqa: E731
+    return oracle.forward(x_bits, Wr_bits, bias, W1, W2, wl.k, act=act, tokens=tokens,
+                          want_intermediates=want_intermediates)

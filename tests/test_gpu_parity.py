@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every input comes from the seeded generator; device tensors are drawn on the
+GPU by the torch implementation, which is bit-identical to the host one the
+oracle uses (checked by test_device_generator_matches_host)."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_top_gb300 as moe
+import oracle
+import synth
+from helpers import bits, check_y, f64, from_bits, oracle_for, routing_equal, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    moe.build()
+    oracle.build()
+    synth.build_host()
+    torch.cuda.init()
+
+
+def _layer(wl, schedule=0, flags=0, T_max=None, timeout_ns=0, wave_experts=0, lead=1, bias=None):
+    cfg = moe.MoEConfig(T_max or wl.T, wl.H, wl.I, wl.E, wl.k, schedule=schedule, flags=flags,
+                        timeout_ns=timeout_ns, wave_experts=wave_experts, lead_waves=lead)
+    return moe.MoELayer(cfg, 0, router_bias=bias)
+
+
+def _bias(wl):
+    return synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
+
+
+# --------------------------------------------------------------------------- generator
+def test_device_generator_matches_host():
+    for tid, std, start in [(1, 1.0, 0), (3, 0.02, 5 * 10 ** 9 + 17)]:
+        a = synth.normal_bf16_host(1 << 20, std, tid, 0, start=start)
+        d = synth.normal_bf16_torch(1 << 20, std, tid, 0, start=start, device="cuda")
+        assert np.array_equal(a, bits(d))
+
+
+# --------------------------------------------------------------------------- tiny config
+@pytest.mark.parametrize("schedule", [0, 1, 2])
+def test_tiny_full_parity(schedule):
+    wl = synth.WORKLOADS["tiny"]
+    h = synth.host_inputs(wl)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    layer = _layer(wl, schedule)
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    assert np.array_equal(logits.cpu().numpy(), ref["logits"]), "logits not bit-exact"
+    routing_equal(layer.routing(wl.T), ref, wl.T)
+    check_y(bits(y), ref["y"])
+    assert layer.launch_count() == (6 if schedule == 2 else 5)
+
+
+def test_bilinear_integer_exact():
+    """Integer-valued inputs and the bilinear GLU: every accumulation is exact, so
+    h, P and y must match the oracle bit for bit (tiling, TMA boxes, descriptors)."""
+    T, H, I, E, k = 300, 512, 256, 8, 2
+    rng = np.random.default_rng(11)
+
+    def tern(shape, p):
+        return ((rng.random(shape) < p) * rng.choice([-1.0, 1.0], size=shape)).astype(np.float32)
+
+    x = oracle.f32_to_bf16(tern((T, H), 0.5))
+    Wr = oracle.f32_to_bf16((rng.standard_normal((H, E)) / np.sqrt(H)).astype(np.float32))
+    W1 = oracle.f32_to_bf16(tern((E, H, 2 * I), 0.2))
+    W2 = oracle.f32_to_bf16(tern((E, I, H), 0.2))
+    ref = oracle.forward(x, Wr, None, W1, W2, k, act=oracle.ACT_BILINEAR, want_intermediates=True)
+    layer = moe.MoELayer(moe.MoEConfig(T, H, I, E, k, flags=moe.MOE_FLAG_ACT_BILINEAR), 0)
+    y, _ = layer.forward(from_bits(x), from_bits(Wr), from_bits(W1), from_bits(W2), check=True)
+    r = layer.routing(T)
+    routing_equal(r, ref, T)
+    hh, P = layer.intermediates(T)
+    row_of = ref["row_of"].reshape(T, k)
+    h_gpu = f64(bits(hh))
+    P_gpu = P.cpu().numpy()
+    a_ref = f64(ref["a"])
+    P_ref = ref["w"][:, :, None].astype(np.float32) * ref["o"]       # fp32 product, as the epilogue
+    for t in range(T):
+        for j in range(k):
+            assert np.array_equal(h_gpu[row_of[t, j]], a_ref[t, j]), f"h row (t={t}, j={j})"
+            assert np.array_equal(P_gpu[t * k + j], P_ref[t, j]), f"P row (t={t}, j={j})"
+    assert np.array_equal(f64(bits(y)), f64(ref["y"])), "y not bit-exact on integer inputs"
+
+
+def test_schedules_bitwise_identical():
+    wl = synth.Workload("mid", 2048, 1024, 512, 32, 4)
+    d = synth.device_inputs(wl)
+    outs = []
+    for sched, we, lead in [(0, 0, 1), (1, 0, 1), (1, 0, 3), (2, 0, 1), (0, 3, 1), (1, 2, 2)]:
+        layer = _layer(wl, sched, wave_experts=we, lead=lead)
+        y, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+        y2, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "repeat not bitwise identical"
+        outs.append(bits(y))
+        layer.close()
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "schedules differ"
+    h = synth.host_inputs(wl, weights=False)
+    tok = sample_tokens(wl.T, 48)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, tok)
+    check_y(outs[0][tok], ref["y"])
+
+
+# --------------------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name,nsample,schedule", [
+    ("fine", 48, 0), ("fine", 16, 1), ("skew", 32, 0), ("large", 4, 0), ("smallT", 4, 0)])
+def test_workload_parity(name, nsample, schedule):
+    wl = synth.WORKLOADS[name]
+    bias = _bias(wl)
+    d = synth.device_inputs(wl)
+    layer = _layer(wl, schedule, bias=bias)
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    h = synth.host_inputs(wl, weights=False)
+    tok = sample_tokens(wl.T, nsample)
+    ref = oracle_for(wl, h["x"], h["Wr"], bias, tok)
+    assert np.array_equal(logits.cpu().numpy(), ref["logits"]), "logits not bit-exact"
+    routing_equal(layer.routing(wl.T), ref, wl.T)
+    if name == "skew":
+        assert (ref["counts"] == 0).any(), "skewed workload should leave experts idle"
+    check_y(bits(y)[tok], ref["y"], what=name)
+    del d
+    layer.close()
+    torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("T", [1, 127, 129, 1000])
+def test_ragged_token_counts(T):
+    wl = synth.Workload("edge", T, 512, 256, 16, 4)
+    h = synth.host_inputs(wl)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    layer = _layer(wl, 0, T_max=1024)
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    assert np.array_equal(logits.cpu().numpy(), ref["logits"])
+    routing_equal(layer.routing(T), ref, T)
+    check_y(bits(y), ref["y"])
+
+
+def test_zero_tokens_is_noop():
+    wl = synth.WORKLOADS["tiny"]
+    layer = _layer(wl)
+    x = torch.zeros((0, wl.H), dtype=torch.bfloat16, device="cuda")
+    st = moe.moe_forward(layer.plan, 0, 16, 16, 16, 16, 16, 16, 0)   # nothing dereferenced at T = 0
+    assert st == moe.MOE_OK and layer.launch_count() == 0
+    del x
+
+
+def test_logits_as_input_and_one_hot_expert():
+    """W_router = NULL: the caller's logits route; all tokens to one expert (all
+    rows in one expert, every other expert empty)."""
+    wl = synth.Workload("onehot", 700, 512, 256, 8, 1)
+    h = synth.host_inputs(wl)
+    logits = np.full((wl.T, wl.E), -5.0, np.float32)
+    logits[:, 6] = 3.0
+    ref = oracle.forward(h["x"], h["Wr"], None, h["W1"], h["W2"], wl.k, logits=logits)
+    assert ref["counts"][6] == wl.T and ref["counts"].sum() == wl.T
+    layer = _layer(wl)
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    lg = torch.from_numpy(logits).cuda()
+    y, _ = layer.forward(d["x"], None, d["W1"], d["W2"], logits=lg, check=True)
+    routing_equal(layer.routing(wl.T), ref, wl.T)
+    check_y(bits(y), ref["y"])
+
+
+def test_nan_token_stays_local():
+    wl = synth.Workload("nan", 256, 512, 256, 8, 2)
+    h = synth.host_inputs(wl)
+    x = h["x"].copy()
+    x[5, 17] = 0x7FC0           # bf16 quiet NaN
+    ref = oracle_for(wl, x, h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    layer = _layer(wl)
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    y, logits = layer.forward(from_bits(x), d["Wr"], d["W1"], d["W2"], check=True)
+    yg = f64(bits(y))
+    assert np.all(np.isnan(yg[5])) and np.all(np.isnan(f64(ref["y"])[5]))
+    others = np.arange(wl.T) != 5
+    assert np.all(np.isfinite(yg[others]))
+    assert np.array_equal(layer.routing(wl.T)["ids"].cpu().numpy(), ref["ids"])
+    check_y(bits(y)[others], ref["y"][others])
+
+
+def test_timeout_reports_status_and_context_survives():
+    """Host-made fault: Linear-2 tiles wait for a readiness count that nothing
+    reaches; the bounded wait expires (20 ms), the kernel exits cleanly and the
+    status word says MOE_ERR_TIMEOUT.  The next forward on a fresh plan works."""
+    wl = synth.WORKLOADS["tiny"]
+    d = synth.device_inputs(wl)
+    bad = _layer(wl, 0, flags=moe.MOE_FLAG_TEST_STALL, timeout_ns=20_000_000)
+    bad.forward(d["x"], d["Wr"], d["W1"], d["W2"])
+    assert moe.moe_get_status(bad.plan, bad._stream()) == moe.MOE_ERR_TIMEOUT
+    assert moe.moe_get_status(bad.plan, bad._stream()) == moe.MOE_OK      # cleared after reading
+    bad.close()
+    good = _layer(wl, 0)
+    y, _ = good.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    h = synth.host_inputs(wl)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    check_y(bits(y), ref["y"])
+
+
+def test_invalid_arguments_rejected_before_launch():
+    wl = synth.WORKLOADS["tiny"]
+    layer = _layer(wl)
+    d = synth.device_inputs(wl)
+    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    p = [d["x"].data_ptr(), lg.data_ptr(), d["Wr"].data_ptr(), d["W1"].data_ptr(), d["W2"].data_ptr(),
+         y.data_ptr()]
+    s = layer._stream()
+    assert moe.moe_forward(layer.plan, wl.T + 1, *p, s) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_forward(layer.plan, -1, *p, s) == moe.MOE_ERR_INVALID_ARG
+    bad = list(p)
+    bad[0] += 2                                                  # misaligned x
+    assert moe.moe_forward(layer.plan, wl.T, *bad, s) == moe.MOE_ERR_INVALID_ARG
+    bad = list(p)
+    bad[3] = None
+    assert moe.moe_forward(layer.plan, wl.T, *bad, s) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_get_status(layer.plan, s) == moe.MOE_OK
