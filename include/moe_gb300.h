@@ -117,6 +117,16 @@ MOE_API moe_status_t moe_forward(moe_plan_t plan, int32_t T, const void* x, floa
                          const void* W_router, const void* W1_gate_up, const void* W2, void* y,
                          void* stream);
 
+/* moe_forward with the token tensors in HOST memory: copies x_host (bf16 [T, H]) into a
+ * plan-owned device buffer, runs the layer, and copies y (bf16 [T, H]) back into y_host, all
+ * enqueued on `stream` (the copies overlap nothing and are asynchronous when the host buffers
+ * are page-locked; pageable buffers make them synchronous).  router_logits, W_router,
+ * W1_gate_up and W2 are DEVICE pointers exactly as in moe_forward.  The caller must not touch
+ * y_host before the stream reaches this point (e.g. cudaStreamSynchronize). */
+MOE_API moe_status_t moe_forward_host(moe_plan_t plan, int32_t T, const void* x_host, float* router_logits,
+                              const void* W_router, const void* W1_gate_up, const void* W2, void* y_host,
+                              void* stream);
+
 /* Synchronise `stream`, then read and clear the plan's device error word.
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */
 MOE_API moe_status_t moe_get_status(moe_plan_t plan, void* stream);

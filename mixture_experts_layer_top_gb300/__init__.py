@@ -40,7 +40,8 @@ MOE_FLAG_TEST_STALL = 1 << 8
 MOE_NUM_STAGES = 5
 STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")
 
-EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_get_status", "moe_debug_routing",
+EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_get_status",
+            "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
             "moe_status_string", "moe_schedule_host")
 
@@ -81,6 +82,7 @@ def load() -> ctypes.CDLL:
     L.moe_plan.argtypes = [P(moe_config_t), ctypes.c_int, P(vp)]
     L.moe_workspace_bytes.argtypes = [P(moe_config_t), P(ctypes.c_size_t)]
     L.moe_forward.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_forward_host.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     L.moe_get_status.argtypes = [vp, vp]
     L.moe_debug_routing.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     L.moe_debug_intermediates.argtypes = [vp, i32, vp, vp, vp]
@@ -121,6 +123,12 @@ def moe_plan(cfg: moe_config_t, device: int = 0) -> int:
 def moe_forward(plan: int, T: int, x: int, router_logits: int, W_router: Optional[int], W1_gate_up: int,
                 W2: int, y: int, stream: int) -> int:
     return load().moe_forward(plan, int(T), x, router_logits, W_router, W1_gate_up, W2, y, stream)
+
+
+def moe_forward_host(plan: int, T: int, x_host: int, router_logits: int, W_router: Optional[int],
+                     W1_gate_up: int, W2: int, y_host: int, stream: int) -> int:
+    return load().moe_forward_host(plan, int(T), x_host, router_logits, W_router, W1_gate_up, W2, y_host,
+                                   stream)
 
 
 def moe_get_status(plan: int, stream: int) -> int:
@@ -251,6 +259,17 @@ class MoELayer:
         if check:
             self.check()
         return y, logits
+
+    def forward_host(self, x_host, W_router, W1, W2, logits, y_host, check: bool = False):
+        """x_host / y_host: CPU bf16 tensors (page-locked for asynchronous copies)."""
+        T = x_host.shape[0]
+        st = moe_forward_host(self.plan, T, _ptr(x_host), _ptr(logits), _ptr(W_router), _ptr(W1), _ptr(W2),
+                              _ptr(y_host), self._stream())
+        if st != MOE_OK:
+            raise MoEError(st, "moe_forward_host")
+        if check:
+            self.check()
+        return y_host, logits
 
     def check(self):
         st = moe_get_status(self.plan, self._stream())

@@ -22,6 +22,8 @@ struct moe_plan_s {
   int64_t R_max, max_mt, max_tiles;
   void* base;
   size_t bytes;
+  void* x_stage;
+  void* y_stage;
   float* bias;
   Workspace ws;
   cudaEvent_t ev[MOE_NUM_STAGES + 1];
@@ -74,13 +76,15 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   return MOE_OK;
 }
 
+constexpr int N_BUFS = 16;
+
 struct Layout {
-  size_t off[14];
+  size_t off[N_BUFS];
   size_t total;
 };
 
 Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_tiles) {
-  const size_t sizes[14] = {
+  const size_t sizes[N_BUFS] = {
       (size_t)R * 4,                       // ids
       (size_t)R * 4,                       // w
       (size_t)c.E * 4,                     // counts
@@ -95,10 +99,12 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
       16,                                  // sched
       (size_t)max_mt * 4,                  // ready
       16,                                  // err
+      (size_t)c.T_max * c.H * 2,           // x staging (moe_forward_host)
+      (size_t)c.T_max * c.H * 2,           // y staging (moe_forward_host)
   };
   Layout L;
   size_t o = 0;
-  for (int i = 0; i < 14; ++i) {
+  for (int i = 0; i < N_BUFS; ++i) {
     L.off[i] = o;
     o += (sizes[i] + 255) & ~(size_t)255;
   }
@@ -183,6 +189,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->ws.sched = reinterpret_cast<int32_t*>(b + L.off[11]);
   p->ws.ready = reinterpret_cast<int32_t*>(b + L.off[12]);
   p->ws.err = reinterpret_cast<uint32_t*>(b + L.off[13]);
+  p->x_stage = b + L.off[14];
+  p->y_stage = b + L.off[15];
   if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cfg->router_bias) {
     if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
@@ -193,7 +201,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
     if (cudaMemcpy(p->bias, cfg->router_bias, sizeof(float) * cfg->E, cudaMemcpyHostToDevice) != cudaSuccess)
       return fail(MOE_ERR_CUDA);
   }
-  if (gemm_prepare(device) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (gemm_prepare(device) != cudaSuccess || router_prepare() != cudaSuccess) return fail(MOE_ERR_CUDA);
   p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
   if (p->timing)
     for (int i = 0; i <= MOE_NUM_STAGES; ++i)
@@ -288,6 +296,23 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   rec(5);
 #undef MOE_CK
   p->last_launches = nl;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float* router_logits,
+                              const void* W_router, const void* W1, const void* W2, void* y_host, void* stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > p->cfg.T_max || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if (T == 0) {
+    p->last_launches = 0;
+    return MOE_OK;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)T * p->cfg.H * 2;
+  if (cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status_t s = moe_forward(p, T, p->x_stage, router_logits, W_router, W1, W2, p->y_stage, stream);
+  if (s != MOE_OK) return s;
+  if (cudaMemcpyAsync(y_host, p->y_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -11,9 +11,10 @@
 // roles coupled through finite accumulator staging - follows the fused-kernel
 // description there, rebuilt here for tcgen05/TMEM on sm_103a.)
 //
-// Roles (192 threads):  warp 0 = TMA producer, warp 1 = TMEM owner + MMA
-// issuer (one thread), warps 2..5 = epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31, i.e. tile rows).  Tiles come from a ticket list built by
+// Roles (320 threads):  warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer (one thread), warps 2..9 = epilogue: warp w reads TMEM lanes
+// 32*(w%4) .. +31 (tile rows) and one half of the tile's columns, so two
+// epilogue warps share every SM sub-partition.  Tiles come from a ticket list built by
 // the dispatch kernel; CTA b takes tickets b, b+grid, ... in order.  A
 // Linear-2 tile first waits until the ready counter of its m-tile shows all
 // Linear-1 tiles of those rows stored; tickets are in a topological order and
@@ -36,7 +37,9 @@ namespace moe {
 
 namespace {
 
-constexpr int GEMM_THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int GEMM_THREADS = 64 + EPI_THREADS;
 constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int GEMM_SMEM = SMEM_BAR_OFF + 256 + 1024;   // + barriers/flags + alignment slack
@@ -64,6 +67,9 @@ __device__ __forceinline__ void tile_range(const GemmArgs& a, int& begin, int& e
   end = (a.range_sel == 0) ? n1 : tot;
 }
 
+// SwiGLU element silu(g) * u = g / (1 + exp(-g)) * u (fast exp and divide: the
+// tensor-core accumulation of g and u, not these last-place errors, decides
+// how often the bf16 rounding of the result differs from a host evaluation).
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
@@ -89,7 +95,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->tfull[b], 1);
-      ptx::mbar_init(&ctl->tempty[b], 4 * 32);
+      ptx::mbar_init(&ctl->tempty[b], EPI_THREADS);
     }
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort_flag = 0;
@@ -232,7 +238,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;               // TMEM lane quadrant
     const int r = q * 32 + lane;          // tile row
-    const int ep_tid = threadIdx.x - 64;  // 0..127
+    const int ep_tid = threadIdx.x - 64;  // 0..255
+    const int ch = (warp - 2) >> 2;       // column half of this warp
     int local = 0;
     const bool bilinear = (args.flags & MOE_FLAG_ACT_BILINEAR) != 0;
     for (int i = t_begin + blockIdx.x; i < t_end; i += gridDim.x, ++local) {
@@ -240,13 +247,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, m = tl.z, g = tl.w;
       const int as = local & 1;
       const uint32_t aphase = (local >> 1) & 1;
-      // one thread waits, the named barrier broadcasts its decision to all 128
+      // one thread waits, the named barrier broadcasts its decision to all epilogue threads
       if (ep_tid == 0) {
         const bool okw = ptx::mbar_wait(&ctl->tfull[as], aphase, tmo, abort_flag);
         if (!okw) set_abort(ctl, args.err, ERR_TIMEOUT);
         *(volatile int*)&ctl->ep_ok[local & 1] = okw ? 1 : 0;
       }
-      ptx::named_bar_sync(1, 128);
+      ptx::named_bar_sync(1, EPI_THREADS);
       if (!*(volatile int*)&ctl->ep_ok[local & 1]) break;
       ptx::tc_fence_after();
       const int rows_valid = args.counts[e] - m * BM;
@@ -260,7 +267,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       if (ph == 0) {
         uint16_t* hrow = args.h + (size_t)grow * args.I + nb * L1_COLS;
 #pragma unroll 1
-        for (int c = 0; c < L1_COLS / 32; ++c) {
+        for (int c = ch * 2; c < ch * 2 + 2; ++c) {
           uint32_t gv[32], uv[32];
           ptx::tmem_ld32(taddr + c * 32, gv);
           ptx::tmem_ld32(taddr + L1_COLS + c * 32, uv);
@@ -285,7 +292,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         const int pair = valid ? args.row_pair[grow] : 0;
         float* prow = args.P + (size_t)pair * args.H + nb * L2_COLS;
 #pragma unroll 1
-        for (int c = 0; c < L2_COLS / 32; ++c) {
+        for (int c = ch * 4; c < ch * 4 + 4; ++c) {
           uint32_t v[32];
           ptx::tmem_ld32(taddr + c * 32, v);
           ptx::tmem_ld_wait();
@@ -303,7 +310,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       if (ph == 0) {
         // publish: these rows' h columns are stored (visible to TMA readers)
         ptx::fence_proxy_async_global();
-        ptx::named_bar_sync(1, 128);
+        ptx::named_bar_sync(1, EPI_THREADS);
         if (ep_tid == 0) {
           __threadfence();
           ptx::red_release_add_gpu(args.ready + g, 1);

@@ -42,6 +42,7 @@ struct GemmArgs {
   int64_t timeout_ns;
 };
 
+cudaError_t router_prepare();
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
                                  int H, int E, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,

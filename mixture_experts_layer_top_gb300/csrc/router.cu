@@ -17,20 +17,25 @@ namespace moe {
 
 namespace {
 
-constexpr int RT_TOK = 32;    // tokens per CTA
-constexpr int RT_EXP = 32;    // experts per CTA
-constexpr int RT_HC = 128;    // h per staged chunk (4 x 32)
-constexpr int RT_ROW = 40;    // bf16 elements per smem row (32 + 8 pad = 80 bytes, conflict-free 16 B reads)
+constexpr int RT_TOK = 32;      // tokens per CTA
+constexpr int RT_EXP = 32;      // experts per CTA
+constexpr int RT_HC = 128;      // h per pipeline stage (4 x 32)
+constexpr int RT_NS = 4;        // pipeline stages
+constexpr int RT_XROW = RT_HC + 8;   // bf16 per staged x row (272 B; 16-B multiple, conflict-free reads)
+constexpr int RT_WROW = RT_EXP + 8;  // bf16 per staged Wr row (80 B; conflict-free 16-B reads)
+constexpr int RT_STAGE_X = RT_TOK * RT_XROW;   // elements
+constexpr int RT_STAGE_W = RT_HC * RT_WROW;
+constexpr int RT_SMEM = RT_NS * (RT_STAGE_X + RT_STAGE_W) * 2;
 constexpr int RT_THREADS = 512;
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(u[i] << 16);
-    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-  }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const int n = valid ? 16 : 0;   // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // One reduce-scatter step of the butterfly: lanes pair with lane ^ 2^S, each
 // keeps half of its 2^(S+2) values and adds its partner's copy of that half.
@@ -51,96 +56,99 @@ __device__ __forceinline__ void rs_step(float (&acc)[64], int lane) {
 
 // grid (ceil(T/32), ceil(E/32)), 512 threads = 16 warps; warp (tg, eg) owns
 // tokens t0 + 8*tg .. +8 and experts e0 + 8*eg .. +8.  Lane L holds the
-// partial sums of residue class h = L (mod 32) for all 64 of those outputs.
+// partial sums of residue class h = L (mod 32) for all 64 of those outputs,
+// each accumulated with one rounded fused multiply-add per h in ascending h
+// (two outputs per packed f32x2 FMA).  x and Wr chunks of 128 h stream through
+// a 4-stage cp.async ring in shared memory.
 __global__ void __launch_bounds__(RT_THREADS, 1)
 router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wr,
                      const float* __restrict__ bias, float* __restrict__ logits, int T, int H, int E) {
-  __shared__ __align__(16) uint16_t xs[2][RT_HC][RT_ROW];   // x transposed: [h][token]
-  __shared__ __align__(16) uint16_t ws[2][RT_HC][RT_ROW];   // Wr: [h][expert]
+  extern __shared__ __align__(16) uint16_t rsm[];
+  uint16_t* xs = rsm;                               // [NS][32 tok][XROW]
+  uint16_t* ws = rsm + RT_NS * RT_STAGE_X;          // [NS][HC][WROW]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * RT_TOK, e0 = blockIdx.y * RT_EXP;
   const int tg = warp >> 2, eg = warp & 3;
 
-  // staging roles: x: token = tid & 31, 8-element h chunk = tid >> 5 (16 chunks of 8 = 128)
-  //                Wr: row = tid >> 2 (128 rows), 8-expert part = tid & 3
-  const int xs_tok = tid & 31, xs_c = tid >> 5;
-  const int ws_row = tid >> 2, ws_part = tid & 3;
-  const bool x_ok = (t0 + xs_tok) < T;
-  const int we = e0 + ws_part * 8;
-  const bool w_full = (we + 8) <= E;
-  const bool e_vec = (E % 8) == 0;
+  // copy roles: x: token tid>>4, 8-element chunk tid&15;  Wr: row tid>>2, 8-expert part tid&3
+  const int cx_tok = tid >> 4, cx_c = tid & 15;
+  const int cw_row = tid >> 2, cw_part = tid & 3;
+  const bool x_ok = (t0 + cx_tok) < T;
+  const int we = e0 + cw_part * 8;
+  const bool w_vec = (E % 8) == 0;
+  const uint16_t* xsrc = x + (size_t)(x_ok ? t0 + cx_tok : 0) * H + cx_c * 8;
 
-  auto load_x = [&](int h0) -> uint4 {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (x_ok) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + xs_tok) * H + h0 + xs_c * 8);
-    return v;
-  };
-  auto load_w = [&](int h0) -> uint4 {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    const uint16_t* src = Wr + (size_t)(h0 + ws_row) * E + we;
-    if (w_full && e_vec) {
-      v = *reinterpret_cast<const uint4*>(src);
+  auto issue = [&](int chunk) {
+    const int st = chunk % RT_NS;
+    const int h0 = chunk * RT_HC;
+    cp_async16(xs + st * RT_STAGE_X + cx_tok * RT_XROW + cx_c * 8, xsrc + h0, x_ok);
+    uint16_t* wdst = ws + st * RT_STAGE_W + cw_row * RT_WROW + cw_part * 8;
+    const uint16_t* wsrc = Wr + (size_t)(h0 + cw_row) * E + we;
+    if (w_vec) {
+      cp_async16(wdst, (we < E) ? wsrc : Wr, we < E);
     } else {
-      uint16_t tmp[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) tmp[i] = (we + i < E) ? src[i] : (uint16_t)0;
-      v.x = tmp[0] | ((uint32_t)tmp[1] << 16);
-      v.y = tmp[2] | ((uint32_t)tmp[3] << 16);
-      v.z = tmp[4] | ((uint32_t)tmp[5] << 16);
-      v.w = tmp[6] | ((uint32_t)tmp[7] << 16);
+      for (int i = 0; i < 8; ++i) wdst[i] = (we + i < E) ? wsrc[i] : (uint16_t)0;
     }
-    return v;
-  };
-  auto store_stage = [&](int buf, const uint4& xv, const uint4& wv) {
-    const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      xs[buf][xs_c * 8 + 2 * i][xs_tok] = (uint16_t)(u[i] & 0xFFFFu);
-      xs[buf][xs_c * 8 + 2 * i + 1][xs_tok] = (uint16_t)(u[i] >> 16);
-    }
-    *reinterpret_cast<uint4*>(&ws[buf][ws_row][ws_part * 8]) = wv;
   };
 
-  float acc[64];
+  float2 acc[32];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+  for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
   const int nchunk = H / RT_HC;   // H is a multiple of 256
-  uint4 xv = load_x(0), wv = load_w(0);
-  store_stage(0, xv, wv);
-  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < RT_NS - 1; ++c) {
+    if (c < nchunk) issue(c);
+    cp_async_commit();
+  }
   for (int c = 0; c < nchunk; ++c) {
-    const int buf = c & 1;
-    if (c + 1 < nchunk) {
-      xv = load_x((c + 1) * RT_HC);
-      wv = load_w((c + 1) * RT_HC);
-    }
+    if (c + RT_NS - 1 < nchunk) issue(c + RT_NS - 1);
+    cp_async_commit();
+    cp_async_wait<RT_NS - 1>();
+    __syncthreads();
+    const uint16_t* xb = xs + (c % RT_NS) * RT_STAGE_X + (tg * 8) * RT_XROW;
+    const uint16_t* wb = ws + (c % RT_NS) * RT_STAGE_W + eg * 8;
 #pragma unroll
     for (int i = 0; i < RT_HC / 32; ++i) {
-      const int hr = i * 32 + lane;   // global h = c*128 + 32*i + lane  ==  lane (mod 32)
-      float xf[8], wf[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(&xs[buf][hr][tg * 8]), xf);
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(&ws[buf][hr][eg * 8]), wf);
+      const int hr = i * 32 + lane;   // global h = c*128 + 32*i + lane == lane (mod 32)
+      const uint4 wv = *reinterpret_cast<const uint4*>(wb + hr * RT_WROW);
+      const float2 w01 = make_float2(__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xFFFF0000u));
+      const float2 w23 = make_float2(__uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xFFFF0000u));
+      const float2 w45 = make_float2(__uint_as_float(wv.z << 16), __uint_as_float(wv.z & 0xFFFF0000u));
+      const float2 w67 = make_float2(__uint_as_float(wv.w << 16), __uint_as_float(wv.w & 0xFFFF0000u));
 #pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a * 8 + b] = __fmaf_rn(xf[a], wf[b], acc[a * 8 + b]);
+      for (int a = 0; a < 8; ++a) {
+        const float xf = __uint_as_float((uint32_t)xb[a * RT_XROW + hr] << 16);
+        const float2 xx = make_float2(xf, xf);
+        acc[a * 4 + 0] = __ffma2_rn(xx, w01, acc[a * 4 + 0]);
+        acc[a * 4 + 1] = __ffma2_rn(xx, w23, acc[a * 4 + 1]);
+        acc[a * 4 + 2] = __ffma2_rn(xx, w45, acc[a * 4 + 2]);
+        acc[a * 4 + 3] = __ffma2_rn(xx, w67, acc[a * 4 + 3]);
+      }
     }
-    if (c + 1 < nchunk) store_stage(buf ^ 1, xv, wv);
     __syncthreads();
   }
+  cp_async_wait<0>();
 
-  // Reduce-scatter butterfly (see rs_step); lane L ends with outputs 2L, 2L+1.
-  rs_step<4>(acc, lane);
-  rs_step<3>(acc, lane);
-  rs_step<2>(acc, lane);
-  rs_step<1>(acc, lane);
-  rs_step<0>(acc, lane);
+  float f[64];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    f[2 * i] = acc[i].x;
+    f[2 * i + 1] = acc[i].y;
+  }
+  // Reduce-scatter butterfly (see rs_step); lane L ends with outputs 2L, 2L+1
+  // (output o = 8 * token + expert within the warp's 8 x 8 tile).
+  rs_step<4>(f, lane);
+  rs_step<3>(f, lane);
+  rs_step<2>(f, lane);
+  rs_step<1>(f, lane);
+  rs_step<0>(f, lane);
   const int o = 2 * lane;
   const int t = t0 + tg * 8 + (o >> 3);
   const int e = e0 + eg * 8 + (o & 7);
   if (t < T) {
-    float v0 = acc[0], v1 = acc[1];
+    const float v0 = f[0], v1 = f[1];
     if (e < E) logits[(size_t)t * E + e] = bias ? v0 + bias[e] : v0;
     if (e + 1 < E) logits[(size_t)t * E + e + 1] = bias ? v1 + bias[e + 1] : v1;
   }
@@ -204,10 +212,14 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __re
 
 }  // namespace
 
+cudaError_t router_prepare() {
+  return cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
                                  int H, int E, cudaStream_t st) {
   dim3 grid((T + RT_TOK - 1) / RT_TOK, (E + RT_EXP - 1) / RT_EXP);
-  router_logits_kernel<<<grid, RT_THREADS, 0, st>>>(x, Wr, bias, logits, T, H, E);
+  router_logits_kernel<<<grid, RT_THREADS, RT_SMEM, st>>>(x, Wr, bias, logits, T, H, E);
   return cudaGetLastError();
 }
 
