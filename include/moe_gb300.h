@@ -157,6 +157,29 @@ MOE_API moe_status_t moe_plan_destroy(moe_plan_t plan);
 /* Static description of a status code. */
 MOE_API const char* moe_status_string(moe_status_t s);
 
+/* Dispatch (the stable counting sort of moe_forward's Dispatch step) for callers that cannot
+ * allocate device memory.  The paper has no counterpart: it exists for code that may not call
+ * cudaMalloc, e.g. while a stream is being captured into a CUDA graph, under an allocator that
+ * owns all device memory or a fixed memory budget, or on paths that must not risk the implicit
+ * synchronisation of cudaMalloc/cudaFree.  It allocates nothing: its scratch (one row counter
+ * per expert) is a fixed array of 256 counters inside the library, present on every device
+ * that loads it until the process exits.
+ *   ids      int32 [T,k]  expert of each (token, slot); entries outside [0,E) are not placed
+ *   w        fp32  [T,k]  router weights, or NULL (then row_w must be NULL)
+ *   offsets  int32 [E+1]  OUTPUT: rows of expert e are offsets[e] .. offsets[e+1]-1
+ *   row_pair int32 [T*k]  OUTPUT: row -> t*k+j, ascending t within an expert
+ *   row_of   int32 [T*k]  OUTPUT: t*k+j -> row
+ *   row_w    fp32  [T*k]  OUTPUT: w of each row, or NULL
+ * Device pointers, enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * Limits: E <= 256 and T*k < 2^30, else MOE_ERR_UNSUPPORTED.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) and should happen before any stream
+ * capture; later calls only enqueue a memset of the counters and two kernels.  All calls share
+ * the one array: calls whose work overlaps on the GPU (different streams without ordering) race
+ * and give wrong rows; calls ordered on one stream are safe, each clears the counters first. */
+MOE_API moe_status_t moe_dispatch_static(int32_t T, int32_t E, int32_t k, const int32_t* ids, const float* w,
+                                 int32_t* offsets, int32_t* row_pair, int32_t* row_of, float* row_w,
+                                 void* stream);
+
 /* Host-side evaluation of the tile schedule the device builds (for tests; no GPU needed).
  * counts[E] rows per expert; writes up to cap tiles as 4 ints each
  * {phase | n_block << 1, expert, m_block, global m-tile index} into tiles_out and the

@@ -43,7 +43,7 @@ STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")
 EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_get_status",
             "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
-            "moe_status_string", "moe_schedule_host")
+            "moe_status_string", "moe_schedule_host", "moe_dispatch_static")
 
 
 class MoEError(RuntimeError):
@@ -92,6 +92,7 @@ def load() -> ctypes.CDLL:
     L.moe_status_string.argtypes = [ctypes.c_int]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_schedule_host.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, i64, P(i64)]
+    L.moe_dispatch_static.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
     for f in EXPORTED:
         if f != "moe_status_string":
             getattr(L, f).restype = ctypes.c_int
@@ -161,6 +162,12 @@ def moe_last_launch_count(plan: int) -> int:
 
 def moe_plan_destroy(plan: int) -> int:
     return load().moe_plan_destroy(plan)
+
+
+def moe_dispatch_static(T: int, E: int, k: int, ids, w, offsets, row_pair, row_of, row_w, stream: int) -> int:
+    """Dispatch sort that allocates nothing (scratch in a fixed array inside the library);
+    for callers that cannot call cudaMalloc.  Device pointers; see include/moe_gb300.h."""
+    return load().moe_dispatch_static(int(T), int(E), int(k), ids, w, offsets, row_pair, row_of, row_w, stream)
 
 
 def moe_schedule_host(counts, H: int, I: int, num_sms: int, schedule: int, wave_experts: int = 0,
