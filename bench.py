@@ -164,8 +164,10 @@ def calibrate_tokens(wl, budget_s: float):
     dt, _, threads, n, _ = oracle_sample(wl, max(2, min(os.cpu_count() or 1, 16)))
     per_tok = dt / n
     n_target = int(budget_s / max(per_tok, 1e-9))
-    cap = max(2, int(24e9 / (wl.k * 6.0 * wl.H * wl.I)))   # keep the sample's weights under ~24 GB
-    return max(2, min(n_target, wl.T, cap))
+    expert_bytes = 6.0 * wl.H * wl.I                        # W1[e] + W2[e], bf16
+    if wl.E * expert_bytes > 24e9:                          # keep the sample's host weights under ~24 GB
+        n_target = min(n_target, max(2, int(24e9 / (wl.k * expert_bytes))))
+    return max(2, min(n_target, wl.T))
 
 
 def cpu_baseline(wl, budget_s: float):
@@ -371,7 +373,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="fine")
-    ap.add_argument("--schedule", type=int, choices=(0, 1, 2), default=0)
+    ap.add_argument("--schedule", type=int, choices=(0, 1, 2), default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
