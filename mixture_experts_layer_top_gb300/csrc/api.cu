@@ -71,7 +71,8 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   if (c->H % L2_COLS != 0 || c->I % L1_COLS != 0) return MOE_ERR_UNSUPPORTED;
   if (c->E > MAX_E || c->top_k > MAX_K || c->top_k > c->E) return MOE_ERR_UNSUPPORTED;
   const int64_t R = (int64_t)c->T_max * c->top_k;
-  if (R >= (1ll << 30) || (int64_t)c->E * c->H >= (1ll << 31) || (int64_t)c->E * c->I >= (1ll << 31))
+  if (R >= (1ll << 30) || (int64_t)c->E * c->H >= (1ll << 31) || (int64_t)c->E * c->I >= (1ll << 31) ||
+      (int64_t)c->T_max * c->H >= (1ll << 32))
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
