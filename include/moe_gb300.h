@@ -74,6 +74,7 @@ typedef enum {
 #define MOE_FLAG_ACT_BILINEAR (1u << 0) /* activation g*u instead of silu(g)*u (GLU "bilinear"
                                            variant, same paper as SwiGLU); used by exactness tests */
 #define MOE_FLAG_STAGE_TIMING (1u << 1) /* record CUDA events between stages (moe_stage_times)    */
+#define MOE_FLAG_TRACE (1u << 2)        /* grouped GEMM records per-CTA wait times (moe_trace_read) */
 #define MOE_FLAG_TEST_STALL (1u << 8)   /* test only: Linear-2 tiles wait for a readiness count that
                                            is never reached, so the bounded wait expires and
                                            moe_get_status reports MOE_ERR_TIMEOUT (no GPU fault)   */
@@ -148,6 +149,13 @@ MOE_API moe_status_t moe_debug_intermediates(moe_plan_t plan, int32_t T, void* h
  * Synchronises on the recorded events.  ms[3] is the grouped-GEMM launch(es). */
 MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
 
+/* Wait-time trace of the last forward's grouped GEMM (needs MOE_FLAG_TRACE; synchronises the
+ * device).  Writes n = CTAs x 8 uint64 values to host_buf (cap = capacity in values); per CTA:
+ * {producer waiting for a free stage, producer waiting for Linear-1 readiness, MMA issuer waiting
+ * for a free accumulator, MMA issuer waiting for operands, epilogue waiting for an accumulator,
+ * CTA lifetime} in nanoseconds, then {Linear-1 tiles, Linear-2 tiles}. */
+MOE_API moe_status_t moe_trace_read(moe_plan_t plan, uint64_t* host_buf, size_t cap, size_t* n);
+
 /* Number of kernels the last moe_forward launched. */
 MOE_API moe_status_t moe_last_launch_count(moe_plan_t plan, int32_t* n);
 
@@ -181,9 +189,10 @@ MOE_API moe_status_t moe_dispatch_static(int32_t T, int32_t E, int32_t k, const 
                                  void* stream);
 
 /* Host-side evaluation of the tile schedule the device builds (for tests; no GPU needed).
- * counts[E] rows per expert; writes up to cap tiles as 4 ints each
- * {phase | n_block << 1, expert, m_block, global m-tile index} into tiles_out and the
- * tile counts {linear-1 tiles, total tiles} into n_out[2]. */
+ * counts[E] rows per expert; num_sms = number of tile workers (2-CTA clusters on the GPU);
+ * a unit is a pair of 128-row m-tiles of one expert.  Writes up to cap tiles as 4 ints each
+ * {phase | n_block << 1, expert, unit within the expert, global unit index} into tiles_out and
+ * the tile counts {linear-1 tiles, total tiles} into n_out[2]. */
 MOE_API moe_status_t moe_schedule_host(const int32_t* counts, int32_t E, int32_t H, int32_t I,
                                int32_t num_sms, int32_t schedule, int32_t wave_experts,
                                int32_t lead_waves, int32_t* tiles_out, int64_t cap, int64_t* n_out);

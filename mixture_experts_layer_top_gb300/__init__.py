@@ -35,6 +35,9 @@ MOE_SCHED_PHASED = 2
 
 MOE_FLAG_ACT_BILINEAR = 1 << 0
 MOE_FLAG_STAGE_TIMING = 1 << 1
+MOE_FLAG_TRACE = 1 << 2
+TRACE_FIELDS = ("prod_wait_empty_ns", "prod_wait_ready_ns", "mma_wait_tempty_ns", "mma_wait_full_ns",
+                "epi_wait_tfull_ns", "cta_ns", "tiles_l1", "tiles_l2")
 MOE_FLAG_TEST_STALL = 1 << 8
 
 MOE_NUM_STAGES = 5
@@ -43,7 +46,7 @@ STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")
 EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_get_status",
             "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
-            "moe_status_string", "moe_schedule_host", "moe_dispatch_static")
+            "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read")
 
 
 class MoEError(RuntimeError):
@@ -93,6 +96,7 @@ def load() -> ctypes.CDLL:
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_schedule_host.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, i64, P(i64)]
     L.moe_dispatch_static.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_trace_read.argtypes = [vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)]
     for f in EXPORTED:
         if f != "moe_status_string":
             getattr(L, f).restype = ctypes.c_int
@@ -158,6 +162,21 @@ def moe_last_launch_count(plan: int) -> int:
     if st != MOE_OK:
         raise MoEError(st, "moe_last_launch_count")
     return n.value
+
+
+def moe_trace_read(plan: int) -> np.ndarray:
+    """Per-CTA wait-time counters of the last forward's grouped GEMM: [CTAs, 8] uint64
+    (fields in TRACE_FIELDS).  Needs MOE_FLAG_TRACE."""
+    n = ctypes.c_size_t(0)
+    L = load()
+    st = L.moe_trace_read(plan, None, 0, ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_trace_read")
+    out = np.zeros(n.value, dtype=np.uint64)
+    st = L.moe_trace_read(plan, out.ctypes.data, n.value, ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_trace_read")
+    return out.reshape(-1, len(TRACE_FIELDS))
 
 
 def moe_plan_destroy(plan: int) -> int:

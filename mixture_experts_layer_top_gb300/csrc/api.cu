@@ -19,6 +19,7 @@ struct moe_plan_s {
   moe_config_t cfg;
   int device;
   int num_sms;
+  int gemm_grid;   // CTAs of the grouped GEMM (all 2-CTA clusters co-resident)
   int64_t R_max, max_mt, max_tiles;
   void* base;
   size_t bytes;
@@ -29,6 +30,7 @@ struct moe_plan_s {
   cudaEvent_t ev[MOE_NUM_STAGES + 1];
   bool timing;
   int last_launches;
+  unsigned long long* trace;   // [gemm_grid][TRACE_SLOTS] when MOE_FLAG_TRACE
 };
 
 namespace {
@@ -164,6 +166,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   Layout L = layout_of(*cfg, p->R_max, p->max_mt, p->max_tiles);
   p->bytes = L.total;
   auto fail = [&](moe_status_t s) {
+    if (p->trace) cudaFree(p->trace);
     if (p->base) cudaFree(p->base);
     if (p->bias) cudaFree(p->bias);
     delete p;
@@ -202,7 +205,15 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
     if (cudaMemcpy(p->bias, cfg->router_bias, sizeof(float) * cfg->E, cudaMemcpyHostToDevice) != cudaSuccess)
       return fail(MOE_ERR_CUDA);
   }
-  if (gemm_prepare(device) != cudaSuccess || router_prepare() != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
+  if (cfg->flags & MOE_FLAG_TRACE) {
+    if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid) != cudaSuccess) {
+      cudaGetLastError();
+      p->trace = nullptr;
+      return fail(MOE_ERR_OOM);
+    }
+  }
   p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
   if (p->timing)
     for (int i = 0; i <= MOE_NUM_STAGES; ++i)
@@ -250,7 +261,8 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, st));
   ++nl;
   rec(1);
-  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->num_sms, c.schedule, c.wave_experts, c.lead_waves, st));
+  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, c.schedule, c.wave_experts, c.lead_waves,
+                         st));
   ++nl;
   rec(2);
   MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.row_pair, R, H, k, p->ws.x_perm, st));
@@ -273,6 +285,9 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.P = p->ws.P;
   ga.ready = p->ws.ready;
   ga.err = p->ws.err;
+  ga.trace = p->trace;
+  if (p->trace)
+    MOE_CK(cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid, st));
   ga.H = H;
   ga.I = I;
   ga.E = E;
@@ -282,13 +297,13 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.timeout_ns = c.timeout_ns;
   if (c.schedule == MOE_SCHED_PHASED) {
     ga.range_sel = 0;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->num_sms, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->gemm_grid, st));
     ga.range_sel = 1;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->num_sms, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->gemm_grid, st));
     nl += 2;
   } else {
     ga.range_sel = 2;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->num_sms, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->gemm_grid, st));
     ++nl;
   }
   rec(4);
@@ -365,6 +380,18 @@ moe_status_t moe_stage_times(moe_plan_t p, float* ms) {
   return MOE_OK;
 }
 
+moe_status_t moe_trace_read(moe_plan_t p, uint64_t* host_buf, size_t cap, size_t* n) {
+  if (!p || !n || !p->trace) return MOE_ERR_INVALID_ARG;
+  const size_t cnt = (size_t)TRACE_SLOTS * p->gemm_grid;
+  *n = cnt;
+  if (!host_buf) return MOE_OK;
+  if (cap < cnt) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(host_buf, p->trace, cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status_t moe_last_launch_count(moe_plan_t p, int32_t* n) {
   if (!p || !n) return MOE_ERR_INVALID_ARG;
   *n = p->last_launches;
@@ -381,6 +408,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
     for (int i = 0; i <= MOE_NUM_STAGES; ++i) cudaEventDestroy(p->ev[i]);
   if (p->base) cudaFree(p->base);
   if (p->bias) cudaFree(p->bias);
+  if (p->trace) cudaFree(p->trace);
   cudaSetDevice(cur);
   delete p;
   return MOE_OK;

@@ -21,6 +21,8 @@ constexpr int MMA_N = 256;       // tcgen05 N of both GEMMs
 constexpr int L1_COLS = 128;     // intermediate columns per Linear-1 tile (gate 128 | up 128)
 constexpr int L2_COLS = 256;     // output columns per Linear-2 tile
 constexpr int STAGES = 4;        // smem ring depth
+constexpr int PAIR = 2;          // m-tiles per cluster tile: a 2-CTA cluster shares each B tile
+constexpr int UNIT_ROWS = BM * PAIR;
 constexpr int MAX_E = 256;
 constexpr int MAX_K = 8;
 
@@ -34,10 +36,12 @@ constexpr uint32_t ERR_TIMEOUT = 1u;
 constexpr uint32_t ERR_CHECK = 2u;
 
 // ------------------------------------------------------------------ schedule
+// Scheduling unit: a pair of consecutive m-tiles of one expert (UNIT_ROWS rows),
+// processed by the two CTAs of a cluster (CTA rank r takes m-tile 2*unit + r).
 struct SchedTables {
   int E, nL1, nL2, W, mode, lead;
-  int total_mt, n1_total, total;
-  int mt[MAX_E];           // m-tiles of expert e
+  int total_mt, n1_total, total;   // total_mt: number of units
+  int mt[MAX_E];           // units of expert e
   int mtb[MAX_E + 1];      // prefix of mt
   int wave_of[MAX_E];      // wave of expert e
   int w_first_mt[MAX_E + 1];
@@ -62,8 +66,10 @@ MOE_HD int merge_pos_b(int j, int a, int b) {
   return j + (int)(cnt < a ? cnt : a);
 }
 
-// Serial part: m-tiles, waves, segment starts.  counts[E] rows per expert.
-MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int nL2, int num_sms, int mode,
+// Serial part: units, waves, segment starts.  counts[E] rows per expert; workers =
+// number of concurrent tile workers (2-CTA clusters); a wave is the smallest run of
+// experts whose Linear-1 tiles reach it.
+MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int nL2, int workers, int mode,
                         int wave_experts, int lead) {
   s.E = E;
   s.nL1 = nL1;
@@ -71,7 +77,7 @@ MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int n
   s.mode = mode;
   int tot = 0;
   for (int e = 0; e < E; ++e) {
-    int m = (counts[e] + BM - 1) / BM;
+    int m = (counts[e] + UNIT_ROWS - 1) / UNIT_ROWS;
     s.mt[e] = m;
     s.mtb[e] = tot;
     tot += m;
@@ -90,7 +96,7 @@ MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int n
     for (int e = 0; e < E; ++e) {
       s.wave_of[e] = w;
       acc += s.mt[e] * nL1;
-      if (acc >= num_sms && e + 1 < E) {
+      if (acc >= workers && e + 1 < E) {
         ++w;
         acc = 0;
       }
@@ -143,7 +149,7 @@ MOE_HD int sched_ticket_l2(const SchedTables& s, int w, int i) {
   return s.seg_b[w] + merge_pos_a(i, sched_n_mt(s, w) * s.nL2, b);
 }
 
-// Expert owning global m-tile g (mtb[e] <= g < mtb[e+1]).
+// Expert owning global unit g (mtb[e] <= g < mtb[e+1]).
 MOE_HD int sched_expert_of(const SchedTables& s, int g) {
   int lo = 0, hi = s.E - 1;
   while (lo < hi) {
@@ -153,8 +159,8 @@ MOE_HD int sched_expert_of(const SchedTables& s, int g) {
   return lo;
 }
 
-// Write every tile reached from global m-tile g.  Tile = {phase | n << 1, e, m, g}.
-// Within a wave the tiles are ordered (expert, n-block, m-block) with m fastest.
+// Write every tile reached from global unit g.  Tile = {phase | n << 1, e, unit, g}.
+// Within a wave the tiles are ordered (expert, n-block, unit) with the unit fastest.
 MOE_HD void sched_emit_mtile(const SchedTables& s, int g, int* tiles /* 4 ints per ticket */) {
   int e = sched_expert_of(s, g);
   int m = g - s.mtb[e];
@@ -176,7 +182,7 @@ MOE_HD void sched_emit_mtile(const SchedTables& s, int g, int* tiles /* 4 ints p
   }
 }
 
-// Upper bound of m-tiles for R routed rows over E experts.
-MOE_HD long long max_mtiles(long long R, int E) { return (R + BM - 1) / BM + E; }
+// Upper bound of units for R routed rows over E experts.
+MOE_HD long long max_mtiles(long long R, int E) { return (R + UNIT_ROWS - 1) / UNIT_ROWS + E; }
 
 }  // namespace moe

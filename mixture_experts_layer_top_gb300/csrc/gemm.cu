@@ -11,14 +11,22 @@
 // roles coupled through finite accumulator staging - follows the fused-kernel
 // description there, rebuilt here for tcgen05/TMEM on sm_103a.)
 //
+// Clusters of 2 CTAs: a tile is a pair of consecutive m-tiles of one expert with
+// one n-block; CTA rank r computes m-tile 2*unit + r.  The B tile (weights) is
+// shared: each CTA TMA-loads one half and multicasts it into both CTAs' shared
+// memory, halving the L2->SM traffic for B; each CTA's MMA completion is
+// multicast to both CTAs' "stage empty" barriers, so a stage is refilled only
+// when both have consumed it.
+//
 // Roles (320 threads):  warp 0 = TMA producer, warp 1 = TMEM owner + MMA
 // issuer (one thread), warps 2..9 = epilogue: warp w reads TMEM lanes
 // 32*(w%4) .. +31 (tile rows) and one half of the tile's columns, so two
 // epilogue warps share every SM sub-partition.  Tiles come from a ticket list built by
-// the dispatch kernel; CTA b takes tickets b, b+grid, ... in order.  A
-// Linear-2 tile first waits until the ready counter of its m-tile shows all
-// Linear-1 tiles of those rows stored; tickets are in a topological order and
-// every CTA is resident (grid <= SMs, 1 CTA/SM), so the waits always finish.
+// the dispatch kernel; cluster c takes tickets c, c+clusters, ... in order.  A
+// Linear-2 tile first waits until the ready counter of its unit shows all
+// Linear-1 tiles of those rows stored by both CTAs; tickets are in a topological
+// order and every cluster is resident (the grid is at most the number of
+// co-resident clusters, 1 CTA/SM), so the waits always finish.
 // Every wait is bounded by timeout_ns; on expiry the CTA records
 // ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
 //
@@ -90,8 +98,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&ctl->full[s], 1);
-      ptx::mbar_init(&ctl->empty[s], 1);
+      ptx::mbar_init(&ctl->full[s], 1);        // own producer's expect_tx (+ bytes from both CTAs)
+      ptx::mbar_init(&ctl->empty[s], PAIR);    // one MMA-completion arrival from each CTA
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->tfull[b], 1);
@@ -111,8 +119,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();     // both CTAs' barriers exist before any multicast lands
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  const bool tracing = (args.flags & MOE_FLAG_TRACE) != 0;
+  const uint64_t t_start = ptx::globaltimer();
+  uint64_t tr_a = 0, tr_b = 0;     // this thread's two wait-time counters (role specific)
+  uint64_t* trp_a = tracing ? &tr_a : nullptr;
+  uint64_t* trp_b = tracing ? &tr_b : nullptr;
+  const int rank = (int)ptx::cluster_ctarank();
+  const int cluster = blockIdx.x / PAIR, nclusters = gridDim.x / PAIR;
+  constexpr uint16_t CTA_MASK = (1u << PAIR) - 1;
   volatile int* abort_flag = &ctl->abort_flag;
 
   int t_begin, t_end;
@@ -127,14 +144,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_par = 0;   // per stage: issued at least once / parity of last issue
-      for (int i = t_begin + blockIdx.x; i < t_end && !*abort_flag; i += gridDim.x) {
+      for (int i = t_begin + cluster; i < t_end && !*abort_flag; i += nclusters) {
         const int4 tl = args.tiles[i];
-        const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, m = tl.z, g = tl.w;
-        const int row0 = args.offsets[e] + m * BM;
+        const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, g = tl.w;
+        const int m = PAIR * tl.z + rank;      // this CTA's m-tile of the unit
+        const int row0 = args.offsets[e] + m * BM;   // past the expert: rows unused (or zero-filled)
         if (ph == 1) {
-          // wait for every Linear-1 tile of this m-tile (bounded)
+          // wait for every Linear-1 tile of this unit, from both CTAs (bounded)
           const int* rp = args.ready + g;
-          const int need = args.nL1 + ((args.flags & MOE_FLAG_TEST_STALL) ? 1 : 0);
+          const int need = PAIR * args.nL1 + ((args.flags & MOE_FLAG_TEST_STALL) ? 1 : 0);
           if (ptx::ld_acquire_gpu(rp) < need) {
             const uint64_t t0 = ptx::globaltimer();
             bool ok = false;
@@ -144,6 +162,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
               if ((int64_t)(ptx::globaltimer() - t0) > tmo) break;
               __nanosleep(64);
             }
+            tr_b += ptx::globaltimer() - t0;
             if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
           }
           ptx::fence_proxy_async_global();
@@ -154,24 +173,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         const int brow0 = e * (ph == 0 ? args.H : args.I);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, tmo, abort_flag)) { ok = false; break; }
+          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, tmo, abort_flag, trp_a)) { ok = false; break; }
           uint8_t* sA = smem + stage * STAGE_BYTES;
           uint8_t* sB = sA + A_STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
           ptx::tma_load_2d(tA, &ctl->full[stage], sA, kb * BK, row0, pol_a);
-          if (ph == 0) {
-            const int c0 = nb * L1_COLS;
-            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 0 * B_BOX_BYTES, c0, brow0 + kb * BK, pol_w);
-            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 1 * B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
-            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 2 * B_BOX_BYTES, args.I + c0, brow0 + kb * BK, pol_w);
-            ptx::tma_load_2d(tB, &ctl->full[stage], sB + 3 * B_BOX_BYTES, args.I + c0 + 64, brow0 + kb * BK,
-                             pol_w);
-          } else {
-            const int c0 = nb * L2_COLS;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              ptx::tma_load_2d(tB, &ctl->full[stage], sB + q * B_BOX_BYTES, c0 + 64 * q, brow0 + kb * BK, pol_w);
-          }
+          // this CTA's half of B (two 64-column boxes), multicast to both CTAs:
+          // Linear-1: rank 0 the gate columns, rank 1 the up columns of the n-block;
+          // Linear-2: rank r the columns [128 r, 128 r + 128) of the 256-column block
+          const int c0 = (ph == 0) ? (rank == 0 ? nb * L1_COLS : args.I + nb * L1_COLS)
+                                   : nb * L2_COLS + rank * 128;
+          uint8_t* sBh = sB + rank * 2 * B_BOX_BYTES;
+          ptx::tma_load_2d_mc(tB, &ctl->full[stage], sBh, c0, brow0 + kb * BK, CTA_MASK, pol_w);
+          ptx::tma_load_2d_mc(tB, &ctl->full[stage], sBh + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, CTA_MASK, pol_w);
           issued_mask |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -195,12 +209,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       uint32_t phase = 0;
       int local = 0;
       bool issued_any = false;
-      for (int i = t_begin + blockIdx.x; i < t_end && !*abort_flag; i += gridDim.x, ++local) {
+      for (int i = t_begin + cluster; i < t_end && !*abort_flag; i += nclusters, ++local) {
         const int4 tl = args.tiles[i];
         const int ph = tl.x & 1;
         const int as = local & 1;
         const uint32_t aphase = (local >> 1) & 1;
-        if (!ptx::mbar_wait(&ctl->tempty[as], aphase ^ 1u, tmo, abort_flag)) {
+        if (!ptx::mbar_wait(&ctl->tempty[as], aphase ^ 1u, tmo, abort_flag, trp_a)) {
           set_abort(ctl, args.err, ERR_TIMEOUT);
           break;
         }
@@ -209,7 +223,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         const int nk = (ph == 0 ? args.H : args.I) / BK;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, tmo, abort_flag)) { ok = false; break; }
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, tmo, abort_flag, trp_b)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b0 = a0 + A_STAGE_BYTES;
@@ -220,7 +234,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
             ptx::mma_bf16(d, ad, bd, IDESC, (kb | kk) != 0);
           }
           issued_any = true;
-          ptx::mma_commit(&ctl->empty[stage]);
+          ptx::mma_commit_mc(&ctl->empty[stage], CTA_MASK);   // frees the stage in both CTAs
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
@@ -242,14 +256,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     const int ch = (warp - 2) >> 2;       // column half of this warp
     int local = 0;
     const bool bilinear = (args.flags & MOE_FLAG_ACT_BILINEAR) != 0;
-    for (int i = t_begin + blockIdx.x; i < t_end; i += gridDim.x, ++local) {
+    for (int i = t_begin + cluster; i < t_end; i += nclusters, ++local) {
       const int4 tl = args.tiles[i];
-      const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, m = tl.z, g = tl.w;
+      const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, g = tl.w;
+      const int m = PAIR * tl.z + rank;
       const int as = local & 1;
       const uint32_t aphase = (local >> 1) & 1;
       // one thread waits, the named barrier broadcasts its decision to all epilogue threads
       if (ep_tid == 0) {
-        const bool okw = ptx::mbar_wait(&ctl->tfull[as], aphase, tmo, abort_flag);
+        const bool okw = ptx::mbar_wait(&ctl->tfull[as], aphase, tmo, abort_flag, trp_a);
         if (!okw) set_abort(ctl, args.err, ERR_TIMEOUT);
         *(volatile int*)&ctl->ep_ok[local & 1] = okw ? 1 : 0;
       }
@@ -319,25 +334,72 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     }
   }
 
+  if (tracing) {
+    unsigned long long* tr = args.trace + (size_t)blockIdx.x * TRACE_SLOTS;
+    if (threadIdx.x == 0) {
+      atomicAdd(tr + TR_PROD_WAIT_EMPTY, (unsigned long long)tr_a);
+      atomicAdd(tr + TR_PROD_WAIT_READY, (unsigned long long)tr_b);
+    } else if (threadIdx.x == 32) {
+      atomicAdd(tr + TR_MMA_WAIT_TEMPTY, (unsigned long long)tr_a);
+      atomicAdd(tr + TR_MMA_WAIT_FULL, (unsigned long long)tr_b);
+    } else if (threadIdx.x == 64) {
+      atomicAdd(tr + TR_EPI_WAIT_TFULL, (unsigned long long)tr_a);
+      int n1 = 0, n2 = 0;
+      for (int i = t_begin + cluster; i < t_end; i += nclusters) (args.tiles[i].x & 1) ? ++n2 : ++n1;
+      atomicAdd(tr + TR_TILES_L1, (unsigned long long)n1);
+      atomicAdd(tr + TR_TILES_L2, (unsigned long long)n2);
+      atomicAdd(tr + TR_KERNEL_NS, (unsigned long long)(ptx::globaltimer() - t_start));
+    }
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc<TMEM_COLS>(tmem_base);
   }
+  ptx::cluster_sync();     // no CTA leaves while its peer may still signal its barriers
 }
 
 }  // namespace
 
-cudaError_t gemm_prepare(int device) {
-  (void)device;
-  return cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+static cudaLaunchConfig_t gemm_config(int grid, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GEMM_SMEM;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+cudaError_t gemm_prepare(int device, int* grid) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return e;
+  // every cluster of the grid must be resident at once (Linear-2 tiles wait for earlier tickets)
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = gemm_config(sms / PAIR * PAIR, nullptr, attr);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters > sms / PAIR) clusters = sms / PAIR;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  *grid = clusters * PAIR;
+  return cudaSuccess;
 }
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const GemmArgs& a, int grid, cudaStream_t st) {
-  grouped_gemm_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, st>>>(tA1, tB1, tA2, tB2, a);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = gemm_config(grid, st, attr);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel, tA1, tB1, tA2, tB2, a);
 }
 
 }  // namespace moe

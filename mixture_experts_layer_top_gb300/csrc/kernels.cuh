@@ -23,6 +23,20 @@ struct Workspace {
   int32_t* sched;     // [4]: linear-1 tiles, total tiles, m-tiles
   int32_t* ready;     // [max_mt]
   uint32_t* err;      // [1]
+  unsigned long long* trace;   // [gemm grid][TRACE_SLOTS] wait-time counters (MOE_FLAG_TRACE)
+};
+
+// Per-CTA counters of the grouped GEMM under MOE_FLAG_TRACE (nanoseconds unless noted).
+enum TraceSlot {
+  TR_PROD_WAIT_EMPTY = 0,  // producer blocked on a free stage
+  TR_PROD_WAIT_READY = 1,  // producer blocked on Linear-1 readiness of a Linear-2 tile
+  TR_MMA_WAIT_TEMPTY = 2,  // MMA issuer blocked on a free TMEM accumulator (epilogue behind)
+  TR_MMA_WAIT_FULL = 3,    // MMA issuer blocked on operands (loads behind)
+  TR_EPI_WAIT_TFULL = 4,   // epilogue blocked on an accumulator (MMA behind)
+  TR_KERNEL_NS = 5,        // CTA lifetime
+  TR_TILES_L1 = 6,         // Linear-1 tiles (count)
+  TR_TILES_L2 = 7,         // Linear-2 tiles (count)
+  TRACE_SLOTS = 8
 };
 
 struct GemmArgs {
@@ -36,6 +50,7 @@ struct GemmArgs {
   float* P;
   int32_t* ready;
   uint32_t* err;
+  unsigned long long* trace;
   int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all
   int H, I, E, R, nL1;
   uint32_t flags;
@@ -51,7 +66,7 @@ cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int
                             int wave_experts, int lead, cudaStream_t st);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, int R, int H, int k, uint16_t* x_perm,
                           cudaStream_t st);
-cudaError_t gemm_prepare(int device);
+cudaError_t gemm_prepare(int device, int* grid);   // grid: CTAs of the co-resident 2-CTA clusters
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const GemmArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_combine(const float* P, int T, int H, int k, uint16_t* y, int num_sms, cudaStream_t st);

@@ -53,18 +53,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for phase `parity` of `bar` to complete; false once `timeout_ns` of
 // %globaltimer have passed or *abort_flag becomes non-zero.
+// If `waited_ns` is given, the time spent in a wait that did not succeed at once is
+// added to it.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int64_t timeout_ns,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint64_t* waited_ns = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t spins = 0;
+  bool ok = true;
   while (!mbar_try_wait(bar, parity)) {
     if ((++spins & 63u) == 0) {
-      if (*abort_flag) return false;
-      if ((int64_t)(globaltimer() - t0) > timeout_ns) return false;
+      if (*abort_flag || (int64_t)(globaltimer() - t0) > timeout_ns) {
+        ok = false;
+        break;
+      }
     }
   }
-  return true;
+  if (waited_ns) *waited_ns += globaltimer() - t0;
+  return ok;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -80,6 +86,17 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* m, uint64_t* bar,
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// The same load delivered to the same shared-memory offset of every CTA in
+// `cta_mask` of the cluster, completing bytes on each CTA's barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap* m, uint64_t* bar, void* dst, int32_t c0, int32_t c1,
+                                               uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
       : "memory");
 }
 
@@ -141,6 +158,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Arrive once on the barrier at `bar`'s offset in every CTA of `cta_mask` when every
+// tcgen05 op issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
 // (quadrant*32 + i), columns [col, col+32).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -181,6 +208,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
          | ((b_mn_major ? 1u : 0u) << 16) // B major
          | ((N >> 3) << 17)               // N / 8
          | ((M >> 4) << 24);              // M / 16
+}
+
+// ------------------------------------------------------------------ cluster
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA in the cluster must execute this.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ misc

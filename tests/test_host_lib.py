@@ -70,7 +70,7 @@ def test_plan_without_device_fails_cleanly(lib):
 def _check_schedule(counts, H, I, sms, mode, wave_experts=0, lead=1):
     tiles, n1 = moe.moe_schedule_host(counts, H, I, sms, mode, wave_experts, lead)
     nL1, nL2 = I // 128, H // 256
-    mt = (np.asarray(counts) + 127) // 128
+    mt = (np.asarray(counts) + 255) // 256          # units: pairs of 128-row m-tiles (one 2-CTA cluster)
     mtb = np.concatenate([[0], np.cumsum(mt)])
     total_mt = int(mtb[-1])
     assert len(tiles) == total_mt * (nL1 + nL2)
@@ -123,8 +123,8 @@ def test_schedule_phased_is_l1_then_l2(lib):
 
 
 def test_schedule_wave_serial_vs_interleaved(lib):
-    counts = np.full(32, 256)        # 2 m-tiles per expert, nL1 = 2 -> 4 L1 tiles per expert
-    sms = 16                         # waves of 4 experts
+    counts = np.full(32, 512)        # 2 units per expert, nL1 = 2 -> 4 L1 tiles per expert
+    sms = 16                         # 16 workers: waves of 4 experts
     t0, _ = _check_schedule(counts, 512, 256, sms, 0)
     t1, _ = _check_schedule(counts, 512, 256, sms, 1, 0, 1)
     ph0, ph1 = t0[:, 0] & 1, t1[:, 0] & 1
@@ -139,7 +139,7 @@ def test_schedule_wave_serial_vs_interleaved(lib):
 
 def test_merge_positions_proportional(lib):
     # unequal lists: a = 3 L2 tiles vs b = 9 L1 tiles per wave
-    counts = np.full(8, 128 * 3)     # 3 m-tiles/expert
+    counts = np.full(8, 256 * 3)     # 3 units/expert
     tiles, _ = _check_schedule(counts, 256, 384, 9, 1, 1, 1)   # 1 expert per wave, nL1=3, nL2=1
     ph = (tiles[:, 0] & 1).tolist()
     seg = ph[9:9 + 12]               # merged segment: 3 L2 + 9 L1
