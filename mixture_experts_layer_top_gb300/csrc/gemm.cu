@@ -1,8 +1,8 @@
 // Persistent grouped GEMM for both expert projections of the MoE layer.
 //
-// Linear-1 tile (phase 0): rows [offsets[e] + 128 m, +128) of x_perm times
-//   W1[e][:, 128 n .. +128] (gate) and W1[e][:, I + 128 n .. +128] (up), one
-//   M=128 x N=256 tcgen05 accumulator; epilogue h = bf16(silu(g) * u).
+// Linear-1 tile (phase 0): 256 dispatch rows of one expert (two 128-row m-tiles)
+//   of x_perm times W1[e][:, 128 n .. +128] (gate) and W1[e][:, I + 128 n .. +128]
+//   (up): one M=256 x N=256 tcgen05 accumulator; epilogue h = bf16(silu(g) * u).
 // Linear-2 tile (phase 1): the same rows of h times W2[e][:, 256 n .. +256];
 //   epilogue P[t*k + j] = w[t,j] * acc (fp32), the router-weight scale.
 // (X-Stage paper, MegaMoE background: Linear-1 projects hidden to
@@ -11,29 +11,32 @@
 // roles coupled through finite accumulator staging - follows the fused-kernel
 // description there, rebuilt here for tcgen05/TMEM on sm_103a.)
 //
-// Clusters of 2 CTAs: a tile is a pair of consecutive m-tiles of one expert with
-// one n-block; CTA rank r computes m-tile 2*unit + r.  The B tile (weights) is
-// shared: each CTA TMA-loads one half and multicasts it into both CTAs' shared
-// memory, halving the L2->SM traffic for B; each CTA's MMA completion is
-// multicast to both CTAs' "stage empty" barriers, so a stage is refilled only
-// when both have consumed it.
+// Pairs of SMs: each tile runs on a 2-CTA cluster with the pair form of the MMA
+// (cta_group::2, M = 256).  CTA rank r owns m-tile 2*unit + r: it loads those
+// 128 rows of A and one half of B (Linear-1: r = 0 the gate columns, r = 1 the up
+// columns; Linear-2: columns [128 r, 128 r + 128)) into its own shared memory,
+// and its TMEM receives its 128 rows x 256 columns of the accumulator.  Per CTA a
+// pipeline stage is 32 KB (16 KB A + 16 KB half of B), so six stages fit; both
+// CTAs' loads complete on the even CTA's "stage full" barrier, whose single
+// thread issues the MMAs for the pair and multicasts completion to both CTAs'
+// "stage empty" and "accumulator full" barriers.  Each CTA's epilogue signals
+// the even CTA's "accumulator empty" barrier.
 //
-// Roles (320 threads):  warp 0 = TMA producer, warp 1 = TMEM owner + MMA
-// issuer (one thread), warps 2..9 = epilogue: warp w reads TMEM lanes
-// 32*(w%4) .. +31 (tile rows) and one half of the tile's columns, so two
-// epilogue warps share every SM sub-partition.  Tiles come from a ticket list built by
-// the dispatch kernel; cluster c takes tickets c, c+clusters, ... in order.  A
-// Linear-2 tile first waits until the ready counter of its unit shows all
-// Linear-1 tiles of those rows stored by both CTAs; tickets are in a topological
-// order and every cluster is resident (the grid is at most the number of
-// co-resident clusters, 1 CTA/SM), so the waits always finish.
-// Every wait is bounded by timeout_ns; on expiry the CTA records
-// ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+// Roles (320 threads):  warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer
+// (one thread, even CTA only), warps 2..9 = epilogue: warp w reads TMEM lanes
+// 32*(w%4) .. +31 (tile rows) and one half of the tile's columns.  Tiles come
+// from a ticket list built by the dispatch kernel; cluster c takes tickets c,
+// c+clusters, ... in order.  A Linear-2 tile first waits until the ready counter
+// of its unit shows all Linear-1 tiles of those rows stored by both CTAs;
+// tickets are in a topological order and every cluster is resident (the grid is
+// at most the number of co-resident clusters, 1 CTA/SM), so the waits finish.
+// Every wait is bounded by timeout_ns; on expiry the CTA records ERR_TIMEOUT,
+// waits (bounded) for its in-flight copies and MMAs, frees TMEM and exits.
 //
 // Shared-memory operand layouts (128-byte swizzle, as written by TMA):
 //   A (K-major): 128 rows x 128 B per stage; descriptor SBO = 1024 B (8-row
 //     group), K step of 16 elements = +32 B on the start address.
-//   B (N-major): four 64-column boxes of 64 K-rows x 128 B (8 KB each);
+//   B half (N-major): two 64-column boxes of 64 K-rows x 128 B (8 KB each);
 //     descriptor LBO = 8 KB (next 64 columns), SBO = 1024 B (next 8 K-rows),
 //     K step of 16 rows = +2048 B.
 #include <cuda_bf16.h>
@@ -48,21 +51,28 @@ namespace {
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int GEMM_THREADS = 64 + EPI_THREADS;
-constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
-constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int GEMM_SMEM = SMEM_BAR_OFF + 256 + 1024;   // + barriers/flags + alignment slack
-constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MMA_N, true);
+constexpr int TMEM_COLS = 512;                         // two 256-column fp32 accumulators
+constexpr int NSTAGE = 6;                              // per-CTA ring depth
+constexpr int BH_BYTES = 2 * B_BOX_BYTES;              // this CTA's half of B: 16 KB
+constexpr int PSTAGE_BYTES = A_STAGE_BYTES + BH_BYTES; // 32 KB
+constexpr int PAIR_TX_BYTES = PAIR * PSTAGE_BYTES;     // bytes completing on the even CTA's barrier
+constexpr int SMEM_BAR_OFF = NSTAGE * PSTAGE_BYTES;
+constexpr int CTL_BYTES = 512;
+constexpr int GEMM_SMEM = SMEM_BAR_OFF + CTL_BYTES + 1024;   // + slack to align the base to 1024 B
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR * BM, MMA_N, true);
 
 struct SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[NSTAGE];    // even CTA: both CTAs' loads of the stage landed
+  uint64_t empty[NSTAGE];   // both CTAs: the pair MMAs of the stage completed
+  uint64_t tfull[2];        // both CTAs: accumulator ready
+  uint64_t tempty[2];       // even CTA: both CTAs' epilogues drained the accumulator
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int ep_ok[2];   // epilogue go/stop decision of the waiting thread, by tile parity
+  int ep_ok[2];             // epilogue go/stop decision of the waiting thread, by tile parity
 };
+static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block exceeds its shared-memory reservation");
+static_assert(GEMM_SMEM <= 232448, "shared memory per CTA exceeded");
 
 __device__ __forceinline__ void set_abort(SmemCtl* ctl, uint32_t* err, uint32_t code) {
   atomicOr(err, code);
@@ -95,15 +105,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  constexpr uint16_t CTA_MASK = (1u << PAIR) - 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&ctl->full[s], 1);        // own producer's expect_tx (+ bytes from both CTAs)
-      ptx::mbar_init(&ctl->empty[s], PAIR);    // one MMA-completion arrival from each CTA
+    for (int s = 0; s < NSTAGE; ++s) {
+      ptx::mbar_init(&ctl->full[s], 1);        // even CTA's producer (expect_tx for both CTAs' bytes)
+      ptx::mbar_init(&ctl->empty[s], 1);       // the pair MMA commit
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&ctl->tfull[b], 1);
-      ptx::mbar_init(&ctl->tempty[b], EPI_THREADS);
+      ptx::mbar_init(&ctl->tfull[b], 1);       // the pair MMA commit
+      ptx::mbar_init(&ctl->tempty[b], PAIR);   // one arrival per CTA's epilogue
     }
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort_flag = 0;
@@ -114,41 +127,39 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     ptx::tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
-    ptx::tmem_alloc<TMEM_COLS>(&ctl->tmem_base);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair<TMEM_COLS>(&ctl->tmem_base);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();     // both CTAs' barriers exist before any multicast lands
+  ptx::cluster_sync();     // both CTAs' barriers exist before any load or arrival crosses
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort_flag;
   const bool tracing = (args.flags & MOE_FLAG_TRACE) != 0;
   const uint64_t t_start = ptx::globaltimer();
   uint64_t tr_a = 0, tr_b = 0;     // this thread's two wait-time counters (role specific)
   uint64_t* trp_a = tracing ? &tr_a : nullptr;
   uint64_t* trp_b = tracing ? &tr_b : nullptr;
-  const int rank = (int)ptx::cluster_ctarank();
   const int cluster = blockIdx.x / PAIR, nclusters = gridDim.x / PAIR;
-  constexpr uint16_t CTA_MASK = (1u << PAIR) - 1;
-  volatile int* abort_flag = &ctl->abort_flag;
 
   int t_begin, t_end;
   tile_range(args, t_begin, t_end);
   const int64_t tmo = args.timeout_ns;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_normal();
       const uint64_t pol_a = ptx::policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_mask = 0, last_par = 0;   // per stage: issued at least once / parity of last issue
+      uint32_t filled_mask = 0, last_par = 0;   // per stage: filled at least once / parity of last fill
       for (int i = t_begin + cluster; i < t_end && !*abort_flag; i += nclusters) {
         const int4 tl = args.tiles[i];
         const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, g = tl.w;
-        const int m = PAIR * tl.z + rank;      // this CTA's m-tile of the unit
-        const int row0 = args.offsets[e] + m * BM;   // past the expert: rows unused (or zero-filled)
+        const int m = PAIR * tl.z + rank;              // this CTA's m-tile of the unit
+        const int row0 = args.offsets[e] + m * BM;      // past the expert: rows unused (or zero-filled)
         if (ph == 1) {
           // wait for every Linear-1 tile of this unit, from both CTAs (bounded)
           const int* rp = args.ready + g;
@@ -171,40 +182,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         const CUtensorMap* tA = ph == 0 ? &tmA1 : &tmA2;
         const CUtensorMap* tB = ph == 0 ? &tmB1 : &tmB2;
         const int brow0 = e * (ph == 0 ? args.H : args.I);
+        // this CTA's half of B: Linear-1 rank 0 gate / rank 1 up columns of the n-block,
+        // Linear-2 columns [128 r, 128 r + 128) of the 256-column block
+        const int c0 = (ph == 0) ? (rank == 0 ? nb * L1_COLS : args.I + nb * L1_COLS) : nb * L2_COLS + rank * 128;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, tmo, abort_flag, trp_a)) { ok = false; break; }
-          uint8_t* sA = smem + stage * STAGE_BYTES;
+          uint8_t* sA = smem + stage * PSTAGE_BYTES;
           uint8_t* sB = sA + A_STAGE_BYTES;
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
-          ptx::tma_load_2d(tA, &ctl->full[stage], sA, kb * BK, row0, pol_a);
-          // this CTA's half of B (two 64-column boxes), multicast to both CTAs:
-          // Linear-1: rank 0 the gate columns, rank 1 the up columns of the n-block;
-          // Linear-2: rank r the columns [128 r, 128 r + 128) of the 256-column block
-          const int c0 = (ph == 0) ? (rank == 0 ? nb * L1_COLS : args.I + nb * L1_COLS)
-                                   : nb * L2_COLS + rank * 128;
-          uint8_t* sBh = sB + rank * 2 * B_BOX_BYTES;
-          ptx::tma_load_2d_mc(tB, &ctl->full[stage], sBh, c0, brow0 + kb * BK, CTA_MASK, pol_w);
-          ptx::tma_load_2d_mc(tB, &ctl->full[stage], sBh + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, CTA_MASK, pol_w);
-          issued_mask |= 1u << stage;
+          const uint32_t full_pair = ptx::mapa_shared(&ctl->full[stage], 0);
+          if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], PAIR_TX_BYTES);
+          ptx::tma_load_2d_pair(tA, full_pair, sA, kb * BK, row0, pol_a);
+          ptx::tma_load_2d_pair(tB, full_pair, sB, c0, brow0 + kb * BK, pol_w);
+          ptx::tma_load_2d_pair(tB, full_pair, sB + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
+          filled_mask |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
         }
         if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
       }
-      if (*abort_flag) {
-        // let every issued copy land before the CTA can exit
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s)) {
-            int dummy = 0;
-            ptx::mbar_wait(&ctl->full[s], (last_par >> s) & 1u, tmo, &dummy);
-          }
-      }
+      // Before the CTA may exit: every fill of every stage has been released by the pair
+      // MMA (its commit arrives here) - which also means every copy into this CTA landed.
+      int dummy = 0;
+      for (int s = 0; s < NSTAGE; ++s)
+        if (filled_mask & (1u << s)) ptx::mbar_wait(&ctl->empty[s], (last_par >> s) & 1u, tmo, &dummy);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -225,35 +231,37 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(&ctl->full[stage], phase, tmo, abort_flag, trp_b)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t a0 = ptx::smem_u32(smem + stage * PSTAGE_BYTES);
           const uint32_t b0 = a0 + A_STAGE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = ptx::smem_desc_sw128(b0 + kk * 2048, B_BOX_BYTES, 1024);
-            ptx::mma_bf16(d, ad, bd, IDESC, (kb | kk) != 0);
+            ptx::mma_bf16_pair(d, ad, bd, IDESC, (kb | kk) != 0);
           }
           issued_any = true;
-          ptx::mma_commit_mc(&ctl->empty[stage], CTA_MASK);   // frees the stage in both CTAs
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          ptx::mma_commit_pair_mc(&ctl->empty[stage], CTA_MASK);   // frees the stage in both CTAs
+          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
         }
         if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
-        ptx::mma_commit(&ctl->tfull[as]);
+        ptx::mma_commit_pair_mc(&ctl->tfull[as], CTA_MASK);
       }
       if (*abort_flag && issued_any) {
         // make sure no MMA still reads shared memory or writes TMEM
-        ptx::mma_commit(&ctl->drain);
+        ptx::mma_commit_pair_mc(&ctl->drain, 1);
         int dummy = 0;
         ptx::mbar_wait(&ctl->drain, 0, tmo, &dummy);
       }
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;               // TMEM lane quadrant
     const int r = q * 32 + lane;          // tile row
     const int ep_tid = threadIdx.x - 64;  // 0..255
     const int ch = (warp - 2) >> 2;       // column half of this warp
+    const uint32_t tempty_pair0 = ptx::mapa_shared(&ctl->tempty[0], 0);
+    const uint32_t tempty_pair1 = ptx::mapa_shared(&ctl->tempty[1], 0);
     int local = 0;
     const bool bilinear = (args.flags & MOE_FLAG_ACT_BILINEAR) != 0;
     for (int i = t_begin + cluster; i < t_end; i += nclusters, ++local) {
@@ -302,6 +310,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
             for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
         }
+        ptx::fence_proxy_async_global();   // h rows will be read by TMA (async proxy)
       } else {
         const float wgt = valid ? args.row_w[grow] : 0.0f;
         const int pair = valid ? args.row_pair[grow] : 0;
@@ -320,13 +329,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           }
         }
       }
+      // all epilogue threads are done with the accumulator (and, for Linear-1, stored h)
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&ctl->tempty[as]);
-      if (ph == 0) {
-        // publish: these rows' h columns are stored (visible to TMA readers)
-        ptx::fence_proxy_async_global();
-        ptx::named_bar_sync(1, EPI_THREADS);
-        if (ep_tid == 0) {
+      ptx::named_bar_sync(1, EPI_THREADS);
+      if (ep_tid == 0) {
+        ptx::mbar_arrive_cluster(as ? tempty_pair1 : tempty_pair0);
+        if (ph == 0) {
           __threadfence();
           ptx::red_release_add_gpu(args.ready + g, 1);
         }
@@ -353,11 +361,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();     // both CTAs finished every role: no arrival or load crosses any more
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc<TMEM_COLS>(tmem_base);
+    ptx::tmem_dealloc_pair<TMEM_COLS>(tmem_base);
   }
-  ptx::cluster_sync();     // no CTA leaves while its peer may still signal its barriers
 }
 
 }  // namespace
