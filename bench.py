@@ -33,6 +33,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 256 << 20
 
 
+def load_traffic(kernel: str, workload: str, schedule: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, only while the
+    kernel's sources are unchanged since the capture (else None)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        if rec["workload"] != workload or rec["schedule"] != schedule:
+            return None
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return float(rec["dram_bytes_per_launch"]) if h.hexdigest() == rec["source_sha256"] else None
+    except Exception:
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -328,7 +346,9 @@ def run_ours(args, wl):
         ach = g_bytes / (g_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
-    roof.update({"traffic": None, "kernel": "grouped_gemm_kernel", "ms_per_launch": g_ms,
+    traffic = load_traffic("grouped_gemm_kernel", wl.name, args.schedule)
+    roof.update({"traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read+write)",
+                 "kernel": "grouped_gemm_kernel", "ms_per_launch": g_ms,
                  "launches_per_step": 2 if args.schedule == 2 else 1,
                  "peak_source": f"{peak_src} ({'bf16_tflops burst' if tensor_bound else 'hbm_gbs'})",
                  "algorithmic": (f"{g_flops:.4g} FLOP (6*H*I per routed row x {R} rows)" if tensor_bound

@@ -19,9 +19,9 @@ namespace {
 
 constexpr int RT_TOK = 32;      // tokens per CTA
 constexpr int RT_EXP = 32;      // experts per CTA
-constexpr int RT_HC = 128;      // h per pipeline stage (4 x 32)
+constexpr int RT_HC = 256;      // h per pipeline stage (8 x 32); H is a multiple of 256
 constexpr int RT_NS = 4;        // pipeline stages
-constexpr int RT_XROW = RT_HC + 8;   // bf16 per staged x row (272 B; 16-B multiple, conflict-free reads)
+constexpr int RT_XROW = RT_HC + 8;   // bf16 per staged x row (528 B; 16-B multiple, conflict-free reads)
 constexpr int RT_WROW = RT_EXP + 8;  // bf16 per staged Wr row (80 B; conflict-free 16-B reads)
 constexpr int RT_STAGE_X = RT_TOK * RT_XROW;   // elements
 constexpr int RT_STAGE_W = RT_HC * RT_WROW;
@@ -58,7 +58,7 @@ __device__ __forceinline__ void rs_step(float (&acc)[64], int lane) {
 // tokens t0 + 8*tg .. +8 and experts e0 + 8*eg .. +8.  Lane L holds the
 // partial sums of residue class h = L (mod 32) for all 64 of those outputs,
 // each accumulated with one rounded fused multiply-add per h in ascending h
-// (two outputs per packed f32x2 FMA).  x and Wr chunks of 128 h stream through
+// (two outputs per packed f32x2 FMA).  x and Wr chunks of 256 h stream through
 // a 4-stage cp.async ring in shared memory.
 __global__ void __launch_bounds__(RT_THREADS, 1)
 router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wr,
@@ -70,25 +70,32 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
   const int t0 = blockIdx.x * RT_TOK, e0 = blockIdx.y * RT_EXP;
   const int tg = warp >> 2, eg = warp & 3;
 
-  // copy roles: x: token tid>>4, 8-element chunk tid&15;  Wr: row tid>>2, 8-expert part tid&3
-  const int cx_tok = tid >> 4, cx_c = tid & 15;
-  const int cw_row = tid >> 2, cw_part = tid & 3;
-  const bool x_ok = (t0 + cx_tok) < T;
-  const int we = e0 + cw_part * 8;
+  // copy roles, RT_HC / 128 rounds per stage: x chunk q = tid + 512 j is token q / XCH,
+  // 8-element chunk q % XCH; Wr chunk q is row q / 4, 8-expert part q % 4
+  constexpr int XCH = RT_HC / 8;
+  const int we_base = e0;
   const bool w_vec = (E % 8) == 0;
-  const uint16_t* xsrc = x + (size_t)(x_ok ? t0 + cx_tok : 0) * H + cx_c * 8;
 
   auto issue = [&](int chunk) {
     const int st = chunk % RT_NS;
     const int h0 = chunk * RT_HC;
-    cp_async16(xs + st * RT_STAGE_X + cx_tok * RT_XROW + cx_c * 8, xsrc + h0, x_ok);
-    uint16_t* wdst = ws + st * RT_STAGE_W + cw_row * RT_WROW + cw_part * 8;
-    const uint16_t* wsrc = Wr + (size_t)(h0 + cw_row) * E + we;
-    if (w_vec) {
-      cp_async16(wdst, (we < E) ? wsrc : Wr, we < E);
-    } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wdst[i] = (we + i < E) ? wsrc[i] : (uint16_t)0;
+    for (int j = 0; j < RT_HC / 128; ++j) {
+      const int q = tid + RT_THREADS * j;
+      const int tok = q / XCH, c = q % XCH;
+      const bool x_ok = (t0 + tok) < T;
+      cp_async16(xs + st * RT_STAGE_X + tok * RT_XROW + c * 8,
+                 x + (size_t)(x_ok ? t0 + tok : 0) * H + h0 + c * 8, x_ok);
+      const int row = q >> 2, part = q & 3;
+      const int we = we_base + part * 8;
+      uint16_t* wdst = ws + st * RT_STAGE_W + row * RT_WROW + part * 8;
+      const uint16_t* wsrc = Wr + (size_t)(h0 + row) * E + we;
+      if (w_vec) {
+        cp_async16(wdst, (we < E) ? wsrc : Wr, we < E);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wdst[i] = (we + i < E) ? wsrc[i] : (uint16_t)0;
+      }
     }
   };
 
@@ -111,7 +118,7 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
     const uint16_t* wb = ws + (c % RT_NS) * RT_STAGE_W + eg * 8;
 #pragma unroll
     for (int i = 0; i < RT_HC / 32; ++i) {
-      const int hr = i * 32 + lane;   // global h = c*128 + 32*i + lane == lane (mod 32)
+      const int hr = i * 32 + lane;   // global h = c*RT_HC + 32*i + lane == lane (mod 32)
       const uint4 wv = *reinterpret_cast<const uint4*>(wb + hr * RT_WROW);
       const float2 w01 = make_float2(__uint_as_float(wv.x << 16), __uint_as_float(wv.x & 0xFFFF0000u));
       const float2 w23 = make_float2(__uint_as_float(wv.y << 16), __uint_as_float(wv.y & 0xFFFF0000u));
