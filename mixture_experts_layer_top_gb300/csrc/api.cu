@@ -20,7 +20,7 @@ struct moe_plan_s {
   int device;
   int num_sms;
   int gemm_grid;   // CTAs of the grouped GEMM (all 2-CTA clusters co-resident)
-  int64_t R_max, max_mt, max_tiles;
+  int64_t R_max, max_mt, max_tiles, R_pad_max;
   void* base;
   size_t bytes;
   void* x_stage;
@@ -50,14 +50,17 @@ bool get_encode() {
   return g_encode != nullptr;
 }
 
-// 2-D bf16 tensor [outer, inner] (row pitch = inner*2 bytes), box {64, box_outer}, 128-byte swizzle,
-// out-of-bounds elements read as zero.
-bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+// 2-D tensor [outer, inner] (bf16, or fp32 when f32), row pitch = inner * element size; box of
+// 128 bytes x box_outer rows, 128-byte swizzle, out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer,
+               bool f32 = false) {
+  const uint32_t es_bytes = f32 ? 4 : 2;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_outer};
+  cuuint64_t strides[1] = {inner * es_bytes};
+  cuuint32_t box[2] = {128 / es_bytes, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -79,7 +82,7 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   return MOE_OK;
 }
 
-constexpr int N_BUFS = 16;
+constexpr int N_BUFS = 17;
 
 struct Layout {
   size_t off[N_BUFS];
@@ -87,6 +90,7 @@ struct Layout {
 };
 
 Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_tiles) {
+  const int64_t Rp = max_mt * UNIT_ROWS;   // padded rows
   const size_t sizes[N_BUFS] = {
       (size_t)R * 4,                       // ids
       (size_t)R * 4,                       // w
@@ -94,10 +98,11 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
       (size_t)(c.E + 1) * 4,               // offsets
       (size_t)R * 4,                       // row_pair
       (size_t)R * 4,                       // row_of
-      (size_t)R * 4,                       // row_w
-      (size_t)R * c.H * 2,                 // x_perm
-      (size_t)R * c.I * 2,                 // h
-      (size_t)R * c.H * 4,                 // P
+      (size_t)R * 4,                       // prow_of
+      (size_t)Rp * 4,                      // prow_w
+      (size_t)Rp * c.H * 2,                // x_pad
+      (size_t)Rp * c.I * 2,                // h_pad
+      (size_t)Rp * c.H * 4,                // P_pad
       (size_t)max_tiles * 16,              // tiles
       16,                                  // sched
       (size_t)max_mt * 4,                  // ready
@@ -163,6 +168,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->R_max = (int64_t)cfg->T_max * cfg->top_k;
   p->max_mt = max_mtiles(p->R_max, cfg->E);
   p->max_tiles = p->max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  p->R_pad_max = p->max_mt * UNIT_ROWS;
   Layout L = layout_of(*cfg, p->R_max, p->max_mt, p->max_tiles);
   p->bytes = L.total;
   auto fail = [&](moe_status_t s) {
@@ -185,16 +191,17 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->ws.offsets = reinterpret_cast<int32_t*>(b + L.off[3]);
   p->ws.row_pair = reinterpret_cast<int32_t*>(b + L.off[4]);
   p->ws.row_of = reinterpret_cast<int32_t*>(b + L.off[5]);
-  p->ws.row_w = reinterpret_cast<float*>(b + L.off[6]);
-  p->ws.x_perm = reinterpret_cast<uint16_t*>(b + L.off[7]);
-  p->ws.h = reinterpret_cast<uint16_t*>(b + L.off[8]);
-  p->ws.P = reinterpret_cast<float*>(b + L.off[9]);
-  p->ws.tiles = reinterpret_cast<int32_t*>(b + L.off[10]);
-  p->ws.sched = reinterpret_cast<int32_t*>(b + L.off[11]);
-  p->ws.ready = reinterpret_cast<int32_t*>(b + L.off[12]);
-  p->ws.err = reinterpret_cast<uint32_t*>(b + L.off[13]);
-  p->x_stage = b + L.off[14];
-  p->y_stage = b + L.off[15];
+  p->ws.prow_of = reinterpret_cast<int32_t*>(b + L.off[6]);
+  p->ws.prow_w = reinterpret_cast<float*>(b + L.off[7]);
+  p->ws.x_pad = reinterpret_cast<uint16_t*>(b + L.off[8]);
+  p->ws.h_pad = reinterpret_cast<uint16_t*>(b + L.off[9]);
+  p->ws.P_pad = reinterpret_cast<float*>(b + L.off[10]);
+  p->ws.tiles = reinterpret_cast<int32_t*>(b + L.off[11]);
+  p->ws.sched = reinterpret_cast<int32_t*>(b + L.off[12]);
+  p->ws.ready = reinterpret_cast<int32_t*>(b + L.off[13]);
+  p->ws.err = reinterpret_cast<uint32_t*>(b + L.off[14]);
+  p->x_stage = b + L.off[15];
+  p->y_stage = b + L.off[16];
   if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cfg->router_bias) {
     if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
@@ -265,12 +272,14 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
                          st));
   ++nl;
   rec(2);
-  MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.row_pair, R, H, k, p->ws.x_perm, st));
+  MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.row_pair, p->ws.prow_of, R, H, k, p->ws.x_pad, st));
   ++nl;
   rec(3);
-  CUtensorMap tA1, tB1, tA2, tB2;
-  if (!make_tmap(&tA1, p->ws.x_perm, H, R, BM) || !make_tmap(&tB1, W1, 2 * I, (uint64_t)E * H, BK) ||
-      !make_tmap(&tA2, p->ws.h, I, R, BM) || !make_tmap(&tB2, W2, H, (uint64_t)E * I, BK)) {
+  CUtensorMap tA1, tB1, tA2, tB2, tH, tP;
+  const uint64_t Rp = (uint64_t)p->R_pad_max;
+  if (!make_tmap(&tA1, p->ws.x_pad, H, Rp, BM) || !make_tmap(&tB1, W1, 2 * I, (uint64_t)E * H, BK) ||
+      !make_tmap(&tA2, p->ws.h_pad, I, Rp, BM) || !make_tmap(&tB2, W2, H, (uint64_t)E * I, BK) ||
+      !make_tmap(&tH, p->ws.h_pad, I, Rp, 32) || !make_tmap(&tP, p->ws.P_pad, H, Rp, 32, true)) {
     p->last_launches = nl;
     return MOE_ERR_CUDA;
   }
@@ -278,11 +287,9 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.tiles = reinterpret_cast<const int4*>(p->ws.tiles);
   ga.sched = p->ws.sched;
   ga.counts = p->ws.counts;
-  ga.offsets = p->ws.offsets;
-  ga.row_w = p->ws.row_w;
-  ga.row_pair = p->ws.row_pair;
-  ga.h = p->ws.h;
-  ga.P = p->ws.P;
+  ga.prow_w = p->ws.prow_w;
+  ga.h_pad = p->ws.h_pad;
+  ga.P_pad = p->ws.P_pad;
   ga.ready = p->ws.ready;
   ga.err = p->ws.err;
   ga.trace = p->trace;
@@ -291,23 +298,23 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.H = H;
   ga.I = I;
   ga.E = E;
-  ga.R = R;
+  ga.R_pad = (int)p->R_pad_max;
   ga.nL1 = I / L1_COLS;
   ga.flags = c.flags;
   ga.timeout_ns = c.timeout_ns;
   if (c.schedule == MOE_SCHED_PHASED) {
     ga.range_sel = 0;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->gemm_grid, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, st));
     ga.range_sel = 1;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->gemm_grid, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, st));
     nl += 2;
   } else {
     ga.range_sel = 2;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, ga, p->gemm_grid, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, st));
     ++nl;
   }
   rec(4);
-  MOE_CK(launch_combine(p->ws.P, T, H, k, static_cast<uint16_t*>(y), p->num_sms, st));
+  MOE_CK(launch_combine(p->ws.P_pad, p->ws.prow_of, T, H, k, static_cast<uint16_t*>(y), p->num_sms, st));
   ++nl;
   rec(5);
 #undef MOE_CK
@@ -364,9 +371,9 @@ moe_status_t moe_debug_intermediates(moe_plan_t p, int32_t T, void* h, float* P,
   if (!p || T < 0 || T > p->cfg.T_max) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t R = (size_t)T * p->cfg.top_k;
-  if (h && R && cudaMemcpyAsync(h, p->ws.h, R * p->cfg.I * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (P && R && cudaMemcpyAsync(P, p->ws.P, R * p->cfg.H * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+  if (R && (h || P) &&
+      launch_compact_intermediates(p->ws.row_pair, p->ws.prow_of, (int)R, p->cfg.H, p->cfg.I, p->ws.h_pad,
+                                   p->ws.P_pad, static_cast<uint16_t*>(h), P, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

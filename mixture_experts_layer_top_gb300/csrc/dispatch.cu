@@ -1,6 +1,6 @@
 // Dispatch on one GPU: a stable counting sort of the (token, slot) pairs into
 // expert-contiguous rows, the tile schedule of the grouped GEMMs, and the row
-// gather x_perm[row] = x[token(row)].
+// gather x_pad[padded row] = x[token(row)].
 //
 // In the X-Stage paper's MegaMoE background, Dispatch "first sends each token
 // to its destination" expert; with every expert on this GPU that becomes a
@@ -47,29 +47,41 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh_warp, int* to
   return res;
 }
 
-// CTAs 0..E-1: compaction of expert e's pairs in ascending pair order f = t*k+j.
+// CTAs 0..E-1: compaction of expert e's pairs in ascending pair order f = t*k+j
+// (compact rows, plus the padded row of each pair and the weight of that row).
 // CTA E: offsets, tile schedule, zeroed readiness counters.
 __global__ void __launch_bounds__(DS_THREADS)
 dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, const int32_t* __restrict__ counts,
                 int T, int E, int k, int nL1, int nL2, int num_sms, int mode, int wave_experts, int lead,
                 int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair, int32_t* __restrict__ row_of,
-                float* __restrict__ row_w, int32_t* __restrict__ tiles, int32_t* __restrict__ sched,
-                int32_t* __restrict__ ready) {
+                int32_t* __restrict__ prow_of, float* __restrict__ prow_w, int32_t* __restrict__ tiles,
+                int32_t* __restrict__ sched, int32_t* __restrict__ ready) {
   const int R = T * k;
   if ((int)blockIdx.x < E) {
     __shared__ int sh_warp[33];
-    __shared__ int s_base;
+    __shared__ int s_base, s_pbase;
     const int e = blockIdx.x;
     if (threadIdx.x < 32) {
-      int s = 0;
-      for (int i = threadIdx.x; i < e; i += 32) s += counts[i];
+      int s = 0, u = 0;
+      for (int i = threadIdx.x; i < e; i += 32) {
+        const int c = counts[i];
+        s += c;
+        u += (c + UNIT_ROWS - 1) / UNIT_ROWS;
+      }
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-      if (threadIdx.x == 0) s_base = s;
+      for (int off = 16; off >= 1; off >>= 1) {
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        u += __shfl_xor_sync(0xFFFFFFFFu, u, off);
+      }
+      if (threadIdx.x == 0) {
+        s_base = s;
+        s_pbase = u * UNIT_ROWS;   // padded rows of expert e start here
+      }
     }
     __syncthreads();
     if (counts[e] == 0) return;
     int running = s_base;
+    const int pdelta = s_pbase - s_base;   // padded row = compact row + pdelta
     const bool vec_ok = (R % 4) == 0;
     for (int base = 0; base < R; base += DS_THREADS * DS_PER_THREAD) {
       const int f0 = base + threadIdx.x * DS_PER_THREAD;
@@ -95,7 +107,8 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
           const int f = f0 + q;
           row_pair[pos] = f;
           row_of[f] = pos;
-          row_w[pos] = w[f];
+          prow_of[f] = pos + pdelta;
+          prow_w[pos + pdelta] = w[f];
           ++pos;
         }
       }
@@ -129,17 +142,36 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
   }
 }
 
-// One warp per dispatch row: x_perm[row, :] = x[row_pair[row] / k, :] (16-byte copies).
+// One warp per dispatch row: x_pad[padded row, :] = x[token, :] (16-byte copies).
 __global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_pair, int R, int H, int k,
-                   uint16_t* __restrict__ x_perm) {
+gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_pair,
+                   const int32_t* __restrict__ prow_of, int R, int H, int k, uint16_t* __restrict__ x_pad) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
-  const int t = row_pair[row] / k;
+  const int f = row_pair[row];
+  const int t = f / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * H);
+  uint4* dst = reinterpret_cast<uint4*>(x_pad + (size_t)prow_of[f] * H);
   for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
+}
+
+// Debug copy of the intermediates into caller order: h[compact row] and P[t*k+j].
+__global__ void __launch_bounds__(256)
+compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t* __restrict__ prow_of, int R,
+                             int H, int I, const uint16_t* __restrict__ h_pad, const float* __restrict__ P_pad,
+                             uint16_t* __restrict__ h, float* __restrict__ P) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  const int f = row_pair[row];
+  const size_t pr = (size_t)prow_of[f];
+  if (h)
+    for (int i = lane; i < I / 8; i += 32)
+      reinterpret_cast<uint4*>(h + (size_t)row * I)[i] = reinterpret_cast<const uint4*>(h_pad + pr * I)[i];
+  if (P)
+    for (int i = lane; i < H / 4; i += 32)
+      reinterpret_cast<float4*>(P + (size_t)f * H)[i] = reinterpret_cast<const float4*>(P_pad + pr * H)[i];
 }
 
 }  // namespace
@@ -148,13 +180,20 @@ cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int
                             int wave_experts, int lead, cudaStream_t st) {
   dispatch_kernel<<<E + 1, DS_THREADS, 0, st>>>(ws.ids, ws.w, ws.counts, T, E, k, I / L1_COLS, H / L2_COLS,
                                                 num_sms, mode, wave_experts, lead, ws.offsets, ws.row_pair,
-                                                ws.row_of, ws.row_w, ws.tiles, ws.sched, ws.ready);
+                                                ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, int R, int H, int k, uint16_t* x_perm,
-                          cudaStream_t st) {
-  gather_rows_kernel<<<(R + 7) / 8, 256, 0, st>>>(x, row_pair, R, H, k, x_perm);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, const int32_t* prow_of, int R, int H, int k,
+                          uint16_t* x_pad, cudaStream_t st) {
+  gather_rows_kernel<<<(R + 7) / 8, 256, 0, st>>>(x, row_pair, prow_of, R, H, k, x_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,
+                                         const uint16_t* h_pad, const float* P_pad, uint16_t* h, float* P,
+                                         cudaStream_t st) {
+  compact_intermediates_kernel<<<(R + 7) / 8, 256, 0, st>>>(row_pair, prow_of, R, H, I, h_pad, P_pad, h, P);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,7 @@
 // 128 rows of A and one half of B (Linear-1: r = 0 the gate columns, r = 1 the up
 // columns; Linear-2: columns [128 r, 128 r + 128)) into its own shared memory,
 // and its TMEM receives its 128 rows x 256 columns of the accumulator.  Per CTA a
-// pipeline stage is 32 KB (16 KB A + 16 KB half of B), so six stages fit; both
+// pipeline stage is 32 KB (16 KB A + 16 KB half of B), five stages; both
 // CTAs' loads complete on the even CTA's "stage full" barrier, whose single
 // thread issues the MMAs for the pair and multicasts completion to both CTAs'
 // "stage empty" and "accumulator full" barriers.  Each CTA's epilogue signals
@@ -32,6 +32,17 @@
 // at most the number of co-resident clusters, 1 CTA/SM), so the waits finish.
 // Every wait is bounded by timeout_ns; on expiry the CTA records ERR_TIMEOUT,
 // waits (bounded) for its in-flight copies and MMAs, frees TMEM and exits.
+//
+// Rows live in a padded row space (unit g owns rows 256 g .. 256 g + 255), so a
+// CTA's 128 rows are contiguous: A tiles are tiled TMA loads, and outputs go out
+// per 32-row quadrant (one epilogue warp pair): a quadrant whose rows are all
+// valid is staged in shared memory in the 128-byte swizzled layout
+// (conflict-free row writes) and written by a bulk tensor store (h: bf16 32 x 64
+// boxes for Linear-1; P: fp32 32 x 32 boxes in four 64-column passes for
+// Linear-2); the valid rows of a partial quadrant are stored directly; empty
+// quadrants write nothing.  Two 32 KB staging buffers alternate, each reused
+// only after its previous store group has read it.  Linear-1 readiness is
+// published after its h rows are written.
 //
 // Shared-memory operand layouts (128-byte swizzle, as written by TMA):
 //   A (K-major): 128 rows x 128 B per stage; descriptor SBO = 1024 B (8-row
@@ -52,11 +63,16 @@ constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int GEMM_THREADS = 64 + EPI_THREADS;
 constexpr int TMEM_COLS = 512;                         // two 256-column fp32 accumulators
-constexpr int NSTAGE = 6;                              // per-CTA ring depth
+constexpr int NSTAGE = 5;                              // per-CTA ring depth
 constexpr int BH_BYTES = 2 * B_BOX_BYTES;              // this CTA's half of B: 16 KB
 constexpr int PSTAGE_BYTES = A_STAGE_BYTES + BH_BYTES; // 32 KB
 constexpr int PAIR_TX_BYTES = PAIR * PSTAGE_BYTES;     // bytes completing on the even CTA's barrier
-constexpr int SMEM_BAR_OFF = NSTAGE * PSTAGE_BYTES;
+constexpr int STG_BOX_BYTES = BM * 128;                // 128 staged rows x 128 bytes (one column half): 16 KB
+constexpr int ST_ROWS = 32;                            // rows per output store box (one TMEM quadrant)
+constexpr int ST_BOX_BYTES = ST_ROWS * 128;            // 4 KB
+constexpr int STG_BYTES = 2 * STG_BOX_BYTES;           // one staging buffer: two boxes (the two column halves)
+constexpr int SMEM_STG_OFF = NSTAGE * PSTAGE_BYTES;
+constexpr int SMEM_BAR_OFF = SMEM_STG_OFF + 2 * STG_BYTES;
 constexpr int CTL_BYTES = 512;
 constexpr int GEMM_SMEM = SMEM_BAR_OFF + CTL_BYTES + 1024;   // + slack to align the base to 1024 B
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR * BM, MMA_N, true);
@@ -100,6 +116,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -125,6 +142,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     ptx::tma_prefetch_desc(&tmB1);
     ptx::tma_prefetch_desc(&tmA2);
     ptx::tma_prefetch_desc(&tmB2);
+    ptx::tma_prefetch_desc(&tmH);
+    ptx::tma_prefetch_desc(&tmP);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair<TMEM_COLS>(&ctl->tmem_base);
@@ -158,8 +177,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       for (int i = t_begin + cluster; i < t_end && !*abort_flag; i += nclusters) {
         const int4 tl = args.tiles[i];
         const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, g = tl.w;
-        const int m = PAIR * tl.z + rank;              // this CTA's m-tile of the unit
-        const int row0 = args.offsets[e] + m * BM;      // past the expert: rows unused (or zero-filled)
+        const int row0 = g * UNIT_ROWS + rank * BM;     // this CTA's 128 padded rows of the unit
         if (ph == 1) {
           // wait for every Linear-1 tile of this unit, from both CTAs (bounded)
           const int* rp = args.ready + g;
@@ -262,8 +280,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     const int ch = (warp - 2) >> 2;       // column half of this warp
     const uint32_t tempty_pair0 = ptx::mapa_shared(&ctl->tempty[0], 0);
     const uint32_t tempty_pair1 = ptx::mapa_shared(&ctl->tempty[1], 0);
+    uint8_t* const stg = smem + SMEM_STG_OFF;
+    uint32_t sb = 0;                      // staging buffers used so far (all epilogue threads agree)
     int local = 0;
     const bool bilinear = (args.flags & MOE_FLAG_ACT_BILINEAR) != 0;
+    // byte offset of 16-byte chunk cc of this thread's row inside a staged box (128-byte swizzle)
+    auto chunk_off = [&](int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); };
+    // make the next staging buffer writable: its previous store has finished reading it
+    auto acquire_stage = [&]() {
+      if (ep_tid == 0) ptx::bulk_wait_read<1>();
+      ptx::named_bar_sync(1, EPI_THREADS);
+    };
     for (int i = t_begin + cluster; i < t_end; i += nclusters, ++local) {
       const int4 tl = args.tiles[i];
       const int ph = tl.x & 1, nb = tl.x >> 1, e = tl.y, g = tl.w;
@@ -279,21 +306,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       ptx::named_bar_sync(1, EPI_THREADS);
       if (!*(volatile int*)&ctl->ep_ok[local & 1]) break;
       ptx::tc_fence_after();
-      const int rows_valid = args.counts[e] - m * BM;
-      const int grow = args.offsets[e] + m * BM + r;
-      bool valid = r < rows_valid;
-      if (valid && (grow < 0 || grow >= args.R)) {
-        atomicOr(args.err, ERR_CHECK);
-        valid = false;
-      }
+      const int prow0 = g * UNIT_ROWS + rank * BM;   // the CTA's 128 padded rows
+      const int rows_v = max(0, min(BM, args.counts[e] - m * BM));
+      const int nfull = rows_v / ST_ROWS;             // quadrants whose rows are all valid
+      const bool staged = q < nfull;                  // this warp pair's rows go through TMA stores
+      const bool direct = !staged && r < rows_v;      // a valid row of the partial quadrant
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * MMA_N);
+      const uint32_t tempty_addr = as ? tempty_pair1 : tempty_pair0;
       if (ph == 0) {
-        uint16_t* hrow = args.h + (size_t)grow * args.I + nb * L1_COLS;
+        // h = silu(gate) * up for columns [64 ch, 64 ch + 64) of the tile
+        acquire_stage();
+        uint8_t* box = stg + (sb & 1) * STG_BYTES + ch * STG_BOX_BYTES;
+        uint16_t* hrow = args.h_pad + (size_t)(prow0 + r) * args.I + nb * L1_COLS + ch * 64;
 #pragma unroll 1
-        for (int c = ch * 2; c < ch * 2 + 2; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t gv[32], uv[32];
-          ptx::tmem_ld32(taddr + c * 32, gv);
-          ptx::tmem_ld32(taddr + L1_COLS + c * 32, uv);
+          ptx::tmem_ld32(taddr + ch * 64 + c * 32, gv);
+          ptx::tmem_ld32(taddr + L1_COLS + ch * 64 + c * 32, uv);
           ptx::tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
@@ -304,42 +333,68 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
             const float v1 = bilinear ? g1 * u1 : silu_mul(g1, u1);
             pk[j] = pack_bf16x2(v0, v1);
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v4 = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            if (staged) *reinterpret_cast<uint4*>(box + chunk_off(4 * c + j)) = v4;
+            else if (direct) reinterpret_cast<uint4*>(hrow)[4 * c + j] = v4;
           }
         }
-        ptx::fence_proxy_async_global();   // h rows will be read by TMA (async proxy)
-      } else {
-        const float wgt = valid ? args.row_w[grow] : 0.0f;
-        const int pair = valid ? args.row_pair[grow] : 0;
-        float* prow = args.P + (size_t)pair * args.H + nb * L2_COLS;
-#pragma unroll 1
-        for (int c = ch * 4; c < ch * 4 + 4; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld32(taddr + c * 32, v);
-          ptx::tmem_ld_wait();
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(wgt * __uint_as_float(v[4 * j]), wgt * __uint_as_float(v[4 * j + 1]),
-                                   wgt * __uint_as_float(v[4 * j + 2]), wgt * __uint_as_float(v[4 * j + 3]));
+        ptx::tc_fence_before();
+        ptx::fence_proxy_async_smem();
+        if (direct) ptx::fence_proxy_async_global();   // h rows will be read by TMA (async proxy)
+        ptx::named_bar_sync(1, EPI_THREADS);
+        if (ep_tid == 0) {
+          ptx::mbar_arrive_cluster(tempty_addr);     // accumulator free for the next tile
+          uint8_t* buf = stg + (sb & 1) * STG_BYTES;
+          for (int gq = 0; gq < nfull; ++gq) {
+            ptx::tma_store_2d(&tmH, buf + gq * ST_BOX_BYTES, nb * L1_COLS, prow0 + gq * ST_ROWS);
+            ptx::tma_store_2d(&tmH, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L1_COLS + 64,
+                              prow0 + gq * ST_ROWS);
           }
-        }
-      }
-      // all epilogue threads are done with the accumulator (and, for Linear-1, stored h)
-      ptx::tc_fence_before();
-      ptx::named_bar_sync(1, EPI_THREADS);
-      if (ep_tid == 0) {
-        ptx::mbar_arrive_cluster(as ? tempty_pair1 : tempty_pair0);
-        if (ph == 0) {
+          ptx::bulk_commit();
+          ptx::bulk_wait<0>();                       // h rows written: publish them to Linear-2
+          ptx::fence_proxy_async_global();
           __threadfence();
           ptx::red_release_add_gpu(args.ready + g, 1);
         }
+        ++sb;
+      } else {
+        // P = w * acc, four passes of 64 columns; warp half ch takes columns [64 p + 32 ch, +32)
+        const float wgt = (staged || direct) ? args.prow_w[prow0 + r] : 0.0f;
+        float* prow = args.P_pad + (size_t)(prow0 + r) * args.H + nb * L2_COLS + ch * 32;
+#pragma unroll 1
+        for (int pass = 0; pass < MMA_N / 64; ++pass) {
+          acquire_stage();
+          uint8_t* box = stg + (sb & 1) * STG_BYTES + ch * STG_BOX_BYTES;
+          uint32_t v[32];
+          ptx::tmem_ld32(taddr + pass * 64 + ch * 32, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f4 = make_float4(wgt * __uint_as_float(v[4 * j]), wgt * __uint_as_float(v[4 * j + 1]),
+                                          wgt * __uint_as_float(v[4 * j + 2]), wgt * __uint_as_float(v[4 * j + 3]));
+            if (staged) *reinterpret_cast<float4*>(box + chunk_off(j)) = f4;
+            else if (direct) reinterpret_cast<float4*>(prow + pass * 64)[j] = f4;
+          }
+          if (pass == MMA_N / 64 - 1) ptx::tc_fence_before();
+          ptx::fence_proxy_async_smem();
+          ptx::named_bar_sync(1, EPI_THREADS);
+          if (ep_tid == 0) {
+            if (pass == MMA_N / 64 - 1) ptx::mbar_arrive_cluster(tempty_addr);
+            uint8_t* buf = stg + (sb & 1) * STG_BYTES;
+            for (int gq = 0; gq < nfull; ++gq) {
+              ptx::tma_store_2d(&tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64, prow0 + gq * ST_ROWS);
+              ptx::tma_store_2d(&tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64 + 32,
+                                prow0 + gq * ST_ROWS);
+            }
+            ptx::bulk_commit();                      // one group per pass, possibly empty
+          }
+          ++sb;
+        }
       }
     }
+    if (ep_tid == 0) ptx::bulk_wait<0>();   // every store of this CTA performed before it exits
   }
 
   if (tracing) {
@@ -404,10 +459,11 @@ cudaError_t gemm_prepare(int device, int* grid) {
 }
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
-                                const CUtensorMap& tB2, const GemmArgs& a, int grid, cudaStream_t st) {
+                                const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
+                                const GemmArgs& a, int grid, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = gemm_config(grid, st, attr);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel, tA1, tB1, tA2, tB2, a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel, tA1, tB1, tA2, tB2, tH, tP, a);
 }
 
 }  // namespace moe

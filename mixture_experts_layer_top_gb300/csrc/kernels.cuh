@@ -8,20 +8,26 @@
 
 namespace moe {
 
+// Row spaces: "compact" rows 0..R-1 group the (token, slot) pairs by expert
+// (row_pair / row_of, as returned by moe_debug_routing); "padded" rows give every
+// 256-row unit of an expert its own block (unit g owns rows 256 g .. 256 g + 255),
+// so the grouped GEMM loads and stores whole 128-row boxes without touching another
+// expert's rows.  x_pad, h_pad and P_pad are indexed by padded row.
 struct Workspace {
   int32_t* ids;       // [T_max*k]
   float* w;           // [T_max*k]
   int32_t* counts;    // [E]
-  int32_t* offsets;   // [E+1]
-  int32_t* row_pair;  // [R_max]
-  int32_t* row_of;    // [R_max]
-  float* row_w;       // [R_max]
-  uint16_t* x_perm;   // [R_max, H] bf16
-  uint16_t* h;        // [R_max, I] bf16
-  float* P;           // [R_max, H] fp32, indexed by t*k+j
+  int32_t* offsets;   // [E+1] compact
+  int32_t* row_pair;  // [R_max] compact row -> t*k+j
+  int32_t* row_of;    // [R_max] t*k+j -> compact row
+  int32_t* prow_of;   // [R_max] t*k+j -> padded row
+  float* prow_w;      // [R_pad_max] router weight of each padded row (valid rows only)
+  uint16_t* x_pad;    // [R_pad_max, H] bf16
+  uint16_t* h_pad;    // [R_pad_max, I] bf16
+  float* P_pad;       // [R_pad_max, H] fp32: w[t,j] * expert output
   int32_t* tiles;     // [max_tiles*4]
-  int32_t* sched;     // [4]: linear-1 tiles, total tiles, m-tiles
-  int32_t* ready;     // [max_mt]
+  int32_t* sched;     // [4]: linear-1 tiles, total tiles, units
+  int32_t* ready;     // [max_units]
   uint32_t* err;      // [1]
   unsigned long long* trace;   // [gemm grid][TRACE_SLOTS] wait-time counters (MOE_FLAG_TRACE)
 };
@@ -43,16 +49,14 @@ struct GemmArgs {
   const int4* tiles;
   const int32_t* sched;
   const int32_t* counts;
-  const int32_t* offsets;
-  const float* row_w;
-  const int32_t* row_pair;
-  uint16_t* h;
-  float* P;
+  const float* prow_w;
+  uint16_t* h_pad;     // direct stores of partial quadrants
+  float* P_pad;
   int32_t* ready;
   uint32_t* err;
   unsigned long long* trace;
   int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all
-  int H, I, E, R, nL1;
+  int H, I, E, R_pad, nL1;
   uint32_t flags;
   int64_t timeout_ns;
 };
@@ -64,11 +68,16 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
                         cudaStream_t st);
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, cudaStream_t st);
-cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, int R, int H, int k, uint16_t* x_perm,
-                          cudaStream_t st);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, const int32_t* prow_of, int R, int H, int k,
+                          uint16_t* x_pad, cudaStream_t st);
+cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,
+                                         const uint16_t* h_pad, const float* P_pad, uint16_t* h, float* P,
+                                         cudaStream_t st);
 cudaError_t gemm_prepare(int device, int* grid);   // grid: CTAs of the co-resident 2-CTA clusters
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
-                                const CUtensorMap& tB2, const GemmArgs& a, int grid, cudaStream_t st);
-cudaError_t launch_combine(const float* P, int T, int H, int k, uint16_t* y, int num_sms, cudaStream_t st);
+                                const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
+                                const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_combine(const float* P_pad, const int32_t* prow_of, int T, int H, int k, uint16_t* y, int num_sms,
+                           cudaStream_t st);
 
 }  // namespace moe

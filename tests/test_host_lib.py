@@ -46,13 +46,17 @@ def test_config_validation(lib, kw, status):
     assert ei.value.status == status
 
 
-def test_workspace_bytes_grows_with_T(lib):
-    a = moe.moe_workspace_bytes(moe.MoEConfig(1024, 2048, 768, 128, 8).c())
-    b = moe.moe_workspace_bytes(moe.MoEConfig(8192, 2048, 768, 128, 8).c())
-    assert b > 7 * a
-    # x_perm (bf16) + h (bf16) + P (fp32) dominate: R*(2H + 2I + 4H) bytes
-    R = 8192 * 8
-    assert b >= R * (2 * 2048 + 2 * 768 + 4 * 2048)
+def test_workspace_bytes_padded_layout(lib):
+    """x, h and P live in a padded row space: every 256-row unit of an expert owns its rows,
+    so the workspace holds at least R and at most R + 256*E rows of (2H + 2I + 4H) bytes."""
+    T, H, I, E, k = 8192, 2048, 768, 128, 8
+    b = moe.moe_workspace_bytes(moe.MoEConfig(T, H, I, E, k).c())
+    per_row = 2 * H + 2 * I + 4 * H
+    R = T * k
+    assert R * per_row <= b
+    assert b <= (R + 256 * E + 256) * (per_row + 8) + R * 24 + T * H * 4 + (16 << 20)
+    small = moe.moe_workspace_bytes(moe.MoEConfig(1024, H, I, E, k).c())
+    assert small < b
 
 
 def test_plan_without_device_fails_cleanly(lib):
