@@ -75,6 +75,13 @@ typedef enum {
                                            variant, same paper as SwiGLU); used by exactness tests */
 #define MOE_FLAG_STAGE_TIMING (1u << 1) /* record CUDA events between stages (moe_stage_times)    */
 #define MOE_FLAG_TRACE (1u << 2)        /* grouped GEMM records per-CTA wait times (moe_trace_read) */
+/* Shared-memory split of the grouped GEMM (results are bit-identical).  Default: a 6-stage
+ * operand ring with one output staging buffer (measured faster on every workload tried, from
+ * weight streaming to 1k rows per expert).  MOE_FLAG_GEMM_COMPUTE selects a 5-stage ring with
+ * two output staging buffers; MOE_FLAG_GEMM_STREAMING names the default explicitly; setting
+ * both is an invalid argument. */
+#define MOE_FLAG_GEMM_STREAMING (1u << 3) /* 6-stage operand ring, one output staging buffer   */
+#define MOE_FLAG_GEMM_COMPUTE (1u << 4)   /* 5-stage operand ring, two output staging buffers  */
 #define MOE_FLAG_TEST_STALL (1u << 8)   /* test only: Linear-2 tiles wait for a readiness count that
                                            is never reached, so the bounded wait expires and
                                            moe_get_status reports MOE_ERR_TIMEOUT (no GPU fault)   */

@@ -36,6 +36,8 @@ MOE_SCHED_PHASED = 2
 MOE_FLAG_ACT_BILINEAR = 1 << 0
 MOE_FLAG_STAGE_TIMING = 1 << 1
 MOE_FLAG_TRACE = 1 << 2
+MOE_FLAG_GEMM_STREAMING = 1 << 3
+MOE_FLAG_GEMM_COMPUTE = 1 << 4
 TRACE_FIELDS = ("prod_wait_empty_ns", "prod_wait_ready_ns", "mma_wait_tempty_ns", "mma_wait_full_ns",
                 "epi_wait_tfull_ns", "cta_ns", "tiles_l1", "tiles_l2")
 MOE_FLAG_TEST_STALL = 1 << 8

@@ -73,6 +73,7 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   if (c->T_max < 1 || c->H < 1 || c->I < 1 || c->E < 1 || c->top_k < 1) return MOE_ERR_INVALID_ARG;
   if (c->schedule < 0 || c->schedule > 2 || c->wave_experts < 0 || c->lead_waves < 0 || c->timeout_ns < 0)
     return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_GEMM_STREAMING) && (c->flags & MOE_FLAG_GEMM_COMPUTE)) return MOE_ERR_INVALID_ARG;
   if (c->H % L2_COLS != 0 || c->I % L1_COLS != 0) return MOE_ERR_UNSUPPORTED;
   if (c->E > MAX_E || c->top_k > MAX_K || c->top_k > c->E) return MOE_ERR_UNSUPPORTED;
   const int64_t R = (int64_t)c->T_max * c->top_k;
@@ -265,7 +266,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
                                 router_logits, T, H, E, st));
     ++nl;
   }
-  MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, st));
+  MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->num_sms, st));
   ++nl;
   rec(1);
   MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, c.schedule, c.wave_experts, c.lead_waves,
@@ -302,15 +303,16 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.nL1 = I / L1_COLS;
   ga.flags = c.flags;
   ga.timeout_ns = c.timeout_ns;
+  const bool streaming = !(c.flags & MOE_FLAG_GEMM_COMPUTE);   // the deeper operand ring by default
   if (c.schedule == MOE_SCHED_PHASED) {
     ga.range_sel = 0;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, streaming, st));
     ga.range_sel = 1;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, streaming, st));
     nl += 2;
   } else {
     ga.range_sel = 2;
-    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, st));
+    MOE_CK(launch_grouped_gemm(tA1, tB1, tA2, tB2, tH, tP, ga, p->gemm_grid, streaming, st));
     ++nl;
   }
   rec(4);

@@ -16,7 +16,7 @@
 // 128 rows of A and one half of B (Linear-1: r = 0 the gate columns, r = 1 the up
 // columns; Linear-2: columns [128 r, 128 r + 128)) into its own shared memory,
 // and its TMEM receives its 128 rows x 256 columns of the accumulator.  Per CTA a
-// pipeline stage is 32 KB (16 KB A + 16 KB half of B), five stages; both
+// pipeline stage is 32 KB (16 KB A + 16 KB half of B), NST stages; both
 // CTAs' loads complete on the even CTA's "stage full" barrier, whose single
 // thread issues the MMAs for the pair and multicasts completion to both CTAs'
 // "stage empty" and "accumulator full" barriers.  Each CTA's epilogue signals
@@ -40,9 +40,15 @@
 // (conflict-free row writes) and written by a bulk tensor store (h: bf16 32 x 64
 // boxes for Linear-1; P: fp32 32 x 32 boxes in four 64-column passes for
 // Linear-2); the valid rows of a partial quadrant are stored directly; empty
-// quadrants write nothing.  Two 32 KB staging buffers alternate, each reused
+// quadrants write nothing.  NBUF 32 KB staging buffers rotate, each reused
 // only after its previous store group has read it.  Linear-1 readiness is
 // published after its h rows are written.
+//
+// Two shared-memory splits are compiled: <6 stages, 1 staging buffer> (the
+// default: the deeper ring keeps more operand bytes in flight, which measured
+// faster both when the GEMMs stream weights and when they are tensor-bound) and
+// <5 stages, 2 staging buffers> (a store drains while the next chunk is
+// written).  Both compute bit-identical results.
 //
 // Shared-memory operand layouts (128-byte swizzle, as written by TMA):
 //   A (K-major): 128 rows x 128 B per stage; descriptor SBO = 1024 B (8-row
@@ -63,7 +69,7 @@ constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int GEMM_THREADS = 64 + EPI_THREADS;
 constexpr int TMEM_COLS = 512;                         // two 256-column fp32 accumulators
-constexpr int NSTAGE = 5;                              // per-CTA ring depth
+constexpr int MAX_NST = 6;                             // deepest per-CTA ring compiled
 constexpr int BH_BYTES = 2 * B_BOX_BYTES;              // this CTA's half of B: 16 KB
 constexpr int PSTAGE_BYTES = A_STAGE_BYTES + BH_BYTES; // 32 KB
 constexpr int PAIR_TX_BYTES = PAIR * PSTAGE_BYTES;     // bytes completing on the even CTA's barrier
@@ -71,15 +77,21 @@ constexpr int STG_BOX_BYTES = BM * 128;                // 128 staged rows x 128 
 constexpr int ST_ROWS = 32;                            // rows per output store box (one TMEM quadrant)
 constexpr int ST_BOX_BYTES = ST_ROWS * 128;            // 4 KB
 constexpr int STG_BYTES = 2 * STG_BOX_BYTES;           // one staging buffer: two boxes (the two column halves)
-constexpr int SMEM_STG_OFF = NSTAGE * PSTAGE_BYTES;
-constexpr int SMEM_BAR_OFF = SMEM_STG_OFF + 2 * STG_BYTES;
 constexpr int CTL_BYTES = 512;
-constexpr int GEMM_SMEM = SMEM_BAR_OFF + CTL_BYTES + 1024;   // + slack to align the base to 1024 B
+// Shared-memory layout of a <NST stages, NBUF staging buffers> instance.
+template <int NST, int NBUF>
+struct Layout {
+  static constexpr int STG_OFF = NST * PSTAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + NBUF * STG_BYTES;
+  static constexpr int SMEM = BAR_OFF + CTL_BYTES + 1024;   // + slack to align the base to 1024 B
+  static_assert(NST <= MAX_NST && NBUF >= 1 && NBUF <= 2, "unsupported ring split");
+  static_assert(SMEM <= 232448, "shared memory per CTA exceeded");
+};
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR * BM, MMA_N, true);
 
 struct SmemCtl {
-  uint64_t full[NSTAGE];    // even CTA: both CTAs' loads of the stage landed
-  uint64_t empty[NSTAGE];   // both CTAs: the pair MMAs of the stage completed
+  uint64_t full[MAX_NST];   // even CTA: both CTAs' loads of the stage landed
+  uint64_t empty[MAX_NST];  // both CTAs: the pair MMAs of the stage completed
   uint64_t tfull[2];        // both CTAs: accumulator ready
   uint64_t tempty[2];       // even CTA: both CTAs' epilogues drained the accumulator
   uint64_t drain;
@@ -88,7 +100,6 @@ struct SmemCtl {
   int ep_ok[2];             // epilogue go/stop decision of the waiting thread, by tile parity
 };
 static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block exceeds its shared-memory reservation");
-static_assert(GEMM_SMEM <= 232448, "shared memory per CTA exceeded");
 
 __device__ __forceinline__ void set_abort(SmemCtl* ctl, uint32_t* err, uint32_t code) {
   atomicOr(err, code);
@@ -113,6 +124,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+template <int NST, int NBUF>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -120,14 +132,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
                     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_BAR_OFF);
+  using L = Layout<NST, NBUF>;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + L::BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const bool leader = rank == 0;
   constexpr uint16_t CTA_MASK = (1u << PAIR) - 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NST; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);        // even CTA's producer (expect_tx for both CTAs' bytes)
       ptx::mbar_init(&ctl->empty[s], 1);       // the pair MMA commit
     }
@@ -215,14 +228,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           ptx::tma_load_2d_pair(tB, full_pair, sB + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
           filled_mask |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
       }
       // Before the CTA may exit: every fill of every stage has been released by the pair
       // MMA (its commit arrives here) - which also means every copy into this CTA landed.
       int dummy = 0;
-      for (int s = 0; s < NSTAGE; ++s)
+      for (int s = 0; s < NST; ++s)
         if (filled_mask & (1u << s)) ptx::mbar_wait(&ctl->empty[s], (last_par >> s) & 1u, tmo, &dummy);
     }
     __syncwarp();
@@ -259,7 +272,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           }
           issued_any = true;
           ptx::mma_commit_pair_mc(&ctl->empty[stage], CTA_MASK);   // frees the stage in both CTAs
-          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
         ptx::mma_commit_pair_mc(&ctl->tfull[as], CTA_MASK);
@@ -280,7 +293,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     const int ch = (warp - 2) >> 2;       // column half of this warp
     const uint32_t tempty_pair0 = ptx::mapa_shared(&ctl->tempty[0], 0);
     const uint32_t tempty_pair1 = ptx::mapa_shared(&ctl->tempty[1], 0);
-    uint8_t* const stg = smem + SMEM_STG_OFF;
+    uint8_t* const stg = smem + L::STG_OFF;
     uint32_t sb = 0;                      // staging buffers used so far (all epilogue threads agree)
     int local = 0;
     const bool bilinear = (args.flags & MOE_FLAG_ACT_BILINEAR) != 0;
@@ -288,7 +301,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
     auto chunk_off = [&](int cc) { return r * 128 + ((cc ^ (r & 7)) << 4); };
     // make the next staging buffer writable: its previous store has finished reading it
     auto acquire_stage = [&]() {
-      if (ep_tid == 0) ptx::bulk_wait_read<1>();
+      if (ep_tid == 0) ptx::bulk_wait_read<NBUF - 1>();
       ptx::named_bar_sync(1, EPI_THREADS);
     };
     for (int i = t_begin + cluster; i < t_end; i += nclusters, ++local) {
@@ -316,7 +329,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
       if (ph == 0) {
         // h = silu(gate) * up for columns [64 ch, 64 ch + 64) of the tile
         acquire_stage();
-        uint8_t* box = stg + (sb & 1) * STG_BYTES + ch * STG_BOX_BYTES;
+        uint8_t* box = stg + (sb % NBUF) * STG_BYTES + ch * STG_BOX_BYTES;
         uint16_t* hrow = args.h_pad + (size_t)(prow0 + r) * args.I + nb * L1_COLS + ch * 64;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
@@ -346,7 +359,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         ptx::named_bar_sync(1, EPI_THREADS);
         if (ep_tid == 0) {
           ptx::mbar_arrive_cluster(tempty_addr);     // accumulator free for the next tile
-          uint8_t* buf = stg + (sb & 1) * STG_BYTES;
+          uint8_t* buf = stg + (sb % NBUF) * STG_BYTES;
           for (int gq = 0; gq < nfull; ++gq) {
             ptx::tma_store_2d(&tmH, buf + gq * ST_BOX_BYTES, nb * L1_COLS, prow0 + gq * ST_ROWS);
             ptx::tma_store_2d(&tmH, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L1_COLS + 64,
@@ -366,7 +379,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
 #pragma unroll 1
         for (int pass = 0; pass < MMA_N / 64; ++pass) {
           acquire_stage();
-          uint8_t* box = stg + (sb & 1) * STG_BYTES + ch * STG_BOX_BYTES;
+          uint8_t* box = stg + (sb % NBUF) * STG_BYTES + ch * STG_BOX_BYTES;
           uint32_t v[32];
           ptx::tmem_ld32(taddr + pass * 64 + ch * 32, v);
           ptx::tmem_ld_wait();
@@ -382,7 +395,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           ptx::named_bar_sync(1, EPI_THREADS);
           if (ep_tid == 0) {
             if (pass == MMA_N / 64 - 1) ptx::mbar_arrive_cluster(tempty_addr);
-            uint8_t* buf = stg + (sb & 1) * STG_BYTES;
+            uint8_t* buf = stg + (sb % NBUF) * STG_BYTES;
             for (int gq = 0; gq < nfull; ++gq) {
               ptx::tma_store_2d(&tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64, prow0 + gq * ST_ROWS);
               ptx::tma_store_2d(&tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64 + 32,
@@ -425,11 +438,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
 
 }  // namespace
 
+using GemmStreaming = Layout<6, 1>;
+using GemmCompute = Layout<5, 2>;
+static_assert(GemmStreaming::SMEM == GemmCompute::SMEM, "both splits share one occupancy computation");
+
 static cudaLaunchConfig_t gemm_config(int grid, cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = GEMM_SMEM;
+  cfg.dynamicSmemBytes = GemmCompute::SMEM;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
@@ -441,7 +458,11 @@ static cudaLaunchConfig_t gemm_config(int grid, cudaStream_t st, cudaLaunchAttri
 }
 
 cudaError_t gemm_prepare(int device, int* grid) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<6, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       GemmStreaming::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<5, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCompute::SMEM);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
@@ -449,9 +470,12 @@ cudaError_t gemm_prepare(int device, int* grid) {
   // every cluster of the grid must be resident at once (Linear-2 tiles wait for earlier tickets)
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = gemm_config(sms / PAIR * PAIR, nullptr, attr);
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel, &cfg);
+  int clusters = 0, clusters_s = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<5, 2>, &cfg);
   if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveClusters(&clusters_s, grouped_gemm_kernel<6, 1>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters_s < clusters) clusters = clusters_s;
   if (clusters > sms / PAIR) clusters = sms / PAIR;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   *grid = clusters * PAIR;
@@ -460,10 +484,11 @@ cudaError_t gemm_prepare(int device, int* grid) {
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
-                                const GemmArgs& a, int grid, cudaStream_t st) {
+                                const GemmArgs& a, int grid, bool streaming, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = gemm_config(grid, st, attr);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel, tA1, tB1, tA2, tB2, tH, tP, a);
+  if (streaming) return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<6, 1>, tA1, tB1, tA2, tB2, tH, tP, a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<5, 2>, tA1, tB1, tA2, tB2, tH, tP, a);
 }
 
 }  // namespace moe

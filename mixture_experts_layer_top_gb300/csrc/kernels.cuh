@@ -65,7 +65,7 @@ cudaError_t router_prepare();
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
                                  int H, int E, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                        cudaStream_t st);
+                        int num_sms, cudaStream_t st);
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, cudaStream_t st);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, const int32_t* prow_of, int R, int H, int k,
@@ -76,7 +76,7 @@ cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t*
 cudaError_t gemm_prepare(int device, int* grid);   // grid: CTAs of the co-resident 2-CTA clusters
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
-                                const GemmArgs& a, int grid, cudaStream_t st);
+                                const GemmArgs& a, int grid, bool streaming, cudaStream_t st);
 cudaError_t launch_combine(const float* P_pad, const int32_t* prow_of, int T, int H, int k, uint16_t* y, int num_sms,
                            cudaStream_t st);
 

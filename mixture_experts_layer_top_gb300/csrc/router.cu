@@ -170,51 +170,91 @@ __device__ __forceinline__ uint32_t logit_key(float l) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per token.  Keys combine (logit key, 0xFFFF - expert) so the
-// maximum is the highest logit and, among equal logits, the lowest id.
-__global__ void __launch_bounds__(256)
+constexpr int TK_WARPS = 8;
+constexpr int TK_MAX_TOK_PER_WARP = 8;
+
+// Exact a - b as hi + lo (Knuth's two-sum); lo = 0 when hi is not finite.
+__device__ __forceinline__ float two_diff(float a, float b, float* lo) {
+  const float hi = __fsub_rn(a, b);
+  if (!isfinite(hi)) {
+    *lo = 0.0f;
+    return hi;
+  }
+  const float bb = __fsub_rn(hi, a);
+  *lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(-b, bb));
+  return hi;
+}
+
+// One warp per token (tpw tokens per warp in turn).  Keys combine (logit key,
+// 0xFFFF - expert) so the maximum is the highest logit and, among equal logits,
+// the lowest id.  Weights: softmax over the k selected logits, in fp32 with the
+// argument l_j - l_0 kept exact as a two-term sum (exp(hi + lo) = exp(hi)(1 + lo)
+// to first order, lo <= half an ulp of hi) and the slot-order sum compensated
+// (Neumaier), so each weight is within a few 1e-7 relative of the exactly
+// rounded softmax; fp64 is avoided (its rate on this GPU is a small fraction of
+// fp32).  Expert counts go through a shared-memory histogram, one global atomic
+// per (block, expert).
+__global__ void __launch_bounds__(TK_WARPS * 32)
 topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
-            float* __restrict__ w, int32_t* __restrict__ counts) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* l = logits + (size_t)t * E;
-  uint64_t key[MAX_E / 32];
+            float* __restrict__ w, int32_t* __restrict__ counts, int tpw) {
+  __shared__ int32_t hist[MAX_E];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nkey = (E + 31) >> 5;
+  for (int it = 0; it < tpw; ++it) {
+    const int t = (blockIdx.x * tpw + it) * TK_WARPS + warp;
+    if (t >= T) break;
+    const float* l = logits + (size_t)t * E;
+    uint64_t key[MAX_E / 32];
 #pragma unroll
-  for (int i = 0; i < MAX_E / 32; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = (e < E) ? (((uint64_t)logit_key(l[e]) << 32) | (uint64_t)(0xFFFFu - (uint32_t)e)) : 0ull;
-  }
-  int my_e = 0;
-  float my_l = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
-#pragma unroll
-    for (int i = 0; i < MAX_E / 32; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-      best = o > best ? o : best;
+    for (int i = 0; i < MAX_E / 32; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = (i < nkey && e < E) ? (((uint64_t)logit_key(l[e]) << 32) | (uint64_t)(0xFFFFu - (uint32_t)e)) : 0ull;
     }
-    const int e = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFu));
+    int my_e = 0;
+    float my_l = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      uint64_t best = 0;
 #pragma unroll
-    for (int i = 0; i < MAX_E / 32; ++i)
-      if (key[i] == best) key[i] = 0ull;
-    if (lane == j) {
-      my_e = e;
-      my_l = l[e];
+      for (int i = 0; i < MAX_E / 32; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+        best = o > best ? o : best;
+      }
+      const int e = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFu));
+#pragma unroll
+      for (int i = 0; i < MAX_E / 32; ++i)
+        if (key[i] == best) key[i] = 0ull;
+      if (lane == j) {
+        my_e = e;
+        my_l = l[e];
+      }
+    }
+    const float m = __shfl_sync(0xFFFFFFFFu, my_l, 0);
+    float lo;
+    const float hi = two_diff(my_l, m, &lo);
+    const float eh = expf(hi);
+    const float ex = (lane < k) ? __fmaf_rn(eh, lo, eh) : 0.0f;
+    float sum = 0.0f, comp = 0.0f;   // Neumaier-compensated sum in slot order
+    for (int j = 0; j < k; ++j) {
+      const float v = __shfl_sync(0xFFFFFFFFu, ex, j);
+      const float s2 = __fadd_rn(sum, v);
+      comp = __fadd_rn(comp, fabsf(sum) >= fabsf(v) ? __fadd_rn(__fsub_rn(sum, s2), v)
+                                                   : __fadd_rn(__fsub_rn(v, s2), sum));
+      sum = s2;
+    }
+    if (isfinite(sum)) sum = __fadd_rn(sum, comp);
+    if (lane < k) {
+      ids[(size_t)t * k + lane] = my_e;
+      w[(size_t)t * k + lane] = __fdiv_rn(ex, sum);
+      atomicAdd(&hist[my_e], 1);
     }
   }
-  // weights: softmax over the k selected logits, exponentials and sum in fp64
-  const double m = (double)__shfl_sync(0xFFFFFFFFu, my_l, 0);
-  const float ex = (lane < k) ? (float)exp((double)my_l - m) : 0.0f;
-  double sum = 0.0;
-  for (int j = 0; j < k; ++j) sum += (double)__shfl_sync(0xFFFFFFFFu, ex, j);
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = my_e;
-    w[(size_t)t * k + lane] = (float)((double)ex / sum);
-    atomicAdd(&counts[my_e], 1);
-  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    if (hist[i]) atomicAdd(&counts[i], hist[i]);
 }
 
 }  // namespace
@@ -231,8 +271,12 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const fl
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                        cudaStream_t st) {
-  topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, k, ids, w, counts);
+                        int num_sms, cudaStream_t st) {
+  // tokens per warp: enough blocks for two per SM, up to TK_MAX_TOK_PER_WARP tokens each
+  int tpw = (T + 2 * num_sms * TK_WARPS - 1) / (2 * num_sms * TK_WARPS);
+  tpw = tpw < 1 ? 1 : (tpw > TK_MAX_TOK_PER_WARP ? TK_MAX_TOK_PER_WARP : tpw);
+  const int per_block = tpw * TK_WARPS;
+  topk_kernel<<<(T + per_block - 1) / per_block, TK_WARPS * 32, 0, st>>>(logits, T, E, k, ids, w, counts, tpw);
   return cudaGetLastError();
 }
 

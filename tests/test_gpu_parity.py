@@ -58,7 +58,9 @@ def test_tiny_full_parity(schedule):
 
 def test_bilinear_integer_exact():
     """Integer-valued inputs and the bilinear GLU: every accumulation is exact, so
-    h, P and y must match the oracle bit for bit (tiling, TMA boxes, descriptors)."""
+    h, P and y must match the oracle bit for bit (tiling, TMA boxes, descriptors).
+    The caller's logits give each token k tied top logits, so every router weight is
+    exactly 1/k and the check does not depend on the rounding of the softmax."""
     T, H, I, E, k = 300, 512, 256, 8, 2
     rng = np.random.default_rng(11)
 
@@ -69,9 +71,15 @@ def test_bilinear_integer_exact():
     Wr = oracle.f32_to_bf16((rng.standard_normal((H, E)) / np.sqrt(H)).astype(np.float32))
     W1 = oracle.f32_to_bf16(tern((E, H, 2 * I), 0.2))
     W2 = oracle.f32_to_bf16(tern((E, I, H), 0.2))
-    ref = oracle.forward(x, Wr, None, W1, W2, k, act=oracle.ACT_BILINEAR, want_intermediates=True)
+    logits = np.zeros((T, E), np.float32)
+    for t in range(T):
+        logits[t, rng.choice(E, size=k, replace=False)] = 1.0
+    ref = oracle.forward(x, Wr, None, W1, W2, k, act=oracle.ACT_BILINEAR, logits=logits,
+                         want_intermediates=True)
+    assert np.all(ref["w"] == np.float32(1.0 / k))
     layer = moe.MoELayer(moe.MoEConfig(T, H, I, E, k, flags=moe.MOE_FLAG_ACT_BILINEAR), 0)
-    y, _ = layer.forward(from_bits(x), from_bits(Wr), from_bits(W1), from_bits(W2), check=True)
+    y, _ = layer.forward(from_bits(x), None, from_bits(W1), from_bits(W2),
+                         logits=torch.from_numpy(logits).cuda(), check=True)
     r = layer.routing(T)
     routing_equal(r, ref, T)
     hh, P = layer.intermediates(T)
@@ -88,11 +96,15 @@ def test_bilinear_integer_exact():
 
 
 def test_schedules_bitwise_identical():
+    """Every tile schedule and both shared-memory splits of the grouped GEMM give the same bits
+    (the default streaming split and the forced compute split)."""
     wl = synth.Workload("mid", 2048, 1024, 512, 32, 4)
     d = synth.device_inputs(wl)
     outs = []
-    for sched, we, lead in [(0, 0, 1), (1, 0, 1), (1, 0, 3), (2, 0, 1), (0, 3, 1), (1, 2, 2)]:
-        layer = _layer(wl, sched, wave_experts=we, lead=lead)
+    S = moe.MOE_FLAG_GEMM_COMPUTE
+    for sched, we, lead, fl in [(0, 0, 1, 0), (1, 0, 1, 0), (1, 0, 3, 0), (2, 0, 1, 0), (0, 3, 1, 0),
+                                (1, 2, 2, 0), (1, 0, 1, S), (2, 0, 1, S), (0, 3, 1, S)]:
+        layer = _layer(wl, sched, wave_experts=we, lead=lead, flags=fl)
         y, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
         y2, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "repeat not bitwise identical"
@@ -129,12 +141,14 @@ def test_workload_parity(name, nsample, schedule):
 
 
 # --------------------------------------------------------------------------- edge cases
-@pytest.mark.parametrize("T", [1, 127, 129, 1000])
-def test_ragged_token_counts(T):
+@pytest.mark.parametrize("T,flags", [(1, 0), (127, 0), (129, 0), (1000, 0),
+                                     (129, moe.MOE_FLAG_GEMM_COMPUTE), (1000, moe.MOE_FLAG_GEMM_COMPUTE)])
+def test_ragged_token_counts(T, flags):
+    """Ragged token counts against the full oracle (default split, and the compute split forced)."""
     wl = synth.Workload("edge", T, 512, 256, 16, 4)
     h = synth.host_inputs(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
-    layer = _layer(wl, 0, T_max=1024)
+    layer = _layer(wl, 0, T_max=1024, flags=flags)
     d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
     y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     assert np.array_equal(logits.cpu().numpy(), ref["logits"])
@@ -164,6 +178,25 @@ def test_logits_as_input_and_one_hot_expert():
     d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
     lg = torch.from_numpy(logits).cuda()
     y, _ = layer.forward(d["x"], None, d["W1"], d["W2"], logits=lg, check=True)
+    routing_equal(layer.routing(wl.T), ref, wl.T)
+    check_y(bits(y), ref["y"])
+
+
+def test_router_weights_wide_logits():
+    """Softmax weights over the k selected logits within 1e-6 relative of the oracle's
+    fp64 evaluation when the logits spread widely (exp arguments down to about -150),
+    tie in blocks (integer-valued rows), and some rows hold only 3 finite logits."""
+    wl = synth.Workload("widelogits", 2048, 512, 256, 64, 8)
+    h = synth.host_inputs(wl)
+    rng = np.random.default_rng(7)
+    logits = (rng.standard_normal((wl.T, wl.E)) * 25.0).astype(np.float32)
+    logits[::5] = np.round(logits[::5] / 10.0)                       # many exact ties
+    few = np.arange(3, wl.T, 11)
+    logits[few, 3:] = -np.inf                                        # only 3 finite logits
+    ref = oracle.forward(h["x"], h["Wr"], None, h["W1"], h["W2"], wl.k, logits=logits)
+    layer = _layer(wl)
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    y, _ = layer.forward(d["x"], None, d["W1"], d["W2"], logits=torch.from_numpy(logits).cuda(), check=True)
     routing_equal(layer.routing(wl.T), ref, wl.T)
     check_y(bits(y), ref["y"])
 
