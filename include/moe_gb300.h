@@ -82,6 +82,17 @@ typedef enum {
  * both is an invalid argument. */
 #define MOE_FLAG_GEMM_STREAMING (1u << 3) /* 6-stage operand ring, one output staging buffer   */
 #define MOE_FLAG_GEMM_COMPUTE (1u << 4)   /* 5-stage operand ring, two output staging buffers  */
+/* Router (W_router != NULL).  Routing is always the top-k of the canonical fp32 logits (per
+ * logit: 32 partial sums, partial j accumulating h = j (mod 32) in ascending h with fused
+ * multiply-adds, then the pairwise tree (j, j+16), (j, j+8), ..., (j, j+1), then + bias).
+ * Default: tensor-core estimates of all logits plus an a-priori error bound; only experts the
+ * bound cannot exclude from the top-k get their canonical logit evaluated.  The logits row
+ * written out then holds canonical values for those experts (always including the k selected)
+ * and the tensor-core estimate (+ bias) elsewhere, within
+ *   d = cH * ||x_t||_2 * ||Wr[:,e]||_2 + 2^-20 (|estimate - bias| + |bias|) of the canonical value,
+ *   cH from moe_router_bound (at most (H/16 + 1) 2^-17 + (H/32 + 8 + 64) 2^-22).
+ * MOE_FLAG_EXACT_LOGITS evaluates every logit in the canonical order on the CUDA cores. */
+#define MOE_FLAG_EXACT_LOGITS (1u << 5)
 #define MOE_FLAG_TEST_STALL (1u << 8)   /* test only: Linear-2 tiles wait for a readiness count that
                                            is never reached, so the bounded wait expires and
                                            moe_get_status reports MOE_ERR_TIMEOUT (no GPU fault)   */
@@ -115,7 +126,8 @@ MOE_API moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes)
 /* One forward of the layer for T tokens (0 <= T <= T_max; T = 0 enqueues nothing), enqueued
  * on `stream` (a cudaStream_t; NULL = the legacy default stream).  Never synchronises.
  *   x             bf16 [T, H]            input tokens
- *   router_logits fp32 [T, E]            OUTPUT when W_router != NULL, else INPUT
+ *   router_logits fp32 [T, E]            OUTPUT when W_router != NULL (see MOE_FLAG_EXACT_LOGITS
+ *                                        for which entries are canonical), else INPUT
  *   W_router      bf16 [H, E] or NULL    router weight
  *   W1_gate_up    bf16 [E, H, 2I]        Linear-1; columns [0,I) gate, [I,2I) up
  *   W2            bf16 [E, I, H]         Linear-2
@@ -162,6 +174,11 @@ MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
  * for a free accumulator, MMA issuer waiting for operands, epilogue waiting for an accumulator,
  * CTA lifetime} in nanoseconds, then {Linear-1 tiles, Linear-2 tiles}. */
 MOE_API moe_status_t moe_trace_read(moe_plan_t plan, uint64_t* host_buf, size_t cap, size_t* n);
+
+/* The coefficient cH of the default router's error bound (MOE_FLAG_EXACT_LOGITS) for a forward
+ * of T tokens (1 <= T <= T_max): n = the MMA steps of the longest accumulation chain, A the
+ * chains per CTA, S the K splits; cH = (n + 1) 2^-17 + (A S + H/32 + 8) 2^-22.  Host only. */
+MOE_API moe_status_t moe_router_bound(moe_plan_t plan, int32_t T, float* cH);
 
 /* Number of kernels the last moe_forward launched. */
 MOE_API moe_status_t moe_last_launch_count(moe_plan_t plan, int32_t* n);

@@ -38,6 +38,7 @@ MOE_FLAG_STAGE_TIMING = 1 << 1
 MOE_FLAG_TRACE = 1 << 2
 MOE_FLAG_GEMM_STREAMING = 1 << 3
 MOE_FLAG_GEMM_COMPUTE = 1 << 4
+MOE_FLAG_EXACT_LOGITS = 1 << 5
 TRACE_FIELDS = ("prod_wait_empty_ns", "prod_wait_ready_ns", "mma_wait_tempty_ns", "mma_wait_full_ns",
                 "epi_wait_tfull_ns", "cta_ns", "tiles_l1", "tiles_l2")
 MOE_FLAG_TEST_STALL = 1 << 8
@@ -48,7 +49,8 @@ STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")
 EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_get_status",
             "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
-            "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read")
+            "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read",
+            "moe_router_bound")
 
 
 class MoEError(RuntimeError):
@@ -93,6 +95,7 @@ def load() -> ctypes.CDLL:
     L.moe_debug_intermediates.argtypes = [vp, i32, vp, vp, vp]
     L.moe_stage_times.argtypes = [vp, P(ctypes.c_float)]
     L.moe_last_launch_count.argtypes = [vp, P(i32)]
+    L.moe_router_bound.argtypes = [vp, i32, P(ctypes.c_float)]
     L.moe_plan_destroy.argtypes = [vp]
     L.moe_status_string.argtypes = [ctypes.c_int]
     L.moe_status_string.restype = ctypes.c_char_p
@@ -156,6 +159,14 @@ def moe_stage_times(plan: int):
     if st != MOE_OK:
         raise MoEError(st, "moe_stage_times")
     return list(arr)
+
+
+def moe_router_bound(plan: int, T: int) -> float:
+    c = ctypes.c_float(0.0)
+    st = load().moe_router_bound(plan, T, ctypes.byref(c))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_router_bound")
+    return c.value
 
 
 def moe_last_launch_count(plan: int) -> int:
@@ -335,3 +346,7 @@ class MoELayer:
 
     def launch_count(self) -> int:
         return moe_last_launch_count(self.plan)
+
+    def router_bound(self, T: int) -> float:
+        """cH of the default router's logit error bound for T tokens."""
+        return moe_router_bound(self.plan, T)

@@ -27,6 +27,7 @@ struct moe_plan_s {
   void* y_stage;
   float* bias;
   Workspace ws;
+  RouterWs rw;
   cudaEvent_t ev[MOE_NUM_STAGES + 1];
   bool timing;
   int last_launches;
@@ -83,7 +84,7 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   return MOE_OK;
 }
 
-constexpr int N_BUFS = 17;
+constexpr int N_BUFS = 22;
 
 struct Layout {
   size_t off[N_BUFS];
@@ -110,6 +111,11 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
       16,                                  // err
       (size_t)c.T_max * c.H * 2,           // x staging (moe_forward_host)
       (size_t)c.T_max * c.H * 2,           // y staging (moe_forward_host)
+      (size_t)c.E * c.H * 2,               // router: Wr transposed
+      (size_t)(c.H / 64) * c.E * 4,        // router: column sums of squares per 64 rows
+      (size_t)c.E * 4,                     // router: column norm bounds
+      16,                                  // router: transpose block counter
+      (size_t)router_part_rows(c.T_max) * c.E * 4,   // router: split-K partial estimates
   };
   Layout L;
   size_t o = 0;
@@ -203,7 +209,13 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->ws.err = reinterpret_cast<uint32_t*>(b + L.off[14]);
   p->x_stage = b + L.off[15];
   p->y_stage = b + L.off[16];
-  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  p->rw.WrT = reinterpret_cast<uint16_t*>(b + L.off[17]);
+  p->rw.nw_part = reinterpret_cast<float*>(b + L.off[18]);
+  p->rw.nw = reinterpret_cast<float*>(b + L.off[19]);
+  p->rw.done = reinterpret_cast<int*>(b + L.off[20]);
+  p->rw.part = reinterpret_cast<float*>(b + L.off[21]);
+  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess || cudaMemset(p->rw.done, 0, 16) != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
   if (cfg->router_bias) {
     if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
       cudaGetLastError();
@@ -213,7 +225,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
     if (cudaMemcpy(p->bias, cfg->router_bias, sizeof(float) * cfg->E, cudaMemcpyHostToDevice) != cudaSuccess)
       return fail(MOE_ERR_CUDA);
   }
-  if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess)
+  if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess ||
+      router_tc_prepare() != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   if (cfg->flags & MOE_FLAG_TRACE) {
     if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid) != cudaSuccess) {
@@ -261,13 +274,26 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   } while (0)
   rec(0);
   MOE_CK(cudaMemsetAsync(p->ws.counts, 0, sizeof(int32_t) * E, st));
-  if (W_router) {
-    MOE_CK(launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router), p->bias,
-                                router_logits, T, H, E, st));
+  if (W_router && !(c.flags & MOE_FLAG_EXACT_LOGITS)) {
+    CUtensorMap tX, tW;
+    const int n_pad = ((E + 15) / 16) * 16;
+    if (!make_tmap(&tX, x, H, (uint64_t)T, 128) || !make_tmap(&tW, p->rw.WrT, H, (uint64_t)E, n_pad)) {
+      p->last_launches = nl;
+      return MOE_ERR_CUDA;
+    }
+    MOE_CK(launch_router_tc(tX, tW, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
+                            p->bias, p->rw, T, H, E, k, p->num_sms, router_logits, p->ws.ids, p->ws.w,
+                            p->ws.counts, p->ws.err, c.timeout_ns, st));
+    nl += 3;
+  } else {
+    if (W_router) {
+      MOE_CK(launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
+                                  p->bias, router_logits, T, H, E, st));
+      ++nl;
+    }
+    MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->num_sms, st));
     ++nl;
   }
-  MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->num_sms, st));
-  ++nl;
   rec(1);
   MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, c.schedule, c.wave_experts, c.lead_waves,
                          st));
@@ -398,6 +424,12 @@ moe_status_t moe_trace_read(moe_plan_t p, uint64_t* host_buf, size_t cap, size_t
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(host_buf, p->trace, cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_router_bound(moe_plan_t p, int32_t T, float* cH) {
+  if (!p || !cH || T < 1 || T > p->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  *cH = router_bound_coef(p->cfg.H, router_split(T, p->cfg.H, p->cfg.E, p->num_sms));
   return MOE_OK;
 }
 

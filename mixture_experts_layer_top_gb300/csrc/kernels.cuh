@@ -62,6 +62,34 @@ struct GemmArgs {
 };
 
 cudaError_t router_prepare();
+
+// Tensor-core router with certified exact selection (router_tc.cu).
+constexpr int ROUTER_MAX_SPLITS = 16;   // K splits of the logit estimate
+struct RouterSplit {
+  int m_tiles, splits, kb_total, kb_per;
+  int n_chain;       // TMEM accumulators per CTA, K blocks dealt round-robin
+  int chain_steps;   // 16-deep MMA steps of the longest chain
+};
+struct RouterWs {
+  uint16_t* WrT;    // [E][H] bf16: Wr transposed
+  float* nw_part;   // [H/64][E] partial sums of squares of Wr's columns
+  float* nw;        // [E] upper bounds of the column norms
+  int* done;        // block counter of the transpose kernel (0 between forwards)
+  float* part;      // [splits][T][E] fp32 partial estimates
+};
+// Rows of `part` needed for any T <= T_max (splits * T is at most this).
+inline int64_t router_part_rows(int64_t T_max) {
+  const int64_t tp = (T_max + 127) / 128 * 128;
+  const int64_t split_rows = 32768 < ROUTER_MAX_SPLITS * tp ? 32768 : ROUTER_MAX_SPLITS * tp;
+  return tp > split_rows ? tp : split_rows;
+}
+cudaError_t router_tc_prepare();
+RouterSplit router_split(int T, int H, int E, int num_sms);
+float router_bound_coef(int H, const RouterSplit& r);
+cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const uint16_t* Wr,
+                             const float* bias, const RouterWs& rw, int T, int H, int E, int k, int num_sms,
+                             float* logits, int32_t* ids, float* w, int32_t* counts, uint32_t* err,
+                             int64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
                                  int H, int E, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,

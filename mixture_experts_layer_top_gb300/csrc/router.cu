@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
+#include "routing.cuh"
 
 namespace moe {
 
@@ -161,39 +162,12 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
   }
 }
 
-// Order-preserving key of a logit: higher logit -> larger key; -0 == +0; NaN -> 0
-// (below -inf, whose key is 0x007FFFFF).
-__device__ __forceinline__ uint32_t logit_key(float l) {
-  if (l != l) return 0u;
-  if (l == 0.0f) l = 0.0f;
-  const uint32_t u = __float_as_uint(l);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 constexpr int TK_WARPS = 8;
 constexpr int TK_MAX_TOK_PER_WARP = 8;
 
-// Exact a - b as hi + lo (Knuth's two-sum); lo = 0 when hi is not finite.
-__device__ __forceinline__ float two_diff(float a, float b, float* lo) {
-  const float hi = __fsub_rn(a, b);
-  if (!isfinite(hi)) {
-    *lo = 0.0f;
-    return hi;
-  }
-  const float bb = __fsub_rn(hi, a);
-  *lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(-b, bb));
-  return hi;
-}
-
-// One warp per token (tpw tokens per warp in turn).  Keys combine (logit key,
-// 0xFFFF - expert) so the maximum is the highest logit and, among equal logits,
-// the lowest id.  Weights: softmax over the k selected logits, in fp32 with the
-// argument l_j - l_0 kept exact as a two-term sum (exp(hi + lo) = exp(hi)(1 + lo)
-// to first order, lo <= half an ulp of hi) and the slot-order sum compensated
-// (Neumaier), so each weight is within a few 1e-7 relative of the exactly
-// rounded softmax; fp64 is avoided (its rate on this GPU is a small fraction of
-// fp32).  Expert counts go through a shared-memory histogram, one global atomic
-// per (block, expert).
+// Top-k over caller-given (or canonical) logits: one warp per token, tpw tokens
+// per warp in turn; selection and weights as in routing.cuh.  Expert counts go
+// through a shared-memory histogram, one global atomic per (block, expert).
 __global__ void __launch_bounds__(TK_WARPS * 32)
 topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
             float* __restrict__ w, int32_t* __restrict__ counts, int tpw) {
@@ -210,45 +184,14 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __re
 #pragma unroll
     for (int i = 0; i < MAX_E / 32; ++i) {
       const int e = lane + 32 * i;
-      key[i] = (i < nkey && e < E) ? (((uint64_t)logit_key(l[e]) << 32) | (uint64_t)(0xFFFFu - (uint32_t)e)) : 0ull;
+      key[i] = (i < nkey && e < E) ? select_key(l[e], e) : 0ull;
     }
-    int my_e = 0;
-    float my_l = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      uint64_t best = 0;
-#pragma unroll
-      for (int i = 0; i < MAX_E / 32; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        best = o > best ? o : best;
-      }
-      const int e = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFu));
-#pragma unroll
-      for (int i = 0; i < MAX_E / 32; ++i)
-        if (key[i] == best) key[i] = 0ull;
-      if (lane == j) {
-        my_e = e;
-        my_l = l[e];
-      }
-    }
-    const float m = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-    float lo;
-    const float hi = two_diff(my_l, m, &lo);
-    const float eh = expf(hi);
-    const float ex = (lane < k) ? __fmaf_rn(eh, lo, eh) : 0.0f;
-    float sum = 0.0f, comp = 0.0f;   // Neumaier-compensated sum in slot order
-    for (int j = 0; j < k; ++j) {
-      const float v = __shfl_sync(0xFFFFFFFFu, ex, j);
-      const float s2 = __fadd_rn(sum, v);
-      comp = __fadd_rn(comp, fabsf(sum) >= fabsf(v) ? __fadd_rn(__fsub_rn(sum, s2), v)
-                                                   : __fadd_rn(__fsub_rn(v, s2), sum));
-      sum = s2;
-    }
-    if (isfinite(sum)) sum = __fadd_rn(sum, comp);
+    const int my_e = warp_select_topk(key, k, lane);
+    const float my_l = (lane < k) ? l[my_e] : 0.0f;
+    const float wt = warp_softmax_weight(my_l, k, lane);
     if (lane < k) {
       ids[(size_t)t * k + lane] = my_e;
-      w[(size_t)t * k + lane] = __fdiv_rn(ex, sum);
+      w[(size_t)t * k + lane] = wt;
       atomicAdd(&hist[my_e], 1);
     }
   }

@@ -16,8 +16,11 @@ outputs of a bf16-intermediate computation:
   and one such flip of a large |h| moves an output by ~0.5% of RMS, which is
   >3e-2 relative on the rare output near 0.1 * RMS that the top-k sum cancels.
 
-Routing (logits, ids, counts, offsets, row_pair, row_of) must be bit-exact;
-router weights within 1e-6 relative (the GPU's exp is not the host's)."""
+Routing (ids, counts, offsets, row_pair, row_of) must be bit-exact; router
+weights within 1e-6 relative (the GPU's exp is not the host's).  Logits: with
+MOE_FLAG_EXACT_LOGITS every entry is bit-exact; by default the entries of the
+selected experts are bit-exact and every other entry is either exact or within
+the library's stated bound of the canonical value (check_logits)."""
 from __future__ import annotations
 
 import numpy as np
@@ -96,3 +99,35 @@ def oracle_for(wl: synth.Workload, x_bits: np.ndarray, Wr_bits: np.ndarray, bias
         W2 = lambda e: synth.expert_slice_host(wl, "W2", e)   # noqa: E731
     return oracle.forward(x_bits, Wr_bits, bias, W1, W2, wl.k, act=act, tokens=tokens,
                           want_intermediates=want_intermediates)
+
+
+def logit_bound(x_bits: np.ndarray, Wr_bits: np.ndarray, bias, est: np.ndarray, cH: float) -> np.ndarray:
+    """The library's stated bound on |estimate - canonical logit| per (t, e), in float64:
+    cH ||x_t|| ||Wr[:,e]|| + 2^-20 (|v| + |b|), v = estimate - bias (cH from moe_router_bound)."""
+    x = f64(x_bits)
+    Wr = f64(Wr_bits)
+    nx = np.sqrt((x * x).sum(axis=1))
+    nw = np.sqrt((Wr * Wr).sum(axis=0))
+    b = np.zeros(Wr.shape[1]) if bias is None else np.abs(np.asarray(bias, np.float64))
+    return cH * np.outer(nx, nw) + 2.0 ** -20 * (np.abs(est.astype(np.float64)) + 2 * b[None, :])
+
+
+def check_logits(lg_gpu: np.ndarray, ref: dict, x_bits: np.ndarray, Wr_bits: np.ndarray, cH: float, bias=None,
+                 rows=None) -> dict:
+    """Default router: every selected expert's logit bit-exact, every other entry exact or
+    within logit_bound; the observed estimate error must stay under a quarter of the bound
+    (the bound carries a wide margin over the tensor-core accumulation error)."""
+    ref_l = ref["logits"]
+    ids = ref["ids"]
+    if rows is not None:
+        lg_gpu, ref_l, ids, x_bits = lg_gpu[rows], ref_l[rows], ids[rows], x_bits[rows]
+    sel = np.take_along_axis(lg_gpu, ids, axis=1)
+    assert np.array_equal(sel.view(np.uint32), np.take_along_axis(ref_l, ids, axis=1).view(np.uint32)), \
+        "selected logits not bit-exact"
+    exact = lg_gpu.view(np.uint32) == ref_l.view(np.uint32)
+    d = np.abs(lg_gpu.astype(np.float64) - ref_l.astype(np.float64))
+    bound = logit_bound(x_bits, Wr_bits, bias, lg_gpu, cH)
+    ratio = np.where(exact, 0.0, d / bound)
+    assert np.all(np.isfinite(lg_gpu[~exact])), "non-finite estimate"
+    assert ratio.max() <= 0.25, f"estimate error {ratio.max():.3f} of the stated bound"
+    return dict(exact_frac=float(exact.mean()), max_ratio=float(ratio.max()))
