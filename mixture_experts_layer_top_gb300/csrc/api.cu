@@ -84,7 +84,7 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   return MOE_OK;
 }
 
-constexpr int N_BUFS = 22;
+constexpr int N_BUFS = 20;
 
 struct Layout {
   size_t off[N_BUFS];
@@ -112,9 +112,7 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
       (size_t)c.T_max * c.H * 2,           // x staging (moe_forward_host)
       (size_t)c.T_max * c.H * 2,           // y staging (moe_forward_host)
       (size_t)c.E * c.H * 2,               // router: Wr transposed
-      (size_t)(c.H / 64) * c.E * 4,        // router: column sums of squares per 64 rows
       (size_t)c.E * 4,                     // router: column norm bounds
-      16,                                  // router: transpose block counter
       (size_t)router_part_rows(c.T_max) * c.E * 4,   // router: split-K partial estimates
   };
   Layout L;
@@ -210,12 +208,9 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->x_stage = b + L.off[15];
   p->y_stage = b + L.off[16];
   p->rw.WrT = reinterpret_cast<uint16_t*>(b + L.off[17]);
-  p->rw.nw_part = reinterpret_cast<float*>(b + L.off[18]);
-  p->rw.nw = reinterpret_cast<float*>(b + L.off[19]);
-  p->rw.done = reinterpret_cast<int*>(b + L.off[20]);
-  p->rw.part = reinterpret_cast<float*>(b + L.off[21]);
-  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess || cudaMemset(p->rw.done, 0, 16) != cudaSuccess)
-    return fail(MOE_ERR_CUDA);
+  p->rw.nw = reinterpret_cast<float*>(b + L.off[18]);
+  p->rw.part = reinterpret_cast<float*>(b + L.off[19]);
+  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cfg->router_bias) {
     if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
       cudaGetLastError();

@@ -72,9 +72,7 @@ struct RouterSplit {
 };
 struct RouterWs {
   uint16_t* WrT;    // [E][H] bf16: Wr transposed
-  float* nw_part;   // [H/64][E] partial sums of squares of Wr's columns
   float* nw;        // [E] upper bounds of the column norms
-  int* done;        // block counter of the transpose kernel (0 between forwards)
   float* part;      // [splits][T][E] fp32 partial estimates
 };
 // Rows of `part` needed for any T <= T_max (splits * T is at most this).

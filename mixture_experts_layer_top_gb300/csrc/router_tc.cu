@@ -8,12 +8,13 @@
 // This path gets the same routing from far fewer of them:
 //
 //  1. router_prep_kernel: WrT = Wr^T (expert-major rows, for K-major tensor-core
-//     tiles and coalesced per-expert reads) and an upper bound nw[e] >= ||Wr[:,e]||_2.
+//     tiles and coalesced per-expert reads).
 //  2. router_tc_kernel: estimates L~[t,e] = sum_h x[t,h] Wr[h,e] with tcgen05
 //     (bf16 products are exact in fp32; accumulation in TMEM).  The K blocks are
 //     dealt round-robin to A independent TMEM accumulators (chains) per CTA and K
 //     is split over S CTAs; the epilogue adds its A chains and the S partial sums
-//     are added by the select kernel, both in a fixed order.
+//     are added by the select kernel, both in a fixed order.  Its epilogue warps,
+//     idle during the mainloop, write upper bounds nw[e] >= ||Wr[:,e]||_2.
 //  3. router_select_kernel (one warp per token): nx >= ||x[t,:]||_2 and, for every
 //     expert, a bound d[e] >= |L~[t,e] - L[t,e]| where L is the canonical logit:
 //        d[e] = cH * nx * nw[e] + 2^-20 (|L~[t,e]| + |bias[e]|),
@@ -50,65 +51,20 @@ namespace {
 // ------------------------------------------------------------------ 1. prep
 constexpr int RP_H = 64;    // h rows per block
 
-// grid (ceil(E/32), H/64), 256 threads.  Block (eb, hc) transposes Wr[hc*64.., eb*32..]
-// into WrT and writes the partial sums of squares of its 32 columns; the last
-// block to finish adds the partials of every column in a fixed order.
+// grid (ceil(E/32), H/64), 256 threads: WrT[e0 .. e0+31][h0 .. h0+63] = Wr[h0.., e0..]^T.
 __global__ void __launch_bounds__(256)
-router_prep_kernel(const uint16_t* __restrict__ Wr, int H, int E, uint16_t* __restrict__ WrT,
-                   float* __restrict__ nw_part, float* __restrict__ nw, int* __restrict__ done) {
+router_prep_kernel(const uint16_t* __restrict__ Wr, int H, int E, uint16_t* __restrict__ WrT) {
   __shared__ __align__(16) uint16_t tile[32][RP_H + 8];
-  __shared__ float sq[8][32];
-  __shared__ int is_last;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int e0 = blockIdx.x * 32, h0 = blockIdx.y * RP_H;
   const int e = e0 + tx;
-  float s = 0.0f;
 #pragma unroll
-  for (int r = ty; r < RP_H; r += 8) {
-    const uint16_t v = (e < E) ? Wr[(size_t)(h0 + r) * E + e] : (uint16_t)0;
-    tile[tx][r] = v;
-    const float f = __uint_as_float((uint32_t)v << 16);
-    s = fmaf(f, f, s);
-  }
-  sq[ty][tx] = s;
+  for (int r = ty; r < RP_H; r += 8) tile[tx][r] = (e < E) ? Wr[(size_t)(h0 + r) * E + e] : (uint16_t)0;
   __syncthreads();
-  if (ty == 0 && e < E) {
-    float a = 0.0f;
-    for (int i = 0; i < 8; ++i) a += sq[i][tx];
-    nw_part[(size_t)blockIdx.y * E + e] = a;
-  }
-  {  // thread -> (expert row i, 8-element chunk c) of the transposed tile
-    const int i = threadIdx.x >> 3, c = threadIdx.x & 7;
-    if (e0 + i < E)
-      *reinterpret_cast<uint4*>(WrT + (size_t)(e0 + i) * H + h0 + c * 8) =
-          *reinterpret_cast<const uint4*>(&tile[i][c * 8]);
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(done, 1) == (int)(gridDim.x * gridDim.y) - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // every block's partials are visible: ||w_e||^2 in a fixed order (warp ty adds the
-  // partial rows c = ty (mod 8), then the 8 warp sums in order), rounded up by more
-  // than the relative error of the H additions and of the square root
-  __shared__ float red[8][MAX_E];
-  const int ny = (int)gridDim.y;
-  for (int g = 0; g * 32 < E; ++g) {
-    const int j = g * 32 + tx;
-    float a = 0.0f;
-#pragma unroll 4
-    for (int c = ty; c < ny; c += 8) a += (j < E) ? __ldcg(nw_part + (size_t)c * E + j) : 0.0f;
-    red[ty][j] = a;
-  }
-  __syncthreads();
-  const float up = 1.0f + (float)H * 0x1p-21f;
-  for (int j = threadIdx.x; j < E; j += blockDim.x) {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a += red[i][j];
-    nw[j] = sqrtf(a) * up;
-  }
+  const int i = threadIdx.x >> 3, c = threadIdx.x & 7;   // expert row i, 8-element chunk c
+  if (e0 + i < E)
+    *reinterpret_cast<uint4*>(WrT + (size_t)(e0 + i) * H + h0 + c * 8) =
+        *reinterpret_cast<const uint4*>(&tile[i][c * 8]);
 }
 
 // ------------------------------------------------------------------ 2. tensor-core estimate
@@ -140,9 +96,10 @@ static_assert(RTC_SMEM <= 232448, "shared memory per CTA exceeded");
 // The epilogue warps (one token row per thread) add the chains in order and write
 // part[s][t][e].
 __global__ void __launch_bounds__(RTC_THREADS, 1)
-router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, int T, int E,
-                 int n_pad, int kb_total, int kb_per, int n_chain, float* __restrict__ part,
-                 uint32_t* __restrict__ err, int64_t tmo) {
+router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                 const uint16_t* __restrict__ WrT, int T, int H, int E, int n_pad, int kb_total, int kb_per,
+                 int n_chain, float* __restrict__ part, float* __restrict__ nw, uint32_t* __restrict__ err,
+                 int64_t tmo) {
   extern __shared__ uint8_t rtc_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rtc_raw) + 1023) & ~(uintptr_t)1023);
   RtcCtl* ctl = reinterpret_cast<RtcCtl*>(smem + RTC_CTL_OFF);
@@ -230,6 +187,31 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     __syncwarp();
   } else {
     const int q = warp & 3;
+    {
+      // while the mainloop runs: nw[e] >= ||Wr[:,e]||_2 for experts e = cta + n_cta * (q + 4 i),
+      // one warp per expert (lane-strided sums of squares, then the xor tree), rounded up by
+      // more than the relative error of the additions and of the square root
+      const int n_cta = (int)(gridDim.x * gridDim.y), cta = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+      const float up = 1.0f + (float)H * 0x1p-21f;
+      for (int e = cta + n_cta * (warp - 2); e < E; e += 4 * n_cta) {
+        const uint16_t* wr = WrT + (size_t)e * H;
+        float ss = 0.0f;
+#pragma unroll 4
+        for (int h = lane * 8; h < H; h += 256) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(wr + h));
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(u[j] << 16), hi = __uint_as_float(u[j] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+          }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+        if (lane == 0) nw[e] = sqrtf(ss) * up;
+      }
+    }
     const bool ok = ptx::mbar_wait(&ctl->acc, 0, tmo, abort_flag);
     if (!ok) {
       atomicOr(err, ERR_TIMEOUT);
@@ -345,7 +327,7 @@ __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, 
 // owning token w: (1) bounds and candidates per token; (2) the block's warps
 // evaluate every (token, candidate) pair together, 8 pairs per warp at a time;
 // (3) each warp selects its token's top-k on the exact values.  E <= 256.
-__global__ void __launch_bounds__(SEL_WARPS * 32)
+__global__ void __launch_bounds__(SEL_WARPS * 32, 4)
 router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ WrT, const float* __restrict__ part,
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
                      float cH, int ntok, float* __restrict__ logits, int32_t* __restrict__ ids,
@@ -508,15 +490,12 @@ cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
                              float* logits, int32_t* ids, float* w, int32_t* counts, uint32_t* err,
                              int64_t timeout_ns, cudaStream_t st) {
   const RouterSplit sp = router_split(T, H, E, num_sms);
-  // the transpose kernel's last-block counter starts every forward at zero
-  cudaError_t e = cudaMemsetAsync(rw.done, 0, sizeof(int), st);
-  if (e != cudaSuccess) return e;
-  router_prep_kernel<<<dim3((E + 31) / 32, H / RP_H), 256, 0, st>>>(Wr, H, E, rw.WrT, rw.nw_part, rw.nw, rw.done);
-  e = cudaGetLastError();
+  router_prep_kernel<<<dim3((E + 31) / 32, H / RP_H), 256, 0, st>>>(Wr, H, E, rw.WrT);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n_pad = ((E + 15) / 16) * 16;
   router_tc_kernel<<<dim3(sp.m_tiles, sp.splits), RTC_THREADS, RTC_SMEM, st>>>(
-      tmX, tmW, T, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, err, timeout_ns);
+      tmX, tmW, rw.WrT, T, H, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, rw.nw, err, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // tokens per block: SEL_WARPS, or fewer when T is small so that every SM gets a block
