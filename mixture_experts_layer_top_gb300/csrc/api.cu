@@ -84,7 +84,11 @@ moe_status_t validate_cfg(const moe_config_t* c) {
   return MOE_OK;
 }
 
-constexpr int N_BUFS = 20;
+// Sub-buffers of the plan workspace (one allocation), by name.
+enum Buf {
+  B_IDS, B_W, B_COUNTS, B_OFFSETS, B_ROW_PAIR, B_ROW_OF, B_PROW_OF, B_PROW_W, B_X_PAD, B_H_PAD, B_P_PAD, B_S_PAD,
+  B_TILES, B_SCHED, B_READY, B_ERR, B_X_STAGE, B_Y_STAGE, B_WRT, B_NW, B_PART, N_BUFS
+};
 
 struct Layout {
   size_t off[N_BUFS];
@@ -93,28 +97,28 @@ struct Layout {
 
 Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_tiles) {
   const int64_t Rp = max_mt * UNIT_ROWS;   // padded rows
-  const size_t sizes[N_BUFS] = {
-      (size_t)R * 4,                       // ids
-      (size_t)R * 4,                       // w
-      (size_t)c.E * 4,                     // counts
-      (size_t)(c.E + 1) * 4,               // offsets
-      (size_t)R * 4,                       // row_pair
-      (size_t)R * 4,                       // row_of
-      (size_t)R * 4,                       // prow_of
-      (size_t)Rp * 4,                      // prow_w
-      (size_t)Rp * c.H * 2,                // x_pad
-      (size_t)Rp * c.I * 2,                // h_pad
-      (size_t)Rp * c.H * 4,                // P_pad
-      (size_t)max_tiles * 16,              // tiles
-      16,                                  // sched
-      (size_t)max_mt * 4,                  // ready
-      16,                                  // err
-      (size_t)c.T_max * c.H * 2,           // x staging (moe_forward_host)
-      (size_t)c.T_max * c.H * 2,           // y staging (moe_forward_host)
-      (size_t)c.E * c.H * 2,               // router: Wr transposed
-      (size_t)c.E * 4,                     // router: column norm bounds
-      (size_t)router_part_rows(c.T_max) * c.E * 4,   // router: split-K partial estimates
-  };
+  size_t sizes[N_BUFS] = {};
+  sizes[B_IDS] = (size_t)R * 4;
+  sizes[B_W] = (size_t)R * 4;
+  sizes[B_COUNTS] = (size_t)c.E * 4;
+  sizes[B_OFFSETS] = (size_t)(c.E + 1) * 4;
+  sizes[B_ROW_PAIR] = (size_t)R * 4;
+  sizes[B_ROW_OF] = (size_t)R * 4;
+  sizes[B_PROW_OF] = (size_t)R * 4;
+  sizes[B_PROW_W] = (size_t)Rp * 4;
+  sizes[B_X_PAD] = (size_t)Rp * c.H * 2;
+  sizes[B_H_PAD] = (size_t)Rp * c.I * 2;
+  sizes[B_P_PAD] = (size_t)Rp * c.H * 2;                 // fp16
+  sizes[B_S_PAD] = (size_t)Rp * (c.H / L2_COLS) * 4;     // per-(row, 256 columns) scale of P_pad
+  sizes[B_TILES] = (size_t)max_tiles * 16;
+  sizes[B_SCHED] = 16;
+  sizes[B_READY] = (size_t)max_mt * 4;
+  sizes[B_ERR] = 16;
+  sizes[B_X_STAGE] = (size_t)c.T_max * c.H * 2;          // moe_forward_host staging
+  sizes[B_Y_STAGE] = (size_t)c.T_max * c.H * 2;
+  sizes[B_WRT] = (size_t)c.E * c.H * 2;                  // router: Wr transposed
+  sizes[B_NW] = (size_t)c.E * 4;                         // router: column norm bounds
+  sizes[B_PART] = (size_t)router_part_rows(c.T_max) * c.E * 4;   // router: split-K partial estimates
   Layout L;
   size_t o = 0;
   for (int i = 0; i < N_BUFS; ++i) {
@@ -190,26 +194,28 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
     return fail(MOE_ERR_OOM);
   }
   char* b = static_cast<char*>(p->base);
-  p->ws.ids = reinterpret_cast<int32_t*>(b + L.off[0]);
-  p->ws.w = reinterpret_cast<float*>(b + L.off[1]);
-  p->ws.counts = reinterpret_cast<int32_t*>(b + L.off[2]);
-  p->ws.offsets = reinterpret_cast<int32_t*>(b + L.off[3]);
-  p->ws.row_pair = reinterpret_cast<int32_t*>(b + L.off[4]);
-  p->ws.row_of = reinterpret_cast<int32_t*>(b + L.off[5]);
-  p->ws.prow_of = reinterpret_cast<int32_t*>(b + L.off[6]);
-  p->ws.prow_w = reinterpret_cast<float*>(b + L.off[7]);
-  p->ws.x_pad = reinterpret_cast<uint16_t*>(b + L.off[8]);
-  p->ws.h_pad = reinterpret_cast<uint16_t*>(b + L.off[9]);
-  p->ws.P_pad = reinterpret_cast<float*>(b + L.off[10]);
-  p->ws.tiles = reinterpret_cast<int32_t*>(b + L.off[11]);
-  p->ws.sched = reinterpret_cast<int32_t*>(b + L.off[12]);
-  p->ws.ready = reinterpret_cast<int32_t*>(b + L.off[13]);
-  p->ws.err = reinterpret_cast<uint32_t*>(b + L.off[14]);
-  p->x_stage = b + L.off[15];
-  p->y_stage = b + L.off[16];
-  p->rw.WrT = reinterpret_cast<uint16_t*>(b + L.off[17]);
-  p->rw.nw = reinterpret_cast<float*>(b + L.off[18]);
-  p->rw.part = reinterpret_cast<float*>(b + L.off[19]);
+  auto at = [&](Buf i) { return b + L.off[i]; };
+  p->ws.ids = reinterpret_cast<int32_t*>(at(B_IDS));
+  p->ws.w = reinterpret_cast<float*>(at(B_W));
+  p->ws.counts = reinterpret_cast<int32_t*>(at(B_COUNTS));
+  p->ws.offsets = reinterpret_cast<int32_t*>(at(B_OFFSETS));
+  p->ws.row_pair = reinterpret_cast<int32_t*>(at(B_ROW_PAIR));
+  p->ws.row_of = reinterpret_cast<int32_t*>(at(B_ROW_OF));
+  p->ws.prow_of = reinterpret_cast<int32_t*>(at(B_PROW_OF));
+  p->ws.prow_w = reinterpret_cast<float*>(at(B_PROW_W));
+  p->ws.x_pad = reinterpret_cast<uint16_t*>(at(B_X_PAD));
+  p->ws.h_pad = reinterpret_cast<uint16_t*>(at(B_H_PAD));
+  p->ws.P_pad = reinterpret_cast<uint16_t*>(at(B_P_PAD));
+  p->ws.S_pad = reinterpret_cast<float*>(at(B_S_PAD));
+  p->ws.tiles = reinterpret_cast<int32_t*>(at(B_TILES));
+  p->ws.sched = reinterpret_cast<int32_t*>(at(B_SCHED));
+  p->ws.ready = reinterpret_cast<int32_t*>(at(B_READY));
+  p->ws.err = reinterpret_cast<uint32_t*>(at(B_ERR));
+  p->x_stage = at(B_X_STAGE);
+  p->y_stage = at(B_Y_STAGE);
+  p->rw.WrT = reinterpret_cast<uint16_t*>(at(B_WRT));
+  p->rw.nw = reinterpret_cast<float*>(at(B_NW));
+  p->rw.part = reinterpret_cast<float*>(at(B_PART));
   if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cfg->router_bias) {
     if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
@@ -301,7 +307,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   const uint64_t Rp = (uint64_t)p->R_pad_max;
   if (!make_tmap(&tA1, p->ws.x_pad, H, Rp, BM) || !make_tmap(&tB1, W1, 2 * I, (uint64_t)E * H, BK) ||
       !make_tmap(&tA2, p->ws.h_pad, I, Rp, BM) || !make_tmap(&tB2, W2, H, (uint64_t)E * I, BK) ||
-      !make_tmap(&tH, p->ws.h_pad, I, Rp, 32) || !make_tmap(&tP, p->ws.P_pad, H, Rp, 32, true)) {
+      !make_tmap(&tH, p->ws.h_pad, I, Rp, 32) || !make_tmap(&tP, p->ws.P_pad, H, Rp, 32)) {
     p->last_launches = nl;
     return MOE_ERR_CUDA;
   }
@@ -312,6 +318,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.prow_w = p->ws.prow_w;
   ga.h_pad = p->ws.h_pad;
   ga.P_pad = p->ws.P_pad;
+  ga.S_pad = p->ws.S_pad;
   ga.ready = p->ws.ready;
   ga.err = p->ws.err;
   ga.trace = p->trace;
@@ -322,6 +329,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   ga.E = E;
   ga.R_pad = (int)p->R_pad_max;
   ga.nL1 = I / L1_COLS;
+  ga.nL2 = H / L2_COLS;
   ga.flags = c.flags;
   ga.timeout_ns = c.timeout_ns;
   const bool streaming = !(c.flags & MOE_FLAG_GEMM_COMPUTE);   // the deeper operand ring by default
@@ -337,7 +345,8 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
     ++nl;
   }
   rec(4);
-  MOE_CK(launch_combine(p->ws.P_pad, p->ws.prow_of, T, H, k, static_cast<uint16_t*>(y), p->num_sms, st));
+  MOE_CK(launch_combine(p->ws.P_pad, p->ws.S_pad, p->ws.prow_of, T, H, k, static_cast<uint16_t*>(y), p->num_sms,
+                        st));
   ++nl;
   rec(5);
 #undef MOE_CK
@@ -396,7 +405,7 @@ moe_status_t moe_debug_intermediates(moe_plan_t p, int32_t T, void* h, float* P,
   const size_t R = (size_t)T * p->cfg.top_k;
   if (R && (h || P) &&
       launch_compact_intermediates(p->ws.row_pair, p->ws.prow_of, (int)R, p->cfg.H, p->cfg.I, p->ws.h_pad,
-                                   p->ws.P_pad, static_cast<uint16_t*>(h), P, st) != cudaSuccess)
+                                   p->ws.P_pad, p->ws.S_pad, static_cast<uint16_t*>(h), P, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

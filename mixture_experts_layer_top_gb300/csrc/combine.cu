@@ -1,9 +1,12 @@
 // Combine on one GPU: y[t,:] = bf16( sum_{j=0..k-1} P[row(t,j), :] ), the fp32
 // sum taken in slot order j = 0, 1, ..., k-1 so the result does not depend on
-// which expert finished first.  P already holds w[t,j] * (expert output), so
-// this is the X-Stage paper's MegaMoE-background Combine ("aggregates the
-// top-k results using the router weights") with the weights applied upstream.
+// which expert finished first.  P is stored as fp16 with a power-of-two scale per
+// (row, 256 columns); each term is widened and rescaled exactly before the sum.
+// P already holds w[t,j] * (expert output): this is the Combine of the X-Stage
+// paper's MegaMoE paragraph (introduction) - the router-weighted sum of a
+// token's top-k expert outputs - with the weights applied upstream.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -11,43 +14,57 @@ namespace moe {
 
 namespace {
 
-// One thread per 4 consecutive outputs: k float4 loads from the slots' rows of P
-// (padded row space, found through prow_of), fixed-order fp32 sum, 8-byte store.
+// One thread per 8 consecutive outputs: k 16-byte loads of fp16 P from the slots'
+// rows (padded row space, found through prow_of), each widened and multiplied by
+// its block's power-of-two scale (exact), fixed-order fp32 sum, 16-byte store.
 __global__ void __launch_bounds__(256)
-combine_kernel(const float* __restrict__ P_pad, const int32_t* __restrict__ prow_of, int T, int H, int k,
-               uint16_t* __restrict__ y) {
-  const int64_t n4 = (int64_t)T * H / 4;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = (i * 4) / H;
-    const int64_t c = (i * 4) % H;
+combine_kernel(const uint16_t* __restrict__ P_pad, const float* __restrict__ S_pad, const int32_t* __restrict__ prow_of,
+               int T, int H, int k, uint16_t* __restrict__ y) {
+  const int64_t n8 = (int64_t)T * H / 8;
+  const int nS = H / L2_COLS;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = (i * 8) / H;
+    const int64_t c = (i * 8) % H;
     const int32_t* pr = prow_of + t * k;
-    float4 s = __ldcs(reinterpret_cast<const float4*>(P_pad + (int64_t)pr[0] * H + c));
-    for (int j = 1; j < k; ++j) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(P_pad + (int64_t)pr[j] * H + c));
-      s.x = s.x + v.x;
-      s.y = s.y + v.y;
-      s.z = s.z + v.z;
-      s.w = s.w + v.w;
+    float s[8];
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = pr[j];
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(P_pad + row * H + c));
+      const float sc = S_pad[row * nS + c / L2_COLS];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
+        const float a = f.x * sc, b = f.y * sc;
+        if (j == 0) {
+          s[2 * q] = a;
+          s[2 * q + 1] = b;
+        } else {
+          s[2 * q] = s[2 * q] + a;
+          s[2 * q + 1] = s[2 * q + 1] + b;
+        }
+      }
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(s.z, s.w);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t*>(&lo);
-    o.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(y + t * H + c) = o;
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(s[2 * q], s[2 * q + 1]);
+      o[q] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(y + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const float* P_pad, const int32_t* prow_of, int T, int H, int k, uint16_t* y, int sms,
-                           cudaStream_t st) {
-  const int64_t n4 = (int64_t)T * H / 4;
-  int64_t blocks = (n4 + 255) / 256;
+cudaError_t launch_combine(const uint16_t* P_pad, const float* S_pad, const int32_t* prow_of, int T, int H, int k,
+                           uint16_t* y, int sms, cudaStream_t st) {
+  const int64_t n8 = (int64_t)T * H / 8;
+  int64_t blocks = (n8 + 255) / 256;
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<(int)blocks, 256, 0, st>>>(P_pad, prow_of, T, H, k, y);
+  combine_kernel<<<(int)blocks, 256, 0, st>>>(P_pad, S_pad, prow_of, T, H, k, y);
   return cudaGetLastError();
 }
 

@@ -2,11 +2,12 @@
 // expert-contiguous rows, the tile schedule of the grouped GEMMs, and the row
 // gather x_pad[padded row] = x[token(row)].
 //
-// In the X-Stage paper's MegaMoE background, Dispatch "first sends each token
-// to its destination" expert; with every expert on this GPU that becomes a
-// permutation: rows of expert e occupy offsets[e] .. offsets[e+1]-1, in
+// In the X-Stage paper's MegaMoE paragraph (introduction), Dispatch moves every
+// token to the rank that holds each of its experts; with every expert on this
+// GPU that becomes a permutation: rows of expert e occupy offsets[e] .. offsets[e+1]-1, in
 // ascending token order (each token routes to an expert at most once).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -156,11 +157,12 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ r
   for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
 }
 
-// Debug copy of the intermediates into caller order: h[compact row] and P[t*k+j].
+// Debug copy of the intermediates into caller order: h[compact row] and P[t*k+j]
+// (P as fp32: the stored fp16 value times its block's power-of-two scale, exact).
 __global__ void __launch_bounds__(256)
 compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t* __restrict__ prow_of, int R,
-                             int H, int I, const uint16_t* __restrict__ h_pad, const float* __restrict__ P_pad,
-                             uint16_t* __restrict__ h, float* __restrict__ P) {
+                             int H, int I, const uint16_t* __restrict__ h_pad, const uint16_t* __restrict__ P_pad,
+                             const float* __restrict__ S_pad, uint16_t* __restrict__ h, float* __restrict__ P) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
@@ -170,8 +172,8 @@ compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t
     for (int i = lane; i < I / 8; i += 32)
       reinterpret_cast<uint4*>(h + (size_t)row * I)[i] = reinterpret_cast<const uint4*>(h_pad + pr * I)[i];
   if (P)
-    for (int i = lane; i < H / 4; i += 32)
-      reinterpret_cast<float4*>(P + (size_t)f * H)[i] = reinterpret_cast<const float4*>(P_pad + pr * H)[i];
+    for (int c = lane; c < H; c += 32)
+      P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * (H / L2_COLS) + c / L2_COLS];
 }
 
 }  // namespace
@@ -191,9 +193,9 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, const int3
 }
 
 cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,
-                                         const uint16_t* h_pad, const float* P_pad, uint16_t* h, float* P,
-                                         cudaStream_t st) {
-  compact_intermediates_kernel<<<(R + 7) / 8, 256, 0, st>>>(row_pair, prow_of, R, H, I, h_pad, P_pad, h, P);
+                                         const uint16_t* h_pad, const uint16_t* P_pad, const float* S_pad,
+                                         uint16_t* h, float* P, cudaStream_t st) {
+  compact_intermediates_kernel<<<(R + 7) / 8, 256, 0, st>>>(row_pair, prow_of, R, H, I, h_pad, P_pad, S_pad, h, P);
   return cudaGetLastError();
 }
 

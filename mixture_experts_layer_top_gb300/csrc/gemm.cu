@@ -4,7 +4,10 @@
 //   of x_perm times W1[e][:, 128 n .. +128] (gate) and W1[e][:, I + 128 n .. +128]
 //   (up): one M=256 x N=256 tcgen05 accumulator; epilogue h = bf16(silu(g) * u).
 // Linear-2 tile (phase 1): the same rows of h times W2[e][:, 256 n .. +256];
-//   epilogue P[t*k + j] = w[t,j] * acc (fp32), the router-weight scale.
+//   epilogue P = w[t,j] * acc, the router-weight scale, stored as fp16 times an
+//   exact power-of-two scale per (row, 256-column block): the scale puts the
+//   block's largest finite |P| in [2^14, 2^15], so nothing overflows and every
+//   value keeps fp16's 11 significant bits.
 // (X-Stage paper, MegaMoE background: Linear-1 projects hidden to
 // intermediate, SwiGLU is applied, Linear-2 projects back; the kernel design -
 // persistent, warp-specialised, TMA producer, tensor-core issuer, epilogue
@@ -38,7 +41,7 @@
 // per 32-row quadrant (one epilogue warp pair): a quadrant whose rows are all
 // valid is staged in shared memory in the 128-byte swizzled layout
 // (conflict-free row writes) and written by a bulk tensor store (h: bf16 32 x 64
-// boxes for Linear-1; P: fp32 32 x 32 boxes in four 64-column passes for
+// boxes for Linear-1; P: fp16 32 x 64 boxes in two 128-column passes for
 // Linear-2); the valid rows of a partial quadrant are stored directly; empty
 // quadrants write nothing.  NBUF 32 KB staging buffers rotate, each reused
 // only after its previous store group has read it.  Linear-1 readiness is
@@ -57,6 +60,7 @@
 //     descriptor LBO = 8 KB (next 64 columns), SBO = 1024 B (next 8 K-rows),
 //     K step of 16 rows = +2048 B.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -77,7 +81,7 @@ constexpr int STG_BOX_BYTES = BM * 128;                // 128 staged rows x 128 
 constexpr int ST_ROWS = 32;                            // rows per output store box (one TMEM quadrant)
 constexpr int ST_BOX_BYTES = ST_ROWS * 128;            // 4 KB
 constexpr int STG_BYTES = 2 * STG_BOX_BYTES;           // one staging buffer: two boxes (the two column halves)
-constexpr int CTL_BYTES = 512;
+constexpr int CTL_BYTES = 1536;
 // Shared-memory layout of a <NST stages, NBUF staging buffers> instance.
 template <int NST, int NBUF>
 struct Layout {
@@ -98,6 +102,7 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   int ep_ok[2];             // epilogue go/stop decision of the waiting thread, by tile parity
+  float rmax[2][BM];        // Linear-2 epilogue: largest finite |acc| of each row, per column half
 };
 static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block exceeds its shared-memory reservation");
 
@@ -373,32 +378,75 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         }
         ++sb;
       } else {
-        // P = w * acc, four passes of 64 columns; warp half ch takes columns [64 p + 32 ch, +32)
+        // P = w * acc.  Sweep 1: the largest finite |acc| of the row (this thread's 128
+        // columns, then the other column half's through shared memory) sets the row's
+        // scale 2^se; sweep 2: two passes of 128 columns, warp half ch taking columns
+        // [128 p + 64 ch, +64), each value fp16(fl(w * acc) * 2^-se).
         const float wgt = (staged || direct) ? args.prow_w[prow0 + r] : 0.0f;
-        float* prow = args.P_pad + (size_t)(prow0 + r) * args.H + nb * L2_COLS + ch * 32;
+        float amax = 0.0f;
 #pragma unroll 1
-        for (int pass = 0; pass < MMA_N / 64; ++pass) {
-          acquire_stage();
-          uint8_t* box = stg + (sb % NBUF) * STG_BYTES + ch * STG_BOX_BYTES;
+        for (int c4 = 0; c4 < MMA_N / 64; ++c4) {
           uint32_t v[32];
-          ptx::tmem_ld32(taddr + pass * 64 + ch * 32, v);
+          ptx::tmem_ld32(taddr + c4 * 64 + ch * 32, v);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 f4 = make_float4(wgt * __uint_as_float(v[4 * j]), wgt * __uint_as_float(v[4 * j + 1]),
-                                          wgt * __uint_as_float(v[4 * j + 2]), wgt * __uint_as_float(v[4 * j + 3]));
-            if (staged) *reinterpret_cast<float4*>(box + chunk_off(j)) = f4;
-            else if (direct) reinterpret_cast<float4*>(prow + pass * 64)[j] = f4;
+          for (int j = 0; j < 32; ++j) {
+            const float a = fabsf(__uint_as_float(v[j]));
+            amax = (a < INFINITY) ? fmaxf(amax, a) : amax;   // finite values only (NaN compares false)
           }
-          if (pass == MMA_N / 64 - 1) ptx::tc_fence_before();
+        }
+        ctl->rmax[ch][r] = amax;
+        ptx::named_bar_sync(1, EPI_THREADS);
+        amax = fmaxf(ctl->rmax[0][r], ctl->rmax[1][r]);
+        // M >= every finite |fl(w * acc)| of the row; se = ceil(log2 M) - 15
+        const float M = amax * fabsf(wgt) * (1.0f + 0x1p-20f);
+        int se = 0;
+        if (M > 0.0f) {
+          int cl2 = 128;                              // M rounded up past the largest float
+          if (M < INFINITY) {
+            const uint32_t mb = __float_as_uint(M);
+            const int ex = (int)((mb >> 23) & 0xFFu);
+            cl2 = (ex == 0) ? -126 : ex - 127 + ((mb & 0x7FFFFFu) ? 1 : 0);
+          }
+          se = max(-126, min(127, cl2 - 15));
+        }
+        const float inv = __uint_as_float((uint32_t)(127 - se) << 23);   // 2^-se, exact
+        if ((staged || direct) && ch == 0)
+          args.S_pad[(size_t)(prow0 + r) * args.nL2 + nb] = __uint_as_float((uint32_t)(127 + se) << 23);
+        uint16_t* prow = args.P_pad + (size_t)(prow0 + r) * args.H + nb * L2_COLS + ch * 64;
+#pragma unroll 1
+        for (int pass = 0; pass < MMA_N / 128; ++pass) {
+          acquire_stage();
+          uint8_t* box = stg + (sb % NBUF) * STG_BYTES + ch * STG_BOX_BYTES;
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld32(taddr + pass * 128 + ch * 64 + c * 32, v);
+            ptx::tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float p0 = (wgt * __uint_as_float(v[2 * j])) * inv;
+              const float p1 = (wgt * __uint_as_float(v[2 * j + 1])) * inv;
+              __half2 hv = __floats2half2_rn(p0, p1);
+              pk[j] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v4 = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              if (staged) *reinterpret_cast<uint4*>(box + chunk_off(4 * c + j)) = v4;
+              else if (direct) reinterpret_cast<uint4*>(prow + pass * 128)[4 * c + j] = v4;
+            }
+          }
+          if (pass == MMA_N / 128 - 1) ptx::tc_fence_before();
           ptx::fence_proxy_async_smem();
           ptx::named_bar_sync(1, EPI_THREADS);
           if (ep_tid == 0) {
-            if (pass == MMA_N / 64 - 1) ptx::mbar_arrive_cluster(tempty_addr);
+            if (pass == MMA_N / 128 - 1) ptx::mbar_arrive_cluster(tempty_addr);
             uint8_t* buf = stg + (sb % NBUF) * STG_BYTES;
             for (int gq = 0; gq < nfull; ++gq) {
-              ptx::tma_store_2d(&tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64, prow0 + gq * ST_ROWS);
-              ptx::tma_store_2d(&tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64 + 32,
+              ptx::tma_store_2d(&tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 128, prow0 + gq * ST_ROWS);
+              ptx::tma_store_2d(&tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 128 + 64,
                                 prow0 + gq * ST_ROWS);
             }
             ptx::bulk_commit();                      // one group per pass, possibly empty

@@ -24,7 +24,8 @@ struct Workspace {
   float* prow_w;      // [R_pad_max] router weight of each padded row (valid rows only)
   uint16_t* x_pad;    // [R_pad_max, H] bf16
   uint16_t* h_pad;    // [R_pad_max, I] bf16
-  float* P_pad;       // [R_pad_max, H] fp32: w[t,j] * expert output
+  uint16_t* P_pad;    // [R_pad_max, H] fp16: w[t,j] * expert output / S_pad
+  float* S_pad;       // [R_pad_max, H/256] fp32 powers of two: scale of each 256-column block of P_pad
   int32_t* tiles;     // [max_tiles*4]
   int32_t* sched;     // [4]: linear-1 tiles, total tiles, units
   int32_t* ready;     // [max_units]
@@ -51,12 +52,13 @@ struct GemmArgs {
   const int32_t* counts;
   const float* prow_w;
   uint16_t* h_pad;     // direct stores of partial quadrants
-  float* P_pad;
+  uint16_t* P_pad;    // fp16
+  float* S_pad;
   int32_t* ready;
   uint32_t* err;
   unsigned long long* trace;
   int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all
-  int H, I, E, R_pad, nL1;
+  int H, I, E, R_pad, nL1, nL2;
   uint32_t flags;
   int64_t timeout_ns;
 };
@@ -97,13 +99,15 @@ cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int
 cudaError_t launch_gather(const uint16_t* x, const int32_t* row_pair, const int32_t* prow_of, int R, int H, int k,
                           uint16_t* x_pad, cudaStream_t st);
 cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,
-                                         const uint16_t* h_pad, const float* P_pad, uint16_t* h, float* P,
+                                         const uint16_t* h_pad, const uint16_t* P_pad, const float* S_pad,
+                                         uint16_t* h, float* P,
                                          cudaStream_t st);
 cudaError_t gemm_prepare(int device, int* grid);   // grid: CTAs of the co-resident 2-CTA clusters
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
                                 const GemmArgs& a, int grid, bool streaming, cudaStream_t st);
-cudaError_t launch_combine(const float* P_pad, const int32_t* prow_of, int T, int H, int k, uint16_t* y, int num_sms,
+cudaError_t launch_combine(const uint16_t* P_pad, const float* S_pad, const int32_t* prow_of, int T, int H, int k,
+                           uint16_t* y, int num_sms,
                            cudaStream_t st);
 
 }  // namespace moe

@@ -1,9 +1,9 @@
 // Router: logits in the canonical fp32 order, then top-k selection with
 // softmax weights, and the per-expert row histogram.
 //
-// The layer is the MoE layer of the X-Stage paper's MegaMoE background
-// paragraph: "a router selects one or more experts for each token" and
-// Combine weights the top-k results by "the router weights".  The selection
+// The layer is the MoE layer of the X-Stage paper's MegaMoE paragraph
+// (introduction): each token is routed to its top-k experts, and Combine weights
+// their outputs by the router's weights for that token.  The selection
 // is a discrete decision, so the logits must be bitwise identical to an
 // independent CPU evaluation; the library fixes one summation order:
 //   partial j (j = 0..31) accumulates h = j, j+32, ... with fmaf in ascending h,

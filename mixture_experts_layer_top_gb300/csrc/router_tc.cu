@@ -1,7 +1,7 @@
 // Router on the tensor cores with a certified, exact top-k.
 //
-// The MoE layer of the X-Stage paper's MegaMoE background paragraph routes each
-// token to "one or more experts" chosen by a router; the selection is discrete,
+// The MoE layer of the X-Stage paper's MegaMoE paragraph (introduction) sends
+// each token to the experts its router picks; that choice is discrete,
 // so this library fixes one canonical fp32 order for the logits (lane-strided
 // partial sums, then a pairwise tree; router.cu) and routes on exactly those
 // values.  Evaluating every logit that way costs T*H*E FMAs on the CUDA cores.

@@ -103,6 +103,23 @@ def test_bilinear_integer_exact():
     assert np.array_equal(f64(bits(y)), f64(ref["y"])), "y not bit-exact on integer inputs"
 
 
+@pytest.mark.parametrize("exp2", [20, -30])
+def test_expert_outputs_far_outside_fp16_range(exp2):
+    """P is stored as fp16 times a power-of-two scale per (row, 256 columns): W2 scaled by
+    2^20 (|P| far above 65504) or 2^-30 (|P| far below fp16's normal range) must give the
+    oracle's y within the usual tolerance, with no overflow to inf and no flush to zero."""
+    wl = synth.Workload("range", 512, 512, 256, 8, 2)
+    h = synth.host_inputs(wl)
+    W2 = oracle.f32_to_bf16(oracle.bf16_to_f32(h["W2"]) * np.float32(2.0 ** exp2))   # exact
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], W2))
+    layer = _layer(wl)
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    y, _ = layer.forward(d["x"], d["Wr"], d["W1"], from_bits(W2), check=True)
+    yr = f64(ref["y"])
+    assert np.abs(yr).max() > (1e6 if exp2 > 0 else 0) and np.abs(yr).max() < (np.inf if exp2 > 0 else 1e-6)
+    check_y(bits(y), ref["y"])
+
+
 def test_schedules_bitwise_identical():
     """Every tile schedule and both shared-memory splits of the grouped GEMM give the same bits
     (the default streaming split and the forced compute split)."""
