@@ -212,6 +212,13 @@ MOE_API moe_status_t moe_dispatch_static(int32_t T, int32_t E, int32_t k, const 
                                  int32_t* offsets, int32_t* row_pair, int32_t* row_of, float* row_w,
                                  void* stream);
 
+/* The tile list the last forward's Dispatch built on the device (synchronises `stream`):
+ * n_out[3] = {linear-1 tiles, total tiles, tile workers (2-CTA clusters) it was built for};
+ * up to cap tiles are copied to HOST memory tiles_out (4 ints each, as moe_schedule_host), which
+ * may be NULL to query the counts.  MOE_ERR_INVALID_ARG if cap is smaller than the total. */
+MOE_API moe_status_t moe_debug_schedule(moe_plan_t plan, int32_t* tiles_out, int64_t cap, int64_t* n_out,
+                                void* stream);
+
 /* Host-side evaluation of the tile schedule the device builds (for tests; no GPU needed).
  * counts[E] rows per expert; num_sms = number of tile workers (2-CTA clusters on the GPU);
  * a unit is a pair of 128-row m-tiles of one expert.  Writes up to cap tiles as 4 ints each

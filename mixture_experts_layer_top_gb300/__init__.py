@@ -50,7 +50,7 @@ EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host"
             "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
             "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read",
-            "moe_router_bound")
+            "moe_router_bound", "moe_debug_schedule")
 
 
 class MoEError(RuntimeError):
@@ -96,6 +96,7 @@ def load() -> ctypes.CDLL:
     L.moe_stage_times.argtypes = [vp, P(ctypes.c_float)]
     L.moe_last_launch_count.argtypes = [vp, P(i32)]
     L.moe_router_bound.argtypes = [vp, i32, P(ctypes.c_float)]
+    L.moe_debug_schedule.argtypes = [vp, vp, ctypes.c_int64, P(ctypes.c_int64), vp]
     L.moe_plan_destroy.argtypes = [vp]
     L.moe_status_string.argtypes = [ctypes.c_int]
     L.moe_status_string.restype = ctypes.c_char_p
@@ -346,6 +347,19 @@ class MoELayer:
 
     def launch_count(self) -> int:
         return moe_last_launch_count(self.plan)
+
+    def schedule(self):
+        """(tiles [n, 4] int32, n_linear1, workers) the last forward's Dispatch built on the device."""
+        L = load()
+        n = (ctypes.c_int64 * 3)()
+        st = L.moe_debug_schedule(self.plan, None, 0, n, self._stream())
+        if st != MOE_OK:
+            raise MoEError(st, "moe_debug_schedule")
+        tiles = np.full((n[1], 4), -1, dtype=np.int32)
+        st = L.moe_debug_schedule(self.plan, tiles.ctypes.data, n[1], n, self._stream())
+        if st != MOE_OK:
+            raise MoEError(st, "moe_debug_schedule")
+        return tiles, int(n[0]), int(n[2])
 
     def router_bound(self, T: int) -> float:
         """cH of the default router's logit error bound for T tokens."""

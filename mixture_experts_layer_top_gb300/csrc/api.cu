@@ -300,7 +300,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
                          st));
   ++nl;
   rec(2);
-  MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.row_pair, p->ws.prow_of, R, H, k, p->ws.x_pad, st));
+  MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.prow_of, T, H, k, p->ws.x_pad, st));
   ++nl;
   rec(3);
   CUtensorMap tA1, tB1, tA2, tB2, tH, tP;
@@ -456,6 +456,24 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   if (p->trace) cudaFree(p->trace);
   cudaSetDevice(cur);
   delete p;
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_schedule(moe_plan_t p, int32_t* tiles_out, int64_t cap, int64_t* n_out, void* stream) {
+  if (!p || !n_out) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t sc[4] = {0, 0, 0, 0};
+  if (p->last_launches > 0 && cudaMemcpy(sc, p->ws.sched, sizeof(sc), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  n_out[0] = sc[0];
+  n_out[1] = sc[1];
+  n_out[2] = p->gemm_grid / PAIR;
+  if (tiles_out && sc[1] > 0) {
+    if (cap < sc[1]) return MOE_ERR_INVALID_ARG;
+    if (cudaMemcpy(tiles_out, p->ws.tiles, sizeof(int32_t) * 4 * (size_t)sc[1], cudaMemcpyDeviceToHost) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 

@@ -53,22 +53,59 @@ MOE_HD int sched_n_mt(const SchedTables& s, int w) { return s.w_first_mt[w + 1] 
 
 // Position of element i of list A (size a) when A and B (size b) are merged so
 // that A[i] sits at (2i+1)/(2a) and B[j] at (2j+1)/(2b) of the segment (ties: A first).
+// (Operands below 2^32 take a 32-bit division; the result is the same integer.)
+MOE_HD long long div_nonneg(long long n, long long d) {
+  if (n < (1ll << 32) && d < (1ll << 32)) return (long long)((unsigned)n / (unsigned)d);
+  return n / d;
+}
 MOE_HD int merge_pos_a(int i, int a, int b) {
   if (b == 0) return i;
-  long long c = ((long long)(2 * i + 1) * b + a - 1) / a;
+  long long c = div_nonneg((long long)(2 * i + 1) * b + a - 1, a);
   long long cnt = c / 2;
   return i + (int)(cnt < b ? cnt : b);
 }
 MOE_HD int merge_pos_b(int j, int a, int b) {
   if (a == 0) return j;
-  long long f = ((long long)(2 * j + 1) * a) / b;
+  long long f = div_nonneg((long long)(2 * j + 1) * a, b);
   long long cnt = (f + 1) / 2;
   return j + (int)(cnt < a ? cnt : a);
 }
 
-// Serial part: units, waves, segment starts.  counts[E] rows per expert; workers =
+// Segment starts of the ticket list, from units and waves already in s (mt, mtb,
+// wave_of, w_first_mt, W, total_mt); O(W).  Shared by the host and device builders.
+MOE_HD void sched_segments(SchedTables& s, int lead) {
+  const int W = s.W;
+  int n1_total = 0;
+  int pos = 0;
+  if (s.mode == MOE_SCHED_INTERLEAVED) {
+    int D = lead < 1 ? 1 : lead;
+    if (D > W) D = W;
+    s.lead = D;
+    for (int w = 0; w < D; ++w) {
+      s.seg_a[w] = pos;
+      pos += sched_n_mt(s, w) * s.nL1;
+    }
+    for (int w = 0; w < W; ++w) {
+      s.seg_b[w] = pos;
+      pos += sched_n_mt(s, w) * s.nL2 + (w + D < W ? sched_n_mt(s, w + D) * s.nL1 : 0);
+    }
+  } else {
+    s.lead = 0;
+    for (int w = 0; w < W; ++w) {
+      s.seg_a[w] = pos;
+      pos += sched_n_mt(s, w) * s.nL1;
+      s.seg_b[w] = pos;
+      pos += sched_n_mt(s, w) * s.nL2;
+    }
+  }
+  for (int w = 0; w < W; ++w) n1_total += sched_n_mt(s, w) * s.nL1;
+  s.n1_total = n1_total;
+  s.total = pos;
+}
+
+// Serial builder: units, waves, segment starts.  counts[E] rows per expert; workers =
 // number of concurrent tile workers (2-CTA clusters); a wave is the smallest run of
-// experts whose Linear-1 tiles reach it.
+// experts whose Linear-1 tiles reach it (the last expert never opens a new wave).
 MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int nL2, int workers, int mode,
                         int wave_experts, int lead) {
   s.E = E;
@@ -107,32 +144,7 @@ MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int n
   for (int e = 0; e < E; ++e)
     if (e == 0 || s.wave_of[e] != s.wave_of[e - 1]) s.w_first_mt[s.wave_of[e]] = s.mtb[e];
   s.w_first_mt[W] = tot;
-  int n1_total = 0;
-  int pos = 0;
-  if (mode == MOE_SCHED_INTERLEAVED) {
-    int D = lead < 1 ? 1 : lead;
-    if (D > W) D = W;
-    s.lead = D;
-    for (int w = 0; w < D; ++w) {
-      s.seg_a[w] = pos;
-      pos += sched_n_mt(s, w) * nL1;
-    }
-    for (int w = 0; w < W; ++w) {
-      s.seg_b[w] = pos;
-      pos += sched_n_mt(s, w) * nL2 + (w + D < W ? sched_n_mt(s, w + D) * nL1 : 0);
-    }
-  } else {
-    s.lead = 0;
-    for (int w = 0; w < W; ++w) {
-      s.seg_a[w] = pos;
-      pos += sched_n_mt(s, w) * nL1;
-      s.seg_b[w] = pos;
-      pos += sched_n_mt(s, w) * nL2;
-    }
-  }
-  for (int w = 0; w < W; ++w) n1_total += sched_n_mt(s, w) * nL1;
-  s.n1_total = n1_total;
-  s.total = pos;
+  sched_segments(s, lead);
 }
 
 // Ticket of the Linear-1 tile with wave-local index j in wave w.
@@ -159,27 +171,32 @@ MOE_HD int sched_expert_of(const SchedTables& s, int g) {
   return lo;
 }
 
-// Write every tile reached from global unit g.  Tile = {phase | n << 1, e, unit, g}.
-// Within a wave the tiles are ordered (expert, n-block, unit) with the unit fastest.
+// Write tile j (0 <= j < nL1 + nL2: Linear-1 n-blocks first, then Linear-2) of global
+// unit g, owned by expert e.  Tile = {phase | n << 1, e, unit, g}.  Within a wave the
+// tiles are ordered (expert, n-block, unit) with the unit fastest.
+MOE_HD void sched_emit_tile(const SchedTables& s, int g, int e, int j, int* tiles /* 4 ints per ticket */) {
+  const int m = g - s.mtb[e];
+  const int w = s.wave_of[e];
+  const int base = s.mtb[e] - s.w_first_mt[w];
+  int t, x;
+  if (j < s.nL1) {
+    t = sched_ticket_l1(s, w, base * s.nL1 + j * s.mt[e] + m);
+    x = (j << 1) | 0;
+  } else {
+    const int nb = j - s.nL1;
+    t = sched_ticket_l2(s, w, base * s.nL2 + nb * s.mt[e] + m);
+    x = (nb << 1) | 1;
+  }
+  tiles[4 * t + 0] = x;
+  tiles[4 * t + 1] = e;
+  tiles[4 * t + 2] = m;
+  tiles[4 * t + 3] = g;
+}
+
+// Write every tile reached from global unit g.
 MOE_HD void sched_emit_mtile(const SchedTables& s, int g, int* tiles /* 4 ints per ticket */) {
-  int e = sched_expert_of(s, g);
-  int m = g - s.mtb[e];
-  int w = s.wave_of[e];
-  int base = s.mtb[e] - s.w_first_mt[w];
-  for (int nb = 0; nb < s.nL1; ++nb) {
-    int t = sched_ticket_l1(s, w, base * s.nL1 + nb * s.mt[e] + m);
-    tiles[4 * t + 0] = (nb << 1) | 0;
-    tiles[4 * t + 1] = e;
-    tiles[4 * t + 2] = m;
-    tiles[4 * t + 3] = g;
-  }
-  for (int nb = 0; nb < s.nL2; ++nb) {
-    int t = sched_ticket_l2(s, w, base * s.nL2 + nb * s.mt[e] + m);
-    tiles[4 * t + 0] = (nb << 1) | 1;
-    tiles[4 * t + 1] = e;
-    tiles[4 * t + 2] = m;
-    tiles[4 * t + 3] = g;
-  }
+  const int e = sched_expert_of(s, g);
+  for (int j = 0; j < s.nL1 + s.nL2; ++j) sched_emit_tile(s, g, e, j, tiles);
 }
 
 // Upper bound of units for R routed rows over E experts.

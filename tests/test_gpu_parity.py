@@ -120,6 +120,25 @@ def test_expert_outputs_far_outside_fp16_range(exp2):
     check_y(bits(y), ref["y"])
 
 
+@pytest.mark.parametrize("name", ["skew", "smallT"])
+def test_device_schedule_equals_host_schedule(name):
+    """The Dispatch kernel builds the tile list in parallel; it must equal the serial host
+    builder's (whose permutation and dependency order the host tests check) for every mode."""
+    wl = synth.WORKLOADS[name]
+    bias = _bias(wl)
+    d = synth.device_inputs(wl)
+    for sched, we, lead in [(0, 0, 1), (1, 0, 1), (1, 0, 3), (2, 0, 1), (0, 5, 1), (1, 7, 2)]:
+        layer = _layer(wl, sched, wave_experts=we, lead=lead, bias=bias)
+        layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+        tiles, n1, workers = layer.schedule()
+        counts = layer.routing(wl.T)["counts"].cpu().numpy()
+        ref, n1_ref = moe.moe_schedule_host(counts, wl.H, wl.I, workers, sched, we, lead)
+        assert n1 == n1_ref and np.array_equal(tiles, ref), f"schedule {sched}/{we}/{lead} differs"
+        layer.close()
+    del d
+    torch.cuda.empty_cache()
+
+
 def test_schedules_bitwise_identical():
     """Every tile schedule and both shared-memory splits of the grouped GEMM give the same bits
     (the default streaming split and the forced compute split)."""
