@@ -234,7 +234,8 @@ def config_of(wl, args, l2):
     sched = {0: "wave-serial", 1: "interleaved", 2: "phased (L1 launch, L2 launch)"}[args.schedule]
     split = "streaming" if args.gemm_split == "auto" else args.gemm_split
     return {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-            "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split, "l2": l2,
+            "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
+            "wave_experts": args.wave_experts, "lead_waves": args.lead_waves, "l2": l2,
             "parallelism": f"replicas x{args.gpus} (no sharding)"}
 
 
@@ -258,7 +259,8 @@ def run_ours(args, wl):
     d = synth.device_inputs(wl, device=dev)
     flags = moe.MOE_FLAG_STAGE_TIMING | {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING,
                                          "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
-    layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=args.schedule, flags=flags),
+    layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=args.schedule, flags=flags,
+                                       wave_experts=args.wave_experts, lead_waves=args.lead_waves),
                          local, router_bias=bias)
     logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
@@ -396,6 +398,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="fine")
     ap.add_argument("--schedule", type=int, choices=(0, 1, 2), default=1)
+    ap.add_argument("--wave-experts", type=int, default=0, help="experts per wave (0: fill the SMs)")
+    ap.add_argument("--lead-waves", type=int, default=1, help="interleave lead D (interleaved schedule)")
     ap.add_argument("--gemm-split", choices=("auto", "streaming", "compute"), default="auto",
                     help="shared-memory split of the grouped GEMM (auto: the library default, streaming)")
     ap.add_argument("--no-e2e", action="store_true")

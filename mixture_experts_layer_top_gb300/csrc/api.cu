@@ -261,7 +261,6 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   if (T == 0) return MOE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int k = c.top_k, E = c.E, H = c.H, I = c.I;
-  const int R = T * k;
   int nl = 0;
   auto rec = [&](int i) {
     if (p->timing) cudaEventRecord(p->ev[i], st);

@@ -42,6 +42,7 @@ struct SchedTables {
   int E, nL1, nL2, W, mode, lead;
   int total_mt, n1_total, total;   // total_mt: number of units
   int mt[MAX_E];           // units of expert e
+  int cnt[MAX_E];          // rows of expert e
   int mtb[MAX_E + 1];      // prefix of mt
   int wave_of[MAX_E];      // wave of expert e
   int w_first_mt[MAX_E + 1];
@@ -115,6 +116,7 @@ MOE_HD void sched_build(SchedTables& s, const int* counts, int E, int nL1, int n
   int tot = 0;
   for (int e = 0; e < E; ++e) {
     int m = (counts[e] + UNIT_ROWS - 1) / UNIT_ROWS;
+    s.cnt[e] = counts[e];
     s.mt[e] = m;
     s.mtb[e] = tot;
     tot += m;
@@ -172,12 +174,15 @@ MOE_HD int sched_expert_of(const SchedTables& s, int g) {
 }
 
 // Write tile j (0 <= j < nL1 + nL2: Linear-1 n-blocks first, then Linear-2) of global
-// unit g, owned by expert e.  Tile = {phase | n << 1, e, unit, g}.  Within a wave the
-// tiles are ordered (expert, n-block, unit) with the unit fastest.
+// unit g, owned by expert e.  Tile = {phase | n << 1 | rows << 16, e, unit, g}, rows =
+// the unit's valid rows (1..256).  Within a wave the tiles are ordered (expert, n-block,
+// unit) with the unit fastest.
+MOE_HD int min_i(int a, int b) { return a < b ? a : b; }
 MOE_HD void sched_emit_tile(const SchedTables& s, int g, int e, int j, int* tiles /* 4 ints per ticket */) {
   const int m = g - s.mtb[e];
   const int w = s.wave_of[e];
   const int base = s.mtb[e] - s.w_first_mt[w];
+  const int rows = min_i(UNIT_ROWS, s.cnt[e] - m * UNIT_ROWS);
   int t, x;
   if (j < s.nL1) {
     t = sched_ticket_l1(s, w, base * s.nL1 + j * s.mt[e] + m);
@@ -187,7 +192,7 @@ MOE_HD void sched_emit_tile(const SchedTables& s, int g, int e, int j, int* tile
     t = sched_ticket_l2(s, w, base * s.nL2 + nb * s.mt[e] + m);
     x = (nb << 1) | 1;
   }
-  tiles[4 * t + 0] = x;
+  tiles[4 * t + 0] = x | (rows << 16);
   tiles[4 * t + 1] = e;
   tiles[4 * t + 2] = m;
   tiles[4 * t + 3] = g;

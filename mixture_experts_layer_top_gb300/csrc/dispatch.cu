@@ -101,6 +101,7 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
     for (int i = 0; i < MAX_E / 32; ++i) {
       const int x = lane * (MAX_E / 32) + i;
       if (x < E) {
+        s.cnt[x] = counts[x];
         s.mt[x] = m[i];
         s.mtb[x] = run;
         s_cum[x] = (run + m[i]) * nL1;

@@ -83,9 +83,10 @@ def _check_schedule(counts, H, I, sms, mode, wave_experts=0, lead=1):
     # every tile exactly once
     keys = set()
     for ph_n, e, m, g in tiles.tolist():
-        ph, nb = ph_n & 1, ph_n >> 1
+        ph, nb, rows = ph_n & 1, (ph_n >> 1) & 0x7FFF, ph_n >> 16
         assert 0 <= m < mt[e] and g == mtb[e] + m
         assert nb < (nL1 if ph == 0 else nL2)
+        assert rows == min(256, counts[e] - 256 * m) and rows >= 1
         keys.add((ph, nb, e, m))
     assert len(keys) == len(tiles)
     # topological: every Linear-2 tile after all Linear-1 tiles of its m-tile
