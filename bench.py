@@ -2,7 +2,7 @@
 """Throughput of the single-GPU MoE layer (router top-k -> Dispatch -> Linear-1 +
 SwiGLU -> Linear-2 -> Combine) on synthetic seeded inputs.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload fine] [--schedule 0]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload fine] [--schedule 3]
     python bench.py --impl reference ...     # the CPU oracle, timed the same way
 
 One step = one moe_forward over the whole batch of T tokens, inputs and weights
@@ -231,7 +231,8 @@ def run_reference(args, wl):
 
 
 def config_of(wl, args, l2):
-    sched = {0: "wave-serial", 1: "interleaved", 2: "phased (L1 launch, L2 launch)"}[args.schedule]
+    sched = {0: "wave-serial", 1: "interleaved", 2: "phased (L1 launch, L2 launch)",
+             3: "auto (wave-serial, one wave of all experts)"}[args.schedule]
     split = "streaming" if args.gemm_split == "auto" else args.gemm_split
     return {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
             "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
@@ -397,7 +398,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="fine")
-    ap.add_argument("--schedule", type=int, choices=(0, 1, 2), default=1)
+    ap.add_argument("--schedule", type=int, choices=(0, 1, 2, 3), default=3,
+                    help="0 wave-serial, 1 interleaved, 2 phased, 3 auto (the library's choice)")
     ap.add_argument("--wave-experts", type=int, default=0, help="experts per wave (0: fill the SMs)")
     ap.add_argument("--lead-waves", type=int, default=1, help="interleave lead D (interleaved schedule)")
     ap.add_argument("--gemm-split", choices=("auto", "streaming", "compute"), default="auto",

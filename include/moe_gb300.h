@@ -69,6 +69,10 @@ typedef enum {
 #define MOE_SCHED_WAVE_SERIAL 0 /* L1(w0) L2(w0) L1(w1) L2(w1) ... in one persistent launch      */
 #define MOE_SCHED_INTERLEAVED 1 /* L1(w0..wD-1), then L2(w) merged with L1(w+D), D = lead_waves  */
 #define MOE_SCHED_PHASED 2      /* all Linear-1 tiles in one launch, then all Linear-2 tiles     */
+#define MOE_SCHED_AUTO 3        /* chosen per forward; currently always wave-serial with one wave
+                                   of all experts (every Linear-1 tile, then every Linear-2 tile,
+                                   one launch): measured fastest or tied on every workload tried,
+                                   since one GPU has no Combine-store backpressure to shape       */
 
 /* flags */
 #define MOE_FLAG_ACT_BILINEAR (1u << 0) /* activation g*u instead of silu(g)*u (GLU "bilinear"

@@ -32,6 +32,7 @@ MOE_ERR_DEVICE_CHECK = 6
 MOE_SCHED_WAVE_SERIAL = 0
 MOE_SCHED_INTERLEAVED = 1
 MOE_SCHED_PHASED = 2
+MOE_SCHED_AUTO = 3
 
 MOE_FLAG_ACT_BILINEAR = 1 << 0
 MOE_FLAG_STAGE_TIMING = 1 << 1
@@ -230,7 +231,7 @@ class MoEConfig:
     I: int
     E: int
     top_k: int
-    schedule: int = MOE_SCHED_WAVE_SERIAL
+    schedule: int = MOE_SCHED_AUTO
     wave_experts: int = 0
     lead_waves: int = 1
     flags: int = 0

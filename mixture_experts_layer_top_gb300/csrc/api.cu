@@ -72,7 +72,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 moe_status_t validate_cfg(const moe_config_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T_max < 1 || c->H < 1 || c->I < 1 || c->E < 1 || c->top_k < 1) return MOE_ERR_INVALID_ARG;
-  if (c->schedule < 0 || c->schedule > 2 || c->wave_experts < 0 || c->lead_waves < 0 || c->timeout_ns < 0)
+  if (c->schedule < 0 || c->schedule > MOE_SCHED_AUTO || c->wave_experts < 0 || c->lead_waves < 0 ||
+      c->timeout_ns < 0)
     return MOE_ERR_INVALID_ARG;
   if ((c->flags & MOE_FLAG_GEMM_STREAMING) && (c->flags & MOE_FLAG_GEMM_COMPUTE)) return MOE_ERR_INVALID_ARG;
   if (c->H % L2_COLS != 0 || c->I % L1_COLS != 0) return MOE_ERR_UNSUPPORTED;
@@ -295,8 +296,10 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
     ++nl;
   }
   rec(1);
-  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, c.schedule, c.wave_experts, c.lead_waves,
-                         st));
+  // schedule actually run: MOE_SCHED_AUTO resolves to wave-serial with one wave of all experts
+  const int sched_mode = (c.schedule == MOE_SCHED_AUTO) ? MOE_SCHED_WAVE_SERIAL : c.schedule;
+  const int sched_we = (c.schedule == MOE_SCHED_AUTO) ? E : c.wave_experts;
+  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, sched_mode, sched_we, c.lead_waves, st));
   ++nl;
   rec(2);
   MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.prow_of, T, H, k, p->ws.x_pad, st));

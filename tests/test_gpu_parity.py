@@ -127,11 +127,13 @@ def test_device_schedule_equals_host_schedule(name):
     wl = synth.WORKLOADS[name]
     bias = _bias(wl)
     d = synth.device_inputs(wl)
-    for sched, we, lead in [(0, 0, 1), (1, 0, 1), (1, 0, 3), (2, 0, 1), (0, 5, 1), (1, 7, 2)]:
+    for sched, we, lead in [(0, 0, 1), (1, 0, 1), (1, 0, 3), (2, 0, 1), (0, 5, 1), (1, 7, 2), (3, 0, 1)]:
         layer = _layer(wl, sched, wave_experts=we, lead=lead, bias=bias)
         layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
         tiles, n1, workers = layer.schedule()
         counts = layer.routing(wl.T)["counts"].cpu().numpy()
+        if sched == moe.MOE_SCHED_AUTO:   # resolves to wave-serial with one wave of all experts
+            sched, we = moe.MOE_SCHED_WAVE_SERIAL, wl.E
         ref, n1_ref = moe.moe_schedule_host(counts, wl.H, wl.I, workers, sched, we, lead)
         assert n1 == n1_ref and np.array_equal(tiles, ref), f"schedule {sched}/{we}/{lead} differs"
         layer.close()
@@ -147,7 +149,7 @@ def test_schedules_bitwise_identical():
     outs = []
     S = moe.MOE_FLAG_GEMM_COMPUTE
     for sched, we, lead, fl in [(0, 0, 1, 0), (1, 0, 1, 0), (1, 0, 3, 0), (2, 0, 1, 0), (0, 3, 1, 0),
-                                (1, 2, 2, 0), (1, 0, 1, S), (2, 0, 1, S), (0, 3, 1, S)]:
+                                (1, 2, 2, 0), (3, 0, 1, 0), (1, 0, 1, S), (2, 0, 1, S), (0, 3, 1, S)]:
         layer = _layer(wl, sched, wave_experts=we, lead=lead, flags=fl)
         y, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
         y2, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)

@@ -36,7 +36,7 @@ def test_config_struct_layout():
     (dict(H=100), moe.MOE_ERR_UNSUPPORTED), (dict(I=96), moe.MOE_ERR_UNSUPPORTED),
     (dict(E=300), moe.MOE_ERR_UNSUPPORTED), (dict(top_k=9), moe.MOE_ERR_UNSUPPORTED),
     (dict(top_k=0), moe.MOE_ERR_INVALID_ARG), (dict(T_max=0), moe.MOE_ERR_INVALID_ARG),
-    (dict(schedule=3), moe.MOE_ERR_INVALID_ARG), (dict(E=4, top_k=5), moe.MOE_ERR_UNSUPPORTED),
+    (dict(schedule=4), moe.MOE_ERR_INVALID_ARG), (dict(E=4, top_k=5), moe.MOE_ERR_UNSUPPORTED),
     (dict(flags=moe.MOE_FLAG_GEMM_STREAMING | moe.MOE_FLAG_GEMM_COMPUTE), moe.MOE_ERR_INVALID_ARG),
 ])
 def test_config_validation(lib, kw, status):
