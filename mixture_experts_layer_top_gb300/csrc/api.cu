@@ -110,7 +110,7 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
   sizes[B_X_PAD] = (size_t)Rp * c.H * 2;
   sizes[B_H_PAD] = (size_t)Rp * c.I * 2;
   sizes[B_P_PAD] = (size_t)Rp * c.H * 2;                 // fp16
-  sizes[B_S_PAD] = (size_t)Rp * (c.H / L2_COLS) * 4;     // per-(row, 256 columns) scale of P_pad
+  sizes[B_S_PAD] = (size_t)Rp * (c.H / P_SCALE_COLS) * 4;   // per-(row, 128 columns) scale of P_pad
   sizes[B_TILES] = (size_t)max_tiles * 16;
   sizes[B_SCHED] = 16;
   sizes[B_READY] = (size_t)max_mt * 4;

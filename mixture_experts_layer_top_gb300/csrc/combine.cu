@@ -1,7 +1,7 @@
 // Combine on one GPU: y[t,:] = bf16( sum_{j=0..k-1} P[row(t,j), :] ), the fp32
 // sum taken in slot order j = 0, 1, ..., k-1 so the result does not depend on
 // which expert finished first.  P is stored as fp16 with a power-of-two scale per
-// (row, 256 columns); each term is widened and rescaled exactly before the sum.
+// (row, 128 columns); each term is widened and rescaled exactly before the sum.
 // P already holds w[t,j] * (expert output): this is the Combine of the X-Stage
 // paper's MegaMoE paragraph (introduction) - the router-weighted sum of a
 // token's top-k expert outputs - with the weights applied upstream.
@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const uint16_t* __restrict__ P_pad, const float* __restrict__ S_pad, const int32_t* __restrict__ prow_of,
                int T, int H, int k, uint16_t* __restrict__ y) {
   const int64_t n8 = (int64_t)T * H / 8;
-  const int nS = H / L2_COLS;
+  const int nS = H / P_SCALE_COLS;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = (i * 8) / H;
     const int64_t c = (i * 8) % H;
@@ -30,7 +30,7 @@ combine_kernel(const uint16_t* __restrict__ P_pad, const float* __restrict__ S_p
     for (int j = 0; j < k; ++j) {
       const int64_t row = pr[j];
       const uint4 v = __ldcs(reinterpret_cast<const uint4*>(P_pad + row * H + c));
-      const float sc = S_pad[row * nS + c / L2_COLS];
+      const float sc = S_pad[row * nS + c / P_SCALE_COLS];
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {

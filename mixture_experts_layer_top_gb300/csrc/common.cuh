@@ -20,6 +20,7 @@ constexpr int BK = 64;           // K per pipeline stage: 64 bf16 = one 128-byte
 constexpr int MMA_N = 256;       // tcgen05 N of both GEMMs
 constexpr int L1_COLS = 128;     // intermediate columns per Linear-1 tile (gate 128 | up 128)
 constexpr int L2_COLS = 256;     // output columns per Linear-2 tile
+constexpr int P_SCALE_COLS = 128;  // columns of P sharing one power-of-two scale
 constexpr int STAGES = 4;        // smem ring depth
 constexpr int PAIR = 2;          // m-tiles per cluster tile: a 2-CTA cluster shares each B tile
 constexpr int UNIT_ROWS = BM * PAIR;

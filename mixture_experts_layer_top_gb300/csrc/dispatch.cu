@@ -372,7 +372,7 @@ compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t
       reinterpret_cast<uint4*>(h + (size_t)row * I)[i] = reinterpret_cast<const uint4*>(h_pad + pr * I)[i];
   if (P)
     for (int c = lane; c < H; c += 32)
-      P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * (H / L2_COLS) + c / L2_COLS];
+      P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * (H / P_SCALE_COLS) + c / P_SCALE_COLS];
 }
 
 }  // namespace

@@ -5,7 +5,7 @@
 //   (up): one M=256 x N=256 tcgen05 accumulator; epilogue h = bf16(silu(g) * u).
 // Linear-2 tile (phase 1): the same rows of h times W2[e][:, 256 n .. +256];
 //   epilogue P = w[t,j] * acc, the router-weight scale, stored as fp16 times an
-//   exact power-of-two scale per (row, 256-column block): the scale puts the
+//   exact power-of-two scale per (row, 128-column block): the scale puts the
 //   block's largest finite |P| in [2^14, 2^15], so nothing overflows and every
 //   value keeps fp16's 11 significant bits.
 // (X-Stage paper, MegaMoE background: Linear-1 projects hidden to
@@ -41,8 +41,7 @@
 // per 32-row quadrant (one epilogue warp pair): a quadrant whose rows are all
 // valid is staged in shared memory in the 128-byte swizzled layout
 // (conflict-free row writes) and written by a bulk tensor store (h: bf16 32 x 64
-// boxes for Linear-1; P: fp16 32 x 64 boxes in two 128-column passes for
-// Linear-2); the valid rows of a partial quadrant are stored directly; empty
+// boxes for Linear-1; P: fp16 32 x 64 boxes in two passes for Linear-2); the valid rows of a partial quadrant are stored directly; empty
 // quadrants write nothing.  NBUF 32 KB staging buffers rotate, each reused
 // only after its previous store group has read it.  Linear-1 readiness is
 // published after its h rows are written.
@@ -101,7 +100,6 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   int ep_ok[2];             // epilogue go/stop decision of the waiting thread, by tile parity
-  float rmax[2][BM];        // Linear-2 epilogue: largest finite |acc| of each row, per column half
 };
 static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block exceeds its shared-memory reservation");
 
@@ -378,16 +376,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
         }
         ++sb;
       } else {
-        // P = w * acc.  Sweep 1: the largest finite |acc| of the row (this thread's 128
-        // columns, then the other column half's through shared memory) sets the row's
-        // scale 2^se; sweep 2: two passes of 128 columns, warp half ch taking columns
-        // [128 p + 64 ch, +64), each value fp16(fl(w * acc) * 2^-se).
+        // P = w * acc; warp half ch owns columns [128 ch, 128 ch + 128) of the tile, one
+        // scale block.  Sweep 1: the block's largest finite |acc| of this row sets its
+        // scale 2^se; sweep 2: two passes of 64 columns, each value fp16(fl(w * acc) * 2^-se).
         const float wgt = (staged || direct) ? args.prow_w[prow0 + r] : 0.0f;
         float amax = 0.0f;
 #pragma unroll 1
-        for (int c4 = 0; c4 < MMA_N / 64; ++c4) {
+        for (int c4 = 0; c4 < P_SCALE_COLS / 32; ++c4) {
           uint32_t v[32];
-          ptx::tmem_ld32(taddr + c4 * 64 + ch * 32, v);
+          ptx::tmem_ld32(taddr + ch * P_SCALE_COLS + c4 * 32, v);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -395,10 +392,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
             amax = (a < INFINITY) ? fmaxf(amax, a) : amax;   // finite values only (NaN compares false)
           }
         }
-        ctl->rmax[ch][r] = amax;
-        ptx::named_bar_sync(1, EPI_THREADS);
-        amax = fmaxf(ctl->rmax[0][r], ctl->rmax[1][r]);
-        // M >= every finite |fl(w * acc)| of the row; se = ceil(log2 M) - 15
+        // M >= every finite |fl(w * acc)| of the block; se = ceil(log2 M) - 15
         const float M = amax * fabsf(wgt) * (1.0f + 0x1p-20f);
         int se = 0;
         if (M > 0.0f) {
@@ -411,9 +405,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           se = max(-126, min(127, cl2 - 15));
         }
         const float inv = __uint_as_float((uint32_t)(127 - se) << 23);   // 2^-se, exact
-        if ((staged || direct) && ch == 0)
-          args.S_pad[(size_t)(prow0 + r) * args.nL2 + nb] = __uint_as_float((uint32_t)(127 + se) << 23);
-        uint16_t* prow = args.P_pad + (size_t)(prow0 + r) * args.H + nb * L2_COLS + ch * 64;
+        const int nS = args.H / P_SCALE_COLS;
+        if (staged || direct)
+          args.S_pad[(size_t)(prow0 + r) * nS + nb * (L2_COLS / P_SCALE_COLS) + ch] =
+              __uint_as_float((uint32_t)(127 + se) << 23);
+        uint16_t* prow = args.P_pad + (size_t)(prow0 + r) * args.H + nb * L2_COLS + ch * P_SCALE_COLS;
 #pragma unroll 1
         for (int pass = 0; pass < MMA_N / 128; ++pass) {
           acquire_stage();
@@ -421,7 +417,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
-            ptx::tmem_ld32(taddr + pass * 128 + ch * 64 + c * 32, v);
+            ptx::tmem_ld32(taddr + ch * P_SCALE_COLS + pass * 64 + c * 32, v);
             ptx::tmem_ld_wait();
             uint32_t pk[16];
 #pragma unroll
@@ -435,7 +431,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
             for (int j = 0; j < 4; ++j) {
               const uint4 v4 = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
               if (staged) *reinterpret_cast<uint4*>(box + chunk_off(4 * c + j)) = v4;
-              else if (direct) reinterpret_cast<uint4*>(prow + pass * 128)[4 * c + j] = v4;
+              else if (direct) reinterpret_cast<uint4*>(prow + pass * 64)[4 * c + j] = v4;
             }
           }
           if (pass == MMA_N / 128 - 1) ptx::tc_fence_before();
@@ -445,8 +441,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
             if (pass == MMA_N / 128 - 1) ptx::mbar_arrive_cluster(tempty_addr);
             uint8_t* buf = stg + (sb % NBUF) * STG_BYTES;
             for (int gq = 0; gq < nfull; ++gq) {
-              ptx::tma_store_2d(&tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 128, prow0 + gq * ST_ROWS);
-              ptx::tma_store_2d(&tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 128 + 64,
+              ptx::tma_store_2d(&tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64, prow0 + gq * ST_ROWS);
+              ptx::tma_store_2d(&tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + P_SCALE_COLS + pass * 64,
                                 prow0 + gq * ST_ROWS);
             }
             ptx::bulk_commit();                      // one group per pass, possibly empty

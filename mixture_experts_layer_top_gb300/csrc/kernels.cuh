@@ -25,7 +25,7 @@ struct Workspace {
   uint16_t* x_pad;    // [R_pad_max, H] bf16
   uint16_t* h_pad;    // [R_pad_max, I] bf16
   uint16_t* P_pad;    // [R_pad_max, H] fp16: w[t,j] * expert output / S_pad
-  float* S_pad;       // [R_pad_max, H/256] fp32 powers of two: scale of each 256-column block of P_pad
+  float* S_pad;       // [R_pad_max, H/128] fp32 powers of two: scale of each 128-column block of P_pad
   int32_t* tiles;     // [max_tiles*4]
   int32_t* sched;     // [4]: linear-1 tiles, total tiles, units
   int32_t* ready;     // [max_units]
