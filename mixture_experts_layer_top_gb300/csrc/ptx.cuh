@@ -198,13 +198,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B MN-major (N contiguous in global memory), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major) {
+// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, shape M x N;
+// A K-major unless a_mn_major, B MN-major (N contiguous in memory) when b_mn_major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major,
+                                                      bool a_mn_major = false) {
   return (1u << 4)                        // D format: f32
          | (1u << 7)                      // A format: bf16
          | (1u << 10)                     // B format: bf16
-         | (0u << 15)                     // A K-major
+         | ((a_mn_major ? 1u : 0u) << 15) // A major
          | ((b_mn_major ? 1u : 0u) << 16) // B major
          | ((N >> 3) << 17)               // N / 8
          | ((M >> 4) << 24);              // M / 16

@@ -210,6 +210,27 @@ def test_ragged_token_counts(T, flags):
     check_y(bits(y), ref["y"])
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [(100, 256, 128, 6, 2), (64, 256, 128, 1, 1), (50, 512, 128, 40, 8),
+                                       (300, 256, 384, 3, 3), (33, 768, 256, 200, 8)])
+@pytest.mark.parametrize("flags", [0, EXACT])
+def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
+    """Expert counts that are not multiples of 8 / 16 / 32 (tensor-core router N padding,
+    transpose tiles, selection keys), one expert, k = E, the smallest H and I the layout allows:
+    routing and y against the full oracle, default and all-canonical routers."""
+    wl = synth.Workload("odd", T, H, I, E, k)
+    h = synth.host_inputs(wl)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    layer = _layer(wl, flags=flags)
+    d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    if flags & EXACT:
+        assert np.array_equal(logits.cpu().numpy(), ref["logits"])
+    else:
+        check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
+    routing_equal(layer.routing(T), ref, T)
+    check_y(bits(y), ref["y"])
+
+
 def test_zero_tokens_is_noop():
     wl = synth.WORKLOADS["tiny"]
     layer = _layer(wl)
