@@ -258,8 +258,7 @@ def run_ours(args, wl):
 
     bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
     d = synth.device_inputs(wl, device=dev)
-    flags = moe.MOE_FLAG_STAGE_TIMING | {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING,
-                                         "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
+    flags = {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING, "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
     layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=args.schedule, flags=flags,
                                        wave_experts=args.wave_experts, lead_waves=args.lead_waves),
                          local, router_bias=bias)
@@ -282,13 +281,11 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    stages = []
-    for i in range(args.steps):
+    for i in range(args.steps):                # no host synchronisation inside the timed steps
         flush.zero_()
         ev[i][0].record()
         layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=logits, y=y)
         ev[i][1].record()
-        stages.append(layer.stage_times())     # waits for this step's events
     torch.cuda.synchronize()
     barrier(group)
     torch.cuda.synchronize()
@@ -322,6 +319,19 @@ def run_ours(args, wl):
         e2e = {"value": ws * wl.useful_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
                "ms_per_step": e_ms, "tokens_per_s": ws * wl.T / (e_ms * 1e-3)}
+    # ---- per-stage breakdown on a second plan whose library records events between stages
+    # (those events serialise the stream, so the headline steps above run without them)
+    layer_t = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=args.schedule,
+                                         flags=flags | moe.MOE_FLAG_STAGE_TIMING, wave_experts=args.wave_experts,
+                                         lead_waves=args.lead_waves), local, router_bias=bias)
+    stages = []
+    for i in range(3 + min(args.steps, 20)):
+        flush.zero_()
+        layer_t.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=logits, y=y)
+        if i >= 3:
+            stages.append(layer_t.stage_times())
+    layer_t.check()
+    layer_t.close()
     if sampler:
         sampler.stop()
     clocks = sampler.summary(t0, t1) if sampler else None

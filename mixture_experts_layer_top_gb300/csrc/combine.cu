@@ -9,6 +9,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -20,6 +21,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint16_t* __restrict__ P_pad, const float* __restrict__ S_pad, const int32_t* __restrict__ prow_of,
                int T, int H, int k, uint16_t* __restrict__ y) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int64_t n8 = (int64_t)T * H / 8;
   const int nS = H / P_SCALE_COLS;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
@@ -64,8 +66,7 @@ cudaError_t launch_combine(const uint16_t* P_pad, const float* S_pad, const int3
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<(int)blocks, 256, 0, st>>>(P_pad, S_pad, prow_of, T, H, k, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, P_pad, S_pad, prow_of, T, H, k, y);
 }
 
 }  // namespace moe

@@ -10,6 +10,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -63,6 +64,7 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
                 int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair, int32_t* __restrict__ row_of,
                 int32_t* __restrict__ prow_of, float* __restrict__ prow_w, int32_t* __restrict__ tiles,
                 int32_t* __restrict__ sched, int32_t* __restrict__ ready) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int R = T * k;
   const int e = blockIdx.x % E, part = blockIdx.x / E;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -322,6 +324,7 @@ constexpr int GA_CHUNK = 128;   // 16-byte units per warp task (2 KB)
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ prow_of, int T, int H, int k,
                    uint16_t* __restrict__ x_pad) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int n = H / 8;                                  // 16-byte units per row, a multiple of 32
   const int nch = (n + GA_CHUNK - 1) / GA_CHUNK;
   const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -379,17 +382,13 @@ compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t
 
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, cudaStream_t st) {
-  dispatch_kernel<<<E * DS_SPLIT, DS_THREADS, 0, st>>>(ws.ids, ws.w, ws.counts, T, E, k, I / L1_COLS, H / L2_COLS,
-                                                num_sms, mode, wave_experts, lead, ws.offsets, ws.row_pair,
-                                                ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_kernel, dim3(E * DS_SPLIT), dim3(DS_THREADS), 0, st, ws.ids, ws.w, ws.counts, T, E, k, I / L1_COLS, H / L2_COLS, num_sms, mode, wave_experts, lead, ws.offsets, ws.row_pair, ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready);
 }
 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int H, int k, uint16_t* x_pad,
                           cudaStream_t st) {
   const int nch = (H / 8 + GA_CHUNK - 1) / GA_CHUNK;
-  gather_rows_kernel<<<(T * nch + 7) / 8, 256, 0, st>>>(x, prow_of, T, H, k, x_pad);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3((T * nch + 7) / 8), dim3(256), 0, st, x, prow_of, T, H, k, x_pad);
 }
 
 cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,

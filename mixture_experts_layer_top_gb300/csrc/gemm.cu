@@ -177,6 +177,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
   uint64_t* trp_b = tracing ? &tr_b : nullptr;
   const int cluster = blockIdx.x / PAIR, nclusters = gridDim.x / PAIR;
 
+  ptx::grid_dep_wait();   // Dispatch's tile list and the gathered rows are visible from here on
   int t_begin, t_end;
   tile_range(args, t_begin, t_end);
   const int64_t tmo = args.timeout_ns;
@@ -529,8 +530,11 @@ cudaError_t gemm_prepare(int device, int* grid) {
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
                                 const GemmArgs& a, int grid, bool streaming, cudaStream_t st) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = gemm_config(grid, st, attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap launch and setup with the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   if (streaming) return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<6, 1>, tA1, tB1, tA2, tB2, tH, tP, a);
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<5, 2>, tA1, tB1, tA2, tB2, tH, tP, a);
 }

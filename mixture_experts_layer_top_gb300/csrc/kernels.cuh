@@ -8,6 +8,25 @@
 
 namespace moe {
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel of the stream drains; every kernel launched this way calls
+// ptx::grid_dep_wait() before its first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Row spaces: "compact" rows 0..R-1 group the (token, slot) pairs by expert
 // (row_pair / row_of, as returned by moe_debug_routing); "padded" rows give every
 // 256-row unit of an expert its own block (unit g owns rows 256 g .. 256 g + 255),

@@ -20,6 +20,11 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Programmatic dependent launch: wait until the previous kernel of the stream has
+// completed and its memory is visible (returns at once when launched without the
+// programmatic-serialization attribute).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 #include "routing.cuh"
 
 namespace moe {
@@ -64,6 +65,7 @@ __device__ __forceinline__ void rs_step(float (&acc)[64], int lane) {
 __global__ void __launch_bounds__(RT_THREADS, 1)
 router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wr,
                      const float* __restrict__ bias, float* __restrict__ logits, int T, int H, int E) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   extern __shared__ __align__(16) uint16_t rsm[];
   uint16_t* xs = rsm;                               // [NS][32 tok][XROW]
   uint16_t* ws = rsm + RT_NS * RT_STAGE_X;          // [NS][HC][WROW]
@@ -171,6 +173,7 @@ constexpr int TK_MAX_TOK_PER_WARP = 8;
 __global__ void __launch_bounds__(TK_WARPS * 32)
 topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
             float* __restrict__ w, int32_t* __restrict__ counts, int tpw) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   __shared__ int32_t hist[MAX_E];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -209,8 +212,7 @@ cudaError_t router_prepare() {
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
                                  int H, int E, cudaStream_t st) {
   dim3 grid((T + RT_TOK - 1) / RT_TOK, (E + RT_EXP - 1) / RT_EXP);
-  router_logits_kernel<<<grid, RT_THREADS, RT_SMEM, st>>>(x, Wr, bias, logits, T, H, E);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_kernel, grid, dim3(RT_THREADS), RT_SMEM, st, x, Wr, bias, logits, T, H, E);
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
@@ -219,8 +221,8 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
   int tpw = (T + 2 * num_sms * TK_WARPS - 1) / (2 * num_sms * TK_WARPS);
   tpw = tpw < 1 ? 1 : (tpw > TK_MAX_TOK_PER_WARP ? TK_MAX_TOK_PER_WARP : tpw);
   const int per_block = tpw * TK_WARPS;
-  topk_kernel<<<(T + per_block - 1) / per_block, TK_WARPS * 32, 0, st>>>(logits, T, E, k, ids, w, counts, tpw);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3((T + per_block - 1) / per_block), dim3(TK_WARPS * 32), 0, st, logits, T, E, k, ids,
+                    w, counts, tpw);
 }
 
 }  // namespace moe

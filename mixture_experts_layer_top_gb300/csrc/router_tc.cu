@@ -54,6 +54,7 @@ constexpr int RP_H = 64;    // h rows per block
 // grid (ceil(E/32), H/64), 256 threads: WrT[e0 .. e0+31][h0 .. h0+63] = Wr[h0.., e0..]^T.
 __global__ void __launch_bounds__(256)
 router_prep_kernel(const uint16_t* __restrict__ Wr, int H, int E, uint16_t* __restrict__ WrT) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   __shared__ __align__(16) uint16_t tile[32][RP_H + 8];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int e0 = blockIdx.x * 32, h0 = blockIdx.y * RP_H;
@@ -130,6 +131,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
+  ptx::grid_dep_wait();   // the transposed router weight is visible from here on
 
   if (warp == 0) {
     if (lane == 0) {
@@ -332,6 +334,7 @@ router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
                      float cH, int ntok, float* __restrict__ logits, int32_t* __restrict__ ids,
                      float* __restrict__ w, int32_t* __restrict__ counts) {
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   __shared__ int32_t hist[MAX_E];
   __shared__ float lg[SEL_WARPS][MAX_E];
   __shared__ int16_t cl[SEL_WARPS][MAX_E];
@@ -490,21 +493,18 @@ cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
                              float* logits, int32_t* ids, float* w, int32_t* counts, uint32_t* err,
                              int64_t timeout_ns, cudaStream_t st) {
   const RouterSplit sp = router_split(T, H, E, num_sms);
-  router_prep_kernel<<<dim3((E + 31) / 32, H / RP_H), 256, 0, st>>>(Wr, H, E, rw.WrT);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(router_prep_kernel, dim3((E + 31) / 32, H / RP_H), dim3(256), 0, st, Wr, H, E, rw.WrT);
   if (e != cudaSuccess) return e;
   const int n_pad = ((E + 15) / 16) * 16;
-  router_tc_kernel<<<dim3(sp.m_tiles, sp.splits), RTC_THREADS, RTC_SMEM, st>>>(
-      tmX, tmW, rw.WrT, T, H, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, rw.nw, err, timeout_ns);
-  e = cudaGetLastError();
+  e = launch_pdl(router_tc_kernel, dim3(sp.m_tiles, sp.splits), dim3(RTC_THREADS), RTC_SMEM, st, tmX, tmW, rw.WrT, T,
+                 H, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, rw.nw, err, timeout_ns);
   if (e != cudaSuccess) return e;
   // tokens per block: SEL_WARPS, or fewer when T is small so that every SM gets a block
   int ntok = (T + num_sms - 1) / num_sms;
   ntok = ntok < 1 ? 1 : (ntok > SEL_WARPS ? SEL_WARPS : ntok);
-  router_select_kernel<<<(T + ntok - 1) / ntok, SEL_WARPS * 32, 0, st>>>(
-      x, rw.WrT, rw.part, sp.splits, rw.nw, bias, T, H, E, k, router_bound_coef(H, sp), ntok, logits, ids, w,
-      counts);
-  return cudaGetLastError();
+  return launch_pdl(router_select_kernel, dim3((T + ntok - 1) / ntok), dim3(SEL_WARPS * 32), 0, st, x, rw.WrT,
+                    rw.part, sp.splits, rw.nw, bias, T, H, E, k, router_bound_coef(H, sp), ntok, logits, ids, w,
+                    counts);
 }
 
 }  // namespace moe
