@@ -329,7 +329,7 @@ __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, 
 // owning token w: (1) bounds and candidates per token; (2) the block's warps
 // evaluate every (token, candidate) pair together, 8 pairs per warp at a time;
 // (3) each warp selects its token's top-k on the exact values.  E <= 256.
-__global__ void __launch_bounds__(SEL_WARPS * 32, 4)
+__global__ void __launch_bounds__(SEL_WARPS * 32, 3)
 router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ WrT, const float* __restrict__ part,
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
                      float cH, int ntok, float* __restrict__ logits, int32_t* __restrict__ ids,
