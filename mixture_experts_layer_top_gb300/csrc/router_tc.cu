@@ -499,9 +499,14 @@ cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
   e = launch_pdl(router_tc_kernel, dim3(sp.m_tiles, sp.splits), dim3(RTC_THREADS), RTC_SMEM, st, tmX, tmW, rw.WrT, T,
                  H, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, rw.nw, err, timeout_ns);
   if (e != cudaSuccess) return e;
-  // tokens per block: SEL_WARPS, or fewer when T is small so that every SM gets a block
+  // tokens per block: chosen so that a block's (token, candidate) pairs mostly fit one round
+  // of SEL_WARPS * 8 four-lane groups (a few more pairs would cost a whole second round).
+  // Long rows mean longer accumulation chains, a larger bound coefficient and more
+  // candidates per token: measured best 7 tokens for H = 2048 (fine, skewed workloads) and
+  // 5 for H = 7168.  Fewer when T is small, so that every SM gets a block.
+  const int per_block = (H >= 4096) ? 5 : 7;
   int ntok = (T + num_sms - 1) / num_sms;
-  ntok = ntok < 1 ? 1 : (ntok > SEL_WARPS ? SEL_WARPS : ntok);
+  ntok = ntok < 1 ? 1 : (ntok > per_block ? per_block : ntok);
   return launch_pdl(router_select_kernel, dim3((T + ntok - 1) / ntok), dim3(SEL_WARPS * 32), 0, st, x, rw.WrT,
                     rw.part, sp.splits, rw.nw, bias, T, H, E, k, router_bound_coef(H, sp), ntok, logits, ids, w,
                     counts);
