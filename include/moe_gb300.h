@@ -141,12 +141,15 @@ MOE_API moe_status_t moe_forward(moe_plan_t plan, int32_t T, const void* x, floa
                          const void* W_router, const void* W1_gate_up, const void* W2, void* y,
                          void* stream);
 
-/* moe_forward with the token tensors in HOST memory: copies x_host (bf16 [T, H]) into a
- * plan-owned device buffer, runs the layer, and copies y (bf16 [T, H]) back into y_host, all
- * enqueued on `stream` (the copies overlap nothing and are asynchronous when the host buffers
- * are page-locked; pageable buffers make them synchronous).  router_logits, W_router,
- * W1_gate_up and W2 are DEVICE pointers exactly as in moe_forward.  The caller must not touch
- * y_host before the stream reaches this point (e.g. cudaStreamSynchronize). */
+/* moe_forward with the token tensors in HOST memory: x_host (bf16 [T, H]) is brought into a
+ * plan-owned device buffer, the layer runs, and y (bf16 [T, H]) lands in y_host, all enqueued
+ * on `stream`.  A page-locked buffer that is mapped into the device's address space (any
+ * cudaHostAlloc / cudaMallocHost buffer under unified addressing) at a 16-byte-aligned address
+ * is reached by the kernels directly: a copy kernel reads x_host, and Combine stores y into
+ * y_host in place.  Any other buffer goes through cudaMemcpyAsync and a plan-owned staging
+ * buffer (synchronous for pageable memory).  router_logits, W_router, W1_gate_up and W2 are
+ * DEVICE pointers exactly as in moe_forward.  The caller must not touch y_host before the
+ * stream reaches this point (e.g. cudaStreamSynchronize), and must not write x_host before then. */
 MOE_API moe_status_t moe_forward_host(moe_plan_t plan, int32_t T, const void* x_host, float* router_logits,
                               const void* W_router, const void* W1_gate_up, const void* W2, void* y_host,
                               void* stream);

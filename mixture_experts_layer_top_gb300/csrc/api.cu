@@ -69,6 +69,19 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Address at which the current device reaches host pointer h, if h lies in page-locked
+// memory mapped into its address space and that address is 16-byte aligned; else null.
+const void* mapped_host(const void* h) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned16(a.devicePointer)) return nullptr;
+  return a.devicePointer;
+}
+void* mapped_host(void* h) { return const_cast<void*>(mapped_host(static_cast<const void*>(h))); }
+
 moe_status_t validate_cfg(const moe_config_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T_max < 1 || c->H < 1 || c->I < 1 || c->E < 1 || c->top_k < 1) return MOE_ERR_INVALID_ARG;
@@ -364,12 +377,28 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
     p->last_launches = 0;
     return MOE_OK;
   }
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cur != p->device) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)T * p->cfg.H * 2;
-  if (cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
-  moe_status_t s = moe_forward(p, T, p->x_stage, router_logits, W_router, W1, W2, p->y_stage, stream);
+  // Page-locked buffers are reached from the kernels directly: a copy kernel pulls x
+  // and Combine writes y in place.  Pageable ones go through the copy engines.
+  const void* x_dev = mapped_host(x_host);
+  void* y_dev = mapped_host(y_host);
+  int nl = 0;
+  if (x_dev) {
+    if (launch_stage_copy(x_dev, p->x_stage, bytes, p->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    nl = 1;
+  } else if (cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
+  moe_status_t s = moe_forward(p, T, p->x_stage, router_logits, W_router, W1, W2, y_dev ? y_dev : p->y_stage,
+                               stream);
+  p->last_launches += nl;
   if (s != MOE_OK) return s;
-  if (cudaMemcpyAsync(y_host, p->y_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!y_dev && cudaMemcpyAsync(y_host, p->y_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -378,7 +378,26 @@ compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t
       P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * (H / P_SCALE_COLS) + c / P_SCALE_COLS];
 }
 
+// Token block from page-locked host memory (mapped into this device's address space)
+// into the device staging buffer, pulled by the SMs with 16-byte loads: over the
+// CPU-GPU link these reach a higher rate than the copy engines do for one buffer.
+__global__ void __launch_bounds__(512)
+stage_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
+  ptx::grid_dep_wait();   // the previous forward no longer reads dst from here on
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st) {
+  const int64_t n = (int64_t)(bytes / 16);
+  int64_t blocks = (n + 511) / 512;
+  if (blocks > num_sms) blocks = num_sms;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(stage_copy_kernel, dim3((unsigned)blocks), dim3(512), 0, st, static_cast<const uint4*>(src),
+                    static_cast<uint4*>(dst), n);
+}
 
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, cudaStream_t st) {

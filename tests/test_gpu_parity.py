@@ -240,6 +240,36 @@ def test_zero_tokens_is_noop():
     del x
 
 
+@pytest.mark.parametrize("mode", ["pinned", "pinned_view", "pinned_offset8", "pageable"])
+def test_host_buffers_match_device_forward(mode):
+    """The host-buffer entry point against the device one on the same inputs: y and the
+    logits bit for bit.  Page-locked buffers at 16-byte-aligned addresses (a whole buffer,
+    a view starting 3 rows in) are read by a copy kernel and written by Combine in place
+    (one launch more); a page-locked view 8 bytes off alignment and pageable buffers go
+    through the copy engines (no extra launch).  1000 tokens: a ragged last tile."""
+    wl = synth.Workload("host", 1000, 1024, 256, 16, 4)
+    h = synth.host_inputs(wl)
+    d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
+    layer = _layer(wl)
+    y_dev, lg_dev = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    n_dev = layer.launch_count()
+    n = wl.T * wl.H
+    pin = mode != "pageable"
+    xb = torch.empty(n + 3 * wl.H, dtype=torch.bfloat16, pin_memory=pin)
+    yb = torch.full((n + 3 * wl.H,), float("nan"), dtype=torch.bfloat16, pin_memory=pin)
+    off = {"pinned": 0, "pinned_view": 3 * wl.H, "pinned_offset8": 4, "pageable": 0}[mode]
+    x_host = xb[off:off + n].view(wl.T, wl.H)
+    y_host = yb[off:off + n].view(wl.T, wl.H)
+    x_host.copy_(d["x"].cpu())
+    logits = torch.empty_like(lg_dev)
+    layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host, check=True)
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+    assert torch.equal(logits, lg_dev)
+    direct = mode in ("pinned", "pinned_view")
+    assert layer.launch_count() == n_dev + (1 if direct else 0)
+    assert torch.isnan(yb[:off]).all() and torch.isnan(yb[off + n:]).all()   # nothing outside y_host
+
+
 def test_router_certified_selection_on_ties_and_infinities():
     """Default router on adversarial inputs.  Integer-valued x and Wr make many canonical
     logits tie exactly (the bound then keeps every tied expert a candidate and the exact
