@@ -326,64 +326,75 @@ __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, 
 }
 
 // Block of SEL_WARPS warps, tokens [tb * ntok, +ntok) (ntok <= SEL_WARPS), warp w
-// owning token w: (1) bounds and candidates per token; (2) the block's warps
-// evaluate every (token, candidate) pair together, 8 pairs per warp at a time;
-// (3) each warp selects its token's top-k on the exact values.  E <= 256.
+// owning token w: (1) bounds and candidates per token (the row's loads all in flight
+// at once); (2) the block's warps evaluate every (token, candidate) pair together,
+// 8 pairs per warp at a time; (3) each warp ranks its token's candidates on the
+// exact values (one pass over them when there are at most 32, k rounds of warp
+// arg-max over all experts otherwise).  E <= 32 NK.
+template <int NK>
 __global__ void __launch_bounds__(SEL_WARPS * 32, 3)
 router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ WrT, const float* __restrict__ part,
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
                      float cH, int ntok, float* __restrict__ logits, int32_t* __restrict__ ids,
                      float* __restrict__ w, int32_t* __restrict__ counts) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
-  __shared__ int32_t hist[MAX_E];
-  __shared__ float lg[SEL_WARPS][MAX_E];
-  __shared__ int16_t cl[SEL_WARPS][MAX_E];
+  __shared__ int32_t hist[NK * 32];
+  __shared__ float lg[SEL_WARPS][NK * 32];
+  __shared__ int16_t cl[SEL_WARPS][NK * 32];
+  __shared__ int32_t top[SEL_WARPS][MAX_K];
   __shared__ int pref[SEL_WARPS + 1];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nkey = (E + 31) >> 5;
   const int t = blockIdx.x * ntok + warp;
   const bool has_tok = warp < ntok && t < T;
   float* my_lg = lg[warp];
   int16_t* my_cl = cl[warp];
-  bool cand[MAX_E / 32];
+  bool cand[NK];
 #pragma unroll
-  for (int i = 0; i < MAX_E / 32; ++i) cand[i] = false;
+  for (int i = 0; i < NK; ++i) cand[i] = false;
   int ncand = 0;
   if (has_tok) {
-    const uint16_t* xr = x + (size_t)t * H;
-    // nx >= ||x_t||_2
+    // nx >= ||x_t||_2, 8 loads in flight per lane (they also bring the row into L1 for (2))
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const int n16 = H / 8;
     float ss = 0.0f;
-    for (int h = lane * 8; h < H; h += 256) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + h));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int m0 = lane; m0 < n16; m0 += 256) {
+      uint4 v[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ss = fmaf(bf16_lo(u[j]), bf16_lo(u[j]), ss);
-        ss = fmaf(bf16_hi(u[j]), bf16_hi(u[j]), ss);
-      }
+      for (int u = 0; u < 8; ++u)
+        if (m0 + 32 * u < n16) v[u] = __ldg(xr + m0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (m0 + 32 * u < n16) {
+          const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            ss = fmaf(bf16_lo(q[j]), bf16_lo(q[j]), ss);
+            ss = fmaf(bf16_hi(q[j]), bf16_hi(q[j]), ss);
+          }
+        }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
     const float nx = sqrtf(ss) * (1.0f + (float)H * 0x1p-21f);
     // estimates and their bounds
-    float lo_b[MAX_E / 32], hi_b[MAX_E / 32], vs[MAX_E / 32];
+    float lo_b[NK], hi_b[NK], vs[NK];
     bool bad = !isfinite(nx);
 #pragma unroll
-    for (int i = 0; i < MAX_E / 32; ++i) vs[i] = 0.0f;
+    for (int i = 0; i < NK; ++i) vs[i] = 0.0f;
 #pragma unroll 4
     for (int sp = 0; sp < S; ++sp) {   // split partials in a fixed order, many loads in flight
       const float* pp = part + ((size_t)sp * T + t) * E;
 #pragma unroll
-      for (int i = 0; i < MAX_E / 32; ++i)
-        if (i < nkey && lane + 32 * i < E) vs[i] += __ldcs(pp + lane + 32 * i);
+      for (int i = 0; i < NK; ++i)
+        if (lane + 32 * i < E) vs[i] += __ldcs(pp + lane + 32 * i);
     }
 #pragma unroll
-    for (int i = 0; i < MAX_E / 32; ++i) {
+    for (int i = 0; i < NK; ++i) {
       const int e = lane + 32 * i;
       lo_b[i] = 0.0f;
       hi_b[i] = 0.0f;
-      if (i < nkey && e < E) {
+      if (e < E) {
         const float v = vs[i];
         const float b = bias ? bias[e] : 0.0f;
         const float est = bias ? v + b : v;
@@ -397,21 +408,21 @@ router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
     bad = __any_sync(0xFFFFFFFFu, bad);
     // candidates: every expert not certainly beaten by k others
     if (!bad) {
-      uint64_t key[MAX_E / 32];
+      uint64_t key[NK];
 #pragma unroll
-      for (int i = 0; i < MAX_E / 32; ++i) {
+      for (int i = 0; i < NK; ++i) {
         const int e = lane + 32 * i;
-        key[i] = (i < nkey && e < E) ? select_key(lo_b[i], e) : 0ull;
+        key[i] = (e < E) ? select_key(lo_b[i], e) : 0ull;
       }
       const float theta = key_logit((uint32_t)(warp_kth_key(key, k) >> 32));
 #pragma unroll
-      for (int i = 0; i < MAX_E / 32; ++i) cand[i] = (i < nkey && lane + 32 * i < E) && hi_b[i] >= theta;
+      for (int i = 0; i < NK; ++i) cand[i] = (lane + 32 * i < E) && hi_b[i] >= theta;
     } else {
 #pragma unroll
-      for (int i = 0; i < MAX_E / 32; ++i) cand[i] = (i < nkey && lane + 32 * i < E);
+      for (int i = 0; i < NK; ++i) cand[i] = (lane + 32 * i < E);
     }
 #pragma unroll
-    for (int i = 0; i < MAX_E / 32; ++i) {
+    for (int i = 0; i < NK; ++i) {
       const uint32_t m = __ballot_sync(0xFFFFFFFFu, cand[i]);
       if (cand[i]) my_cl[ncand + __popc(m & ((1u << lane) - 1u))] = (int16_t)(lane + 32 * i);
       ncand += __popc(m);
@@ -441,11 +452,23 @@ router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
   }
   __syncthreads();
   if (has_tok) {
-    // exact top-k among the candidates
-    uint64_t key[MAX_E / 32];
+    // exact top-k among the candidates (keys are distinct: the expert id is part of them)
+    int my_e = 0;
+    if (ncand <= 32) {
+      const bool act = lane < ncand;
+      const int e = act ? my_cl[lane] : 0;
+      const uint64_t key = act ? select_key(my_lg[e], e) : 0ull;
+      int rank = 0;
+      for (int j = 0; j < ncand; ++j) rank += (__shfl_sync(0xFFFFFFFFu, key, j) > key) ? 1 : 0;
+      if (act && rank < k) top[warp][rank] = e;
+      __syncwarp();
+      if (lane < k) my_e = top[warp][lane];
+    } else {
+      uint64_t key[NK];
 #pragma unroll
-    for (int i = 0; i < MAX_E / 32; ++i) key[i] = cand[i] ? select_key(my_lg[lane + 32 * i], lane + 32 * i) : 0ull;
-    const int my_e = warp_select_topk(key, k, lane);
+      for (int i = 0; i < NK; ++i) key[i] = cand[i] ? select_key(my_lg[lane + 32 * i], lane + 32 * i) : 0ull;
+      my_e = warp_select_topk(key, k, lane);
+    }
     const float my_l = (lane < k) ? my_lg[my_e] : 0.0f;
     const float wt = warp_softmax_weight(my_l, k, lane);
     if (lane < k) {
@@ -458,6 +481,14 @@ router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     if (hist[i]) atomicAdd(&counts[i], hist[i]);
+}
+
+template <int NK>
+cudaError_t launch_select(dim3 grid, cudaStream_t st, const uint16_t* x, const RouterWs& rw, int S,
+                          const float* bias, int T, int H, int E, int k, float cH, int ntok, float* logits,
+                          int32_t* ids, float* w, int32_t* counts) {
+  return launch_pdl(router_select_kernel<NK>, grid, dim3(SEL_WARPS * 32), 0, st, x, rw.WrT, rw.part, S, rw.nw, bias,
+                    T, H, E, k, cH, ntok, logits, ids, w, counts);
 }
 
 }  // namespace
@@ -507,9 +538,12 @@ cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
   const int per_block = (H >= 4096) ? 5 : 7;
   int ntok = (T + num_sms - 1) / num_sms;
   ntok = ntok < 1 ? 1 : (ntok > per_block ? per_block : ntok);
-  return launch_pdl(router_select_kernel, dim3((T + ntok - 1) / ntok), dim3(SEL_WARPS * 32), 0, st, x, rw.WrT,
-                    rw.part, sp.splits, rw.nw, bias, T, H, E, k, router_bound_coef(H, sp), ntok, logits, ids, w,
-                    counts);
+  const dim3 grid((T + ntok - 1) / ntok);
+  const float cH = router_bound_coef(H, sp);
+  if (E <= 32) return launch_select<1>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
+  if (E <= 64) return launch_select<2>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
+  if (E <= 128) return launch_select<4>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
+  return launch_select<8>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
 }
 
 }  // namespace moe
