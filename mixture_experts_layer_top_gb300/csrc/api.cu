@@ -114,7 +114,7 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
   size_t sizes[N_BUFS] = {};
   sizes[B_IDS] = (size_t)R * 4;
   sizes[B_W] = (size_t)R * 4;
-  sizes[B_COUNTS] = (size_t)c.E * 4;
+  sizes[B_COUNTS] = (size_t)c.E * 4 * (1 + (c.T_max + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK);   // counts, chist
   sizes[B_OFFSETS] = (size_t)(c.E + 1) * 4;
   sizes[B_ROW_PAIR] = (size_t)R * 4;
   sizes[B_ROW_OF] = (size_t)R * 4;
@@ -212,6 +212,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->ws.ids = reinterpret_cast<int32_t*>(at(B_IDS));
   p->ws.w = reinterpret_cast<float*>(at(B_W));
   p->ws.counts = reinterpret_cast<int32_t*>(at(B_COUNTS));
+  p->ws.chist = p->ws.counts + cfg->E;
   p->ws.offsets = reinterpret_cast<int32_t*>(at(B_OFFSETS));
   p->ws.row_pair = reinterpret_cast<int32_t*>(at(B_ROW_PAIR));
   p->ws.row_of = reinterpret_cast<int32_t*>(at(B_ROW_OF));
@@ -287,7 +288,8 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
     }                                               \
   } while (0)
   rec(0);
-  MOE_CK(cudaMemsetAsync(p->ws.counts, 0, sizeof(int32_t) * E, st));
+  const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
+  MOE_CK(cudaMemsetAsync(p->ws.counts, 0, sizeof(int32_t) * E * (1 + chunks), st));   // counts and chist
   if (W_router && !(c.flags & MOE_FLAG_EXACT_LOGITS)) {
     CUtensorMap tX, tW;
     const int n_pad = ((E + 15) / 16) * 16;
@@ -297,7 +299,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
     }
     MOE_CK(launch_router_tc(tX, tW, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
                             p->bias, p->rw, T, H, E, k, p->num_sms, router_logits, p->ws.ids, p->ws.w,
-                            p->ws.counts, p->ws.err, c.timeout_ns, st));
+                            p->ws.counts, p->ws.chist, p->ws.err, c.timeout_ns, st));
     nl += 3;
   } else {
     if (W_router) {
@@ -305,7 +307,7 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
                                   p->bias, router_logits, T, H, E, st));
       ++nl;
     }
-    MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->num_sms, st));
+    MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->ws.chist, p->num_sms, st));
     ++nl;
   }
   rec(1);

@@ -17,301 +17,272 @@ namespace moe {
 namespace {
 
 constexpr int DS_THREADS = 512;
-constexpr int DS_PER_THREAD = 16;
-constexpr int DS_SPLIT = 8;              // at most this many CTAs share one expert's compaction
-constexpr int DS_ROWS_PER_PART = 256;    // an expert gets one CTA per this many of its rows
+constexpr int DS_WARPS = DS_THREADS / 32;
+constexpr int DS_SCHED_CTAS = 8;   // CTAs that build the schedule tables and share out the tile list
 
-// Block-wide exclusive scan of one int per thread (DS_THREADS threads); returns the
-// exclusive prefix and writes the block total to *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* sh_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-    if (lane >= off) inc += o;
-  }
-  if (lane == 31) sh_warp[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int s = (lane < DS_THREADS / 32) ? sh_warp[lane] : 0;
-    int si = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, si, off);
-      if (lane >= off) si += o;
-    }
-    sh_warp[lane] = si - s;   // exclusive prefix of warp totals
-    if (lane == 31) sh_warp[32] = si;
-  }
-  __syncthreads();
-  const int res = sh_warp[warp] + inc - v;
-  *total = sh_warp[32];
-  __syncthreads();   // sh_warp reusable afterwards
-  return res;
-}
-
-// Grid E * DS_SPLIT: CTA b works for expert e = b % E, part p = b / E.  The CTAs of
-// part 0 build the schedule tables of sched_build in their shared memory (in
-// parallel; identical values) and each writes its slice of the tile list.  Expert
-// e's compaction - its pairs in ascending pair order f = t*k+j, giving compact rows,
-// the padded row of each pair and the weight of that row - is split over
-// P_e = ceil(count_e / DS_ROWS_PER_PART) <= DS_SPLIT parts of the pair range; part p
-// first counts e's pairs before its range, so the order stays stable.
+// Grid DS_SCHED_CTAS + C, C = ceil(T / DS_CHUNK_TOK).
+//
+// CTAs 0 .. DS_SCHED_CTAS-1 build the schedule tables of sched_build in their shared
+// memory (identical values) and each writes its slice of the tile list and of the
+// readiness counters; CTA 0 also writes offsets[] and sched[].
+//
+// CTA DS_SCHED_CTAS + c sorts the pairs f = t*k + j of tokens c*DS_CHUNK_TOK ..
+// +DS_CHUNK_TOK-1 (a counting sort, stable: expert e's rows hold its pairs in ascending
+// f).  The first row of e in this chunk is e's first compact row plus e's pairs in
+// the chunks before, read from the router's chunk histograms chist[c][e].  Within the
+// chunk, pairs go in rounds of DS_THREADS consecutive pairs, one per thread: a pair's
+// row is (e's running row) + (e's pairs in the earlier warps of the round) + (e's
+// pairs in the earlier lanes of its warp, from __match_any_sync).
 __global__ void __launch_bounds__(DS_THREADS)
 dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, const int32_t* __restrict__ counts,
-                int T, int E, int k, int nL1, int nL2, int workers, int mode, int wave_experts, int lead,
-                int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair, int32_t* __restrict__ row_of,
-                int32_t* __restrict__ prow_of, float* __restrict__ prow_w, int32_t* __restrict__ tiles,
-                int32_t* __restrict__ sched, int32_t* __restrict__ ready) {
+                const int32_t* __restrict__ chist, int T, int E, int k, int nL1, int nL2, int workers, int mode,
+                int wave_experts, int lead, int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair,
+                int32_t* __restrict__ row_of, int32_t* __restrict__ prow_of, float* __restrict__ prow_w,
+                int32_t* __restrict__ tiles, int32_t* __restrict__ sched, int32_t* __restrict__ ready) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int R = T * k;
-  const int e = blockIdx.x % E, part = blockIdx.x / E;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int cnt_e = counts[e];
-  const int n_parts = min(DS_SPLIT, max(1, (cnt_e + DS_ROWS_PER_PART - 1) / DS_ROWS_PER_PART));
-  if (part > 0 && part >= n_parts) return;
-  __shared__ SchedTables s;
-  __shared__ int s_cum[MAX_E];          // Linear-1 tiles of experts 0..e (inclusive)
-  __shared__ int s_wstart[MAX_E + 1];   // first expert of each wave
-  __shared__ int s_W;
-  __shared__ int sh_warp[33];
-  if (part == 0) {
-  if (tid == 0) {
-    s.E = E;
-    s.nL1 = nL1;
-    s.nL2 = nL2;
-    s.mode = mode;
-  }
-  // units per expert and their exclusive prefix: warp 0, lane l owning experts 8l .. 8l+7
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // compact and padded first rows of every expert: warp 0, lane l owning experts 8l .. 8l+7
+  __shared__ int s_crow[MAX_E + 1];   // first compact row
+  __shared__ int s_units[MAX_E + 1];  // first unit (padded row / UNIT_ROWS)
+  __shared__ int s_cnt[MAX_E];
   if (tid < 32) {
-    int m[MAX_E / 32], loc = 0;
+    int m[MAX_E / 32], c[MAX_E / 32], loc_m = 0, loc_c = 0;
 #pragma unroll
     for (int i = 0; i < MAX_E / 32; ++i) {
       const int x = lane * (MAX_E / 32) + i;
-      m[i] = (x < E) ? (counts[x] + UNIT_ROWS - 1) / UNIT_ROWS : 0;
-      loc += m[i];
+      c[i] = (x < E) ? counts[x] : 0;
+      m[i] = (c[i] + UNIT_ROWS - 1) / UNIT_ROWS;
+      loc_m += m[i];
+      loc_c += c[i];
     }
-    int inc = loc;
+    int inc_m = loc_m, inc_c = loc_c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-      if (lane >= off) inc += o;
+      const int om = __shfl_up_sync(0xFFFFFFFFu, inc_m, off);
+      const int oc = __shfl_up_sync(0xFFFFFFFFu, inc_c, off);
+      if (lane >= off) {
+        inc_m += om;
+        inc_c += oc;
+      }
     }
-    int run = inc - loc;
+    int run_m = inc_m - loc_m, run_c = inc_c - loc_c;
 #pragma unroll
     for (int i = 0; i < MAX_E / 32; ++i) {
       const int x = lane * (MAX_E / 32) + i;
       if (x < E) {
-        s.cnt[x] = counts[x];
-        s.mt[x] = m[i];
-        s.mtb[x] = run;
-        s_cum[x] = (run + m[i]) * nL1;
+        s_cnt[x] = c[i];
+        s_units[x] = run_m;
+        s_crow[x] = run_c;
       }
-      run += m[i];
+      run_m += m[i];
+      run_c += c[i];
     }
     if (lane == 31) {
-      s.mtb[E] = inc;
-      s.total_mt = inc;
+      s_units[E] = inc_m;
+      s_crow[E] = inc_c;
     }
   }
-  __syncthreads();
-  // waves: the greedy rule of sched_build (a wave that starts at expert x closes at
-  // the first expert y in [x, E-2] whose Linear-1 tiles since x reach `workers`, else
-  // at E-1).  nxt[x] = y + 1 for every x in parallel, then one short pointer chase.
-  __shared__ int s_nxt[MAX_E];
-  if (mode != MOE_SCHED_PHASED && wave_experts <= 0) {
+
+  if (blockIdx.x < DS_SCHED_CTAS) {
+    // ---------------------------------------------------------------- schedule tables
+    __shared__ SchedTables s;
+    __shared__ int s_cum[MAX_E];          // Linear-1 tiles of experts 0..e (inclusive)
+    __shared__ int s_wstart[MAX_E + 1];   // first expert of each wave
+    __shared__ int s_W;
+    __syncthreads();
     for (int x = tid; x < E; x += blockDim.x) {
-      const int base = x > 0 ? s_cum[x - 1] : 0;
-      int lo = x, hi = E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_cum[mid] - base >= workers) hi = mid; else lo = mid + 1;
+      s.cnt[x] = s_cnt[x];
+      s.mt[x] = s_units[x + 1] - s_units[x];
+      s.mtb[x] = s_units[x];
+      s_cum[x] = s_units[x + 1] * nL1;
+    }
+    if (tid == 0) {
+      s.E = E;
+      s.nL1 = nL1;
+      s.nL2 = nL2;
+      s.mode = mode;
+      s.mtb[E] = s_units[E];
+      s.total_mt = s_units[E];
+    }
+    __syncthreads();
+    // waves: the greedy rule of sched_build (a wave that starts at expert x closes at
+    // the first expert y in [x, E-2] whose Linear-1 tiles since x reach `workers`, else
+    // at E-1).  nxt[x] = y + 1 for every x in parallel, then one short pointer chase.
+    __shared__ int s_nxt[MAX_E];
+    if (mode != MOE_SCHED_PHASED && wave_experts <= 0) {
+      for (int x = tid; x < E; x += blockDim.x) {
+        const int base = x > 0 ? s_cum[x - 1] : 0;
+        int lo = x, hi = E - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s_cum[mid] - base >= workers) hi = mid; else lo = mid + 1;
+        }
+        s_nxt[x] = lo + 1;
       }
-      s_nxt[x] = lo + 1;
     }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int W = 0;
-    if (mode == MOE_SCHED_PHASED) {
-      s_wstart[W++] = 0;
-    } else if (wave_experts > 0) {
-      for (int x = 0; x < E; x += wave_experts) s_wstart[W++] = x;
-    } else {
-      for (int x = 0; x < E; x = s_nxt[x]) s_wstart[W++] = x;
+    __syncthreads();
+    if (tid == 0) {
+      int W = 0;
+      if (mode == MOE_SCHED_PHASED) {
+        s_wstart[W++] = 0;
+      } else if (wave_experts > 0) {
+        for (int x = 0; x < E; x += wave_experts) s_wstart[W++] = x;
+      } else {
+        for (int x = 0; x < E; x = s_nxt[x]) s_wstart[W++] = x;
+      }
+      s_wstart[W] = E;
+      s.W = W;
+      s_W = W;
     }
-    s_wstart[W] = E;
-    s.W = W;
-    s_W = W;
-  }
-  __syncthreads();
-  const int W = s_W;
-  for (int x = tid; x < E; x += blockDim.x) {
-    int lo = 0, hi = W - 1;   // last wave whose first expert is <= x
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_wstart[mid] <= x) lo = mid; else hi = mid - 1;
+    __syncthreads();
+    const int W = s_W;
+    for (int x = tid; x < E; x += blockDim.x) {
+      int lo = 0, hi = W - 1;   // last wave whose first expert is <= x
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_wstart[mid] <= x) lo = mid; else hi = mid - 1;
+      }
+      s.wave_of[x] = lo;
     }
-    s.wave_of[x] = lo;
-  }
-  for (int v = tid; v <= W; v += blockDim.x) s.w_first_mt[v] = (v < W) ? s.mtb[s_wstart[v]] : s.mtb[E];
-  __syncthreads();
-  // segment starts (the values of sched_segments) by warp scans over the waves
-  if (tid < 32) {
-    const int D = (mode == MOE_SCHED_INTERLEAVED) ? min(max(lead, 1), W) : 0;
-    auto nmt = [&](int v) { return s.w_first_mt[v + 1] - s.w_first_mt[v]; };
-    // interleaved: pre-segments a[0..D-1] (Linear-1 of the first D waves), then merged
-    // segments b[w] = Linear-2(w) + Linear-1(w + D); otherwise a[w] = L1(w), b[w] = a[w] + L1(w)
-    int carry = 0;
-    if (mode == MOE_SCHED_INTERLEAVED) {
-      for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int v = tid; v <= W; v += blockDim.x) s.w_first_mt[v] = (v < W) ? s.mtb[s_wstart[v]] : s.mtb[E];
+    __syncthreads();
+    // segment starts (the values of sched_segments) by warp scans over the waves
+    if (tid < 32) {
+      const int D = (mode == MOE_SCHED_INTERLEAVED) ? min(max(lead, 1), W) : 0;
+      auto nmt = [&](int v) { return s.w_first_mt[v + 1] - s.w_first_mt[v]; };
+      // interleaved: pre-segments a[0..D-1] (Linear-1 of the first D waves), then merged
+      // segments b[w] = Linear-2(w) + Linear-1(w + D); otherwise a[w] = L1(w), b[w] = a[w] + L1(w)
+      int carry = 0;
+      if (mode == MOE_SCHED_INTERLEAVED) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          const int v = c0 + lane;
+          const int len = v < D ? nmt(v) * nL1 : 0;
+          int inc = len;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+            if (lane >= off) inc += o;
+          }
+          if (v < D) s.seg_a[v] = carry + inc - len;
+          carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
+        }
+      }
+      for (int c0 = 0; c0 < W; c0 += 32) {
         const int v = c0 + lane;
-        const int len = v < D ? nmt(v) * nL1 : 0;
+        int len = 0;
+        if (v < W) {
+          len = (mode == MOE_SCHED_INTERLEAVED)
+                    ? nmt(v) * nL2 + (v + D < W ? nmt(v + D) * nL1 : 0)
+                    : nmt(v) * (nL1 + nL2);
+        }
         int inc = len;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
           if (lane >= off) inc += o;
         }
-        if (v < D) s.seg_a[v] = carry + inc - len;
+        if (v < W) {
+          if (mode == MOE_SCHED_INTERLEAVED) {
+            s.seg_b[v] = carry + inc - len;
+          } else {
+            s.seg_a[v] = carry + inc - len;
+            s.seg_b[v] = carry + inc - len + nmt(v) * nL1;
+          }
+        }
         carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
       }
-    }
-    for (int c0 = 0; c0 < W; c0 += 32) {
-      const int v = c0 + lane;
-      int len = 0;
-      if (v < W) {
-        len = (mode == MOE_SCHED_INTERLEAVED)
-                  ? nmt(v) * nL2 + (v + D < W ? nmt(v + D) * nL1 : 0)
-                  : nmt(v) * (nL1 + nL2);
-      }
-      int inc = len;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-        if (lane >= off) inc += o;
-      }
-      if (v < W) {
-        if (mode == MOE_SCHED_INTERLEAVED) {
-          s.seg_b[v] = carry + inc - len;
-        } else {
-          s.seg_a[v] = carry + inc - len;
-          s.seg_b[v] = carry + inc - len + nmt(v) * nL1;
-        }
-      }
-      carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
-    }
-    if (lane == 0) {
-      s.lead = D;
-      s.n1_total = s.total_mt * nL1;
-      s.total = carry;
-    }
-  }
-  __syncthreads();
-
-  // ---- this CTA's slice of the tile list and readiness counters
-  const int per_unit = nL1 + nL2;
-  const int n_pairs = s.total_mt * per_unit;
-  for (int q = e * DS_THREADS + tid; q < n_pairs; q += E * DS_THREADS) {
-    const int g = q / per_unit, j = q - g * per_unit;
-    sched_emit_tile(s, g, sched_expert_of(s, g), j, tiles);
-  }
-  for (int g = e * DS_THREADS + tid; g < s.total_mt; g += E * DS_THREADS) ready[g] = 0;
-  }  // part == 0
-
-  // ---- compaction of expert e (rows offsets[e] .. offsets[e] + counts[e] - 1), part p:
-  // pairs [f_lo, f_hi) (boundaries on multiples of 16)
-  const int span = ((R + n_parts - 1) / n_parts + 15) & ~15;
-  const int f_lo = min(R, part * span), f_hi = min(R, f_lo + span);
-  __shared__ int c_base, c_off, s_pbase;
-  if (tid < 32) {
-    int acc = 0, u = 0;
-    for (int i = lane; i < e; i += 32) {
-      const int c = counts[i];
-      acc += c;
-      u += (c + UNIT_ROWS - 1) / UNIT_ROWS;
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-      u += __shfl_xor_sync(0xFFFFFFFFu, u, off);
-    }
-    if (lane == 0) {
-      c_base = acc;
-      c_off = acc;              // first compact row of e
-      s_pbase = u * UNIT_ROWS;  // first padded row of e
-      if (part == 0) {
-        offsets[e] = acc;
-        if (e == E - 1) {
-          offsets[E] = acc + cnt_e;
-          sched[0] = s.n1_total;
-          sched[1] = s.total;
-          sched[2] = s.total_mt;
-          sched[3] = acc + cnt_e;
-        }
+      if (lane == 0) {
+        s.lead = D;
+        s.n1_total = s.total_mt * nL1;
+        s.total = carry;
       }
     }
-  }
-  __syncthreads();
-  if (cnt_e == 0) return;
-  if (f_lo > 0) {   // e's pairs before this part's range (read and count only)
-    int c = 0;
-    for (int f = tid * 4; f < f_lo; f += DS_THREADS * 4) {
-      if ((R % 4) == 0 && f + 4 <= f_lo) {
-        const int4 q4 = *reinterpret_cast<const int4*>(ids + f);
-        c += (q4.x == e) + (q4.y == e) + (q4.z == e) + (q4.w == e);
-      } else {
-        for (int q = f; q < min(f + 4, f_lo); ++q) c += (ids[q] == e);
-      }
-    }
-    int total;
-    block_exclusive_scan(c, sh_warp, &total);
-    if (tid == 0) c_base += total;
     __syncthreads();
+    // this CTA's slice of the tile list and readiness counters
+    const int per_unit = nL1 + nL2;
+    const int n_pairs = s.total_mt * per_unit;
+    const int b = blockIdx.x;
+    for (int q = b * DS_THREADS + tid; q < n_pairs; q += DS_SCHED_CTAS * DS_THREADS) {
+      const int g = q / per_unit, j = q - g * per_unit;
+      sched_emit_tile(s, g, sched_expert_of(s, g), j, tiles);
+    }
+    for (int g = b * DS_THREADS + tid; g < s.total_mt; g += DS_SCHED_CTAS * DS_THREADS) ready[g] = 0;
+    if (b == 0) {
+      for (int x = tid; x <= E; x += blockDim.x) offsets[x] = s_crow[x];
+      if (tid == 0) {
+        sched[0] = s.n1_total;
+        sched[1] = s.total;
+        sched[2] = s.total_mt;
+        sched[3] = s_crow[E];
+      }
+    }
+    return;
   }
-  int running = c_base;
-  const int pdelta = s_pbase - c_off;   // padded row = compact row + pdelta
-  const bool vec_ok = (R % 4) == 0;
-  // this thread's DS_PER_THREAD ids of the chunk starting at `base` (-1 past f_hi)
-  auto load_ids = [&](int base, int (&v)[DS_PER_THREAD]) {
-    const int f0 = base + tid * DS_PER_THREAD;
-    if (vec_ok && f0 + DS_PER_THREAD <= f_hi) {
+
+  // ------------------------------------------------------------------ chunk c of the pairs
+  const int c = blockIdx.x - DS_SCHED_CTAS;
+  const int f_lo = c * DS_CHUNK_TOK * k, f_hi = min(R, f_lo + DS_CHUNK_TOK * k);
+  __shared__ int s_part[DS_WARPS * MAX_E];   // [G][E] chunk-prefix partial sums, then [DS_WARPS][E] per-warp counts
+  // e's pairs in chunks 0 .. c-1: thread (g, e) sums chunks g, g + G, ... (G groups of E threads)
+  const int G = DS_THREADS / E;
+  {
+    const int g = tid / E, e = tid - g * E;
+    if (g < G) {
+      int acc = 0;
+      for (int c0 = g; c0 < c; c0 += 8 * G) {
+        int v[8];
 #pragma unroll
-      for (int q = 0; q < DS_PER_THREAD / 4; ++q) {
-        const int4 p = *reinterpret_cast<const int4*>(ids + f0 + 4 * q);
-        v[4 * q] = p.x; v[4 * q + 1] = p.y; v[4 * q + 2] = p.z; v[4 * q + 3] = p.w;
+        for (int u = 0; u < 8; ++u) v[u] = (c0 + u * G < c) ? chist[(size_t)(c0 + u * G) * E + e] : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc += v[u];
       }
-    } else {
-#pragma unroll
-      for (int q = 0; q < DS_PER_THREAD; ++q) v[q] = (f0 + q < f_hi) ? ids[f0 + q] : -1;
+      s_part[g * E + e] = acc;
     }
-  };
-  constexpr int CHUNK = DS_THREADS * DS_PER_THREAD;
-  int v[DS_PER_THREAD], vn[DS_PER_THREAD];
-  load_ids(f_lo, v);
-  for (int base = f_lo; base < f_hi; base += CHUNK) {
-    if (base + CHUNK < f_hi) load_ids(base + CHUNK, vn);   // next chunk in flight during this one
-    const int f0 = base + tid * DS_PER_THREAD;
-    int c = 0;
+  }
+  __syncthreads();
+  int run = 0;   // thread e < E: compact row of e's next pair
+  int pdelta_own = 0;
+  if (tid < E) {
+    run = s_crow[tid];
+    for (int g = 0; g < G; ++g) run += s_part[g * E + tid];
+    pdelta_own = s_units[tid] * UNIT_ROWS - s_crow[tid];
+  }
+  __shared__ int s_pdelta[MAX_E];   // padded row - compact row of e
+  if (tid < E) s_pdelta[tid] = pdelta_own;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r0 = f_lo; r0 < f_hi; r0 += DS_THREADS) {
+    const int f = r0 + tid;
+    int e = f < f_hi ? ids[f] : -1;
+    if ((unsigned)e >= (unsigned)E) e = -1;   // ids come from the router, always in range; kept safe regardless
+    const bool valid = e >= 0;
+    const float wf = valid ? w[f] : 0.0f;
+    __syncthreads();   // s_part free (previous round's rows read)
+    for (int i = tid; i < DS_WARPS * E; i += DS_THREADS) s_part[i] = 0;
+    __syncthreads();
+    const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(m & lt_mask);
+    if (valid && rank == 0) s_part[warp * E + e] = __popc(m);
+    __syncthreads();
+    if (tid < E) {   // exclusive prefix over the warps, from e's running row
+      int acc = run;
 #pragma unroll
-    for (int q = 0; q < DS_PER_THREAD; ++q) c += (v[q] == e);
-    int total;
-    int pos = running + block_exclusive_scan(c, sh_warp, &total);
-#pragma unroll
-    for (int q = 0; q < DS_PER_THREAD; ++q) {
-      if (v[q] == e) {
-        const int f = f0 + q;
-        row_pair[pos] = f;
-        row_of[f] = pos;
-        prow_of[f] = pos + pdelta;
-        prow_w[pos + pdelta] = w[f];
-        ++pos;
+      for (int q = 0; q < DS_WARPS; ++q) {
+        const int t = s_part[q * E + tid];
+        s_part[q * E + tid] = acc;
+        acc += t;
       }
+      run = acc;
     }
-    running += total;
-#pragma unroll
-    for (int q = 0; q < DS_PER_THREAD; ++q) v[q] = vn[q];
+    __syncthreads();
+    const int pos = valid ? s_part[warp * E + e] + rank : 0;
+    if (valid && pos < s_crow[e + 1]) {   // rows stay in e's range even if counts and ids disagreed
+      const int prow = pos + s_pdelta[e];
+      row_pair[pos] = f;
+      row_of[f] = pos;
+      prow_of[f] = prow;
+      prow_w[prow] = wf;
+    }
   }
 }
 
@@ -401,7 +372,10 @@ cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, int num_
 
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, cudaStream_t st) {
-  return launch_pdl(dispatch_kernel, dim3(E * DS_SPLIT), dim3(DS_THREADS), 0, st, ws.ids, ws.w, ws.counts, T, E, k, I / L1_COLS, H / L2_COLS, num_sms, mode, wave_experts, lead, ws.offsets, ws.row_pair, ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready);
+  const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
+  return launch_pdl(dispatch_kernel, dim3(DS_SCHED_CTAS + chunks), dim3(DS_THREADS), 0, st, ws.ids, ws.w, ws.counts,
+                    ws.chist, T, E, k, I / L1_COLS, H / L2_COLS, num_sms, mode, wave_experts, lead, ws.offsets,
+                    ws.row_pair, ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready);
 }
 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int H, int k, uint16_t* x_pad,

@@ -32,10 +32,15 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // 256-row unit of an expert its own block (unit g owns rows 256 g .. 256 g + 255),
 // so the grouped GEMM loads and stores whole 128-row boxes without touching another
 // expert's rows.  x_pad, h_pad and P_pad are indexed by padded row.
+// Tokens per chunk of Dispatch's counting sort; the router counts each chunk's pairs
+// per expert.
+constexpr int DS_CHUNK_TOK = 128;
+
 struct Workspace {
   int32_t* ids;       // [T_max*k]
   float* w;           // [T_max*k]
   int32_t* counts;    // [E]
+  int32_t* chist;     // [ceil(T_max / DS_CHUNK_TOK) * E] expert counts per chunk of tokens (follows counts)
   int32_t* offsets;   // [E+1] compact
   int32_t* row_pair;  // [R_max] compact row -> t*k+j
   int32_t* row_of;    // [R_max] t*k+j -> compact row
@@ -107,12 +112,12 @@ RouterSplit router_split(int T, int H, int E, int num_sms);
 float router_bound_coef(int H, const RouterSplit& r);
 cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const uint16_t* Wr,
                              const float* bias, const RouterWs& rw, int T, int H, int E, int k, int num_sms,
-                             float* logits, int32_t* ids, float* w, int32_t* counts, uint32_t* err,
-                             int64_t timeout_ns, cudaStream_t st);
+                             float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* chist,
+                             uint32_t* err, int64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,
                                  int H, int E, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                        int num_sms, cudaStream_t st);
+                        int32_t* chist, int num_sms, cudaStream_t st);
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, cudaStream_t st);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int H, int k, uint16_t* x_pad,

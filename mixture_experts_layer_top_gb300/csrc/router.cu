@@ -166,17 +166,19 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
 
 constexpr int TK_WARPS = 8;
 constexpr int TK_MAX_TOK_PER_WARP = 8;
+static_assert(TK_WARPS * TK_MAX_TOK_PER_WARP <= DS_CHUNK_TOK, "a block's tokens span two chunks at most");
 
 // Top-k over caller-given (or canonical) logits: one warp per token, tpw tokens
 // per warp in turn; selection and weights as in routing.cuh.  Expert counts go
 // through a shared-memory histogram, one global atomic per (block, expert).
 __global__ void __launch_bounds__(TK_WARPS * 32)
 topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
-            float* __restrict__ w, int32_t* __restrict__ counts, int tpw) {
+            float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ chist, int tpw) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
-  __shared__ int32_t hist[MAX_E];
-  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __shared__ int32_t hist[2][MAX_E];   // expert counts of the block's tokens in its first / second chunk
+  for (int i = threadIdx.x; i < 2 * MAX_E; i += blockDim.x) hist[i / MAX_E][i % MAX_E] = 0;
   __syncthreads();
+  const int c_first = (blockIdx.x * tpw * TK_WARPS) / DS_CHUNK_TOK;   // tpw * TK_WARPS <= DS_CHUNK_TOK
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nkey = (E + 31) >> 5;
   for (int it = 0; it < tpw; ++it) {
@@ -195,12 +197,16 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __re
     if (lane < k) {
       ids[(size_t)t * k + lane] = my_e;
       w[(size_t)t * k + lane] = wt;
-      atomicAdd(&hist[my_e], 1);
+      atomicAdd(&hist[t / DS_CHUNK_TOK - c_first][my_e], 1);
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < E; i += blockDim.x)
-    if (hist[i]) atomicAdd(&counts[i], hist[i]);
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    const int h0 = hist[0][i], h1 = hist[1][i];
+    if (h0 + h1) atomicAdd(&counts[i], h0 + h1);
+    if (h0) atomicAdd(&chist[(size_t)c_first * E + i], h0);
+    if (h1) atomicAdd(&chist[(size_t)(c_first + 1) * E + i], h1);
+  }
 }
 
 }  // namespace
@@ -216,13 +222,13 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const fl
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                        int num_sms, cudaStream_t st) {
+                        int32_t* chist, int num_sms, cudaStream_t st) {
   // tokens per warp: enough blocks for two per SM, up to TK_MAX_TOK_PER_WARP tokens each
   int tpw = (T + 2 * num_sms * TK_WARPS - 1) / (2 * num_sms * TK_WARPS);
   tpw = tpw < 1 ? 1 : (tpw > TK_MAX_TOK_PER_WARP ? TK_MAX_TOK_PER_WARP : tpw);
   const int per_block = tpw * TK_WARPS;
   return launch_pdl(topk_kernel, dim3((T + per_block - 1) / per_block), dim3(TK_WARPS * 32), 0, st, logits, T, E, k, ids,
-                    w, counts, tpw);
+                    w, counts, chist, tpw);
 }
 
 }  // namespace moe

@@ -260,6 +260,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 
 // ------------------------------------------------------------------ 3. certified selection
 constexpr int SEL_WARPS = 8;
+static_assert(SEL_WARPS <= DS_CHUNK_TOK, "a block's tokens span two chunks at most");
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
@@ -336,16 +337,17 @@ __global__ void __launch_bounds__(SEL_WARPS * 32, 3)
 router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ WrT, const float* __restrict__ part,
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
                      float cH, int ntok, float* __restrict__ logits, int32_t* __restrict__ ids,
-                     float* __restrict__ w, int32_t* __restrict__ counts) {
+                     float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ chist) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
-  __shared__ int32_t hist[NK * 32];
+  __shared__ int32_t hist[2][NK * 32];   // expert counts of the block's tokens in its first / second chunk
   __shared__ float lg[SEL_WARPS][NK * 32];
   __shared__ int16_t cl[SEL_WARPS][NK * 32];
   __shared__ int32_t top[SEL_WARPS][MAX_K];
   __shared__ int pref[SEL_WARPS + 1];
-  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < 2 * NK * 32; i += blockDim.x) hist[i / (NK * 32)][i % (NK * 32)] = 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * ntok + warp;
+  const int c_first = (blockIdx.x * ntok) / DS_CHUNK_TOK;   // ntok <= DS_CHUNK_TOK: two chunks at most
   const bool has_tok = warp < ntok && t < T;
   float* my_lg = lg[warp];
   int16_t* my_cl = cl[warp];
@@ -474,21 +476,25 @@ router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
     if (lane < k) {
       ids[(size_t)t * k + lane] = my_e;
       w[(size_t)t * k + lane] = wt;
-      atomicAdd(&hist[my_e], 1);
+      atomicAdd(&hist[t / DS_CHUNK_TOK - c_first][my_e], 1);
     }
     for (int e = lane; e < E; e += 32) logits[(size_t)t * E + e] = my_lg[e];
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < E; i += blockDim.x)
-    if (hist[i]) atomicAdd(&counts[i], hist[i]);
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    const int h0 = hist[0][i], h1 = hist[1][i];
+    if (h0 + h1) atomicAdd(&counts[i], h0 + h1);
+    if (h0) atomicAdd(&chist[(size_t)c_first * E + i], h0);
+    if (h1) atomicAdd(&chist[(size_t)(c_first + 1) * E + i], h1);
+  }
 }
 
 template <int NK>
 cudaError_t launch_select(dim3 grid, cudaStream_t st, const uint16_t* x, const RouterWs& rw, int S,
                           const float* bias, int T, int H, int E, int k, float cH, int ntok, float* logits,
-                          int32_t* ids, float* w, int32_t* counts) {
+                          int32_t* ids, float* w, int32_t* counts, int32_t* chist) {
   return launch_pdl(router_select_kernel<NK>, grid, dim3(SEL_WARPS * 32), 0, st, x, rw.WrT, rw.part, S, rw.nw, bias,
-                    T, H, E, k, cH, ntok, logits, ids, w, counts);
+                    T, H, E, k, cH, ntok, logits, ids, w, counts, chist);
 }
 
 }  // namespace
@@ -521,8 +527,8 @@ float router_bound_coef(int H, const RouterSplit& r) {
 
 cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const uint16_t* Wr,
                              const float* bias, const RouterWs& rw, int T, int H, int E, int k, int num_sms,
-                             float* logits, int32_t* ids, float* w, int32_t* counts, uint32_t* err,
-                             int64_t timeout_ns, cudaStream_t st) {
+                             float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* chist,
+                             uint32_t* err, int64_t timeout_ns, cudaStream_t st) {
   const RouterSplit sp = router_split(T, H, E, num_sms);
   cudaError_t e = launch_pdl(router_prep_kernel, dim3((E + 31) / 32, H / RP_H), dim3(256), 0, st, Wr, H, E, rw.WrT);
   if (e != cudaSuccess) return e;
@@ -540,10 +546,10 @@ cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, con
   ntok = ntok < 1 ? 1 : (ntok > per_block ? per_block : ntok);
   const dim3 grid((T + ntok - 1) / ntok);
   const float cH = router_bound_coef(H, sp);
-  if (E <= 32) return launch_select<1>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
-  if (E <= 64) return launch_select<2>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
-  if (E <= 128) return launch_select<4>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
-  return launch_select<8>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts);
+  if (E <= 32) return launch_select<1>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts, chist);
+  if (E <= 64) return launch_select<2>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts, chist);
+  if (E <= 128) return launch_select<4>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts, chist);
+  return launch_select<8>(grid, st, x, rw, sp.splits, bias, T, H, E, k, cH, ntok, logits, ids, w, counts, chist);
 }
 
 }  // namespace moe
