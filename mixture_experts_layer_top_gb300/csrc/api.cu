@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -30,11 +31,33 @@ struct moe_plan_s {
   RouterWs rw;
   cudaEvent_t ev[MOE_NUM_STAGES + 1];
   bool timing;
+  // moe_forward_host: x streams in from page-locked host memory on st_aux in HOST_RANGES
+  // token ranges, each routed as soon as it has landed
+  cudaStream_t st_aux;
+  cudaEvent_t ev_fork;
+  cudaEvent_t ev_range[4];
   int last_launches;
   unsigned long long* trace;   // [gemm_grid][TRACE_SLOTS] when MOE_FLAG_TRACE
 };
 
 namespace {
+
+constexpr int HOST_RANGES = 4;   // token ranges of the pipelined host-to-device transfer
+static_assert(HOST_RANGES <= (int)(sizeof(moe_plan_s::ev_range) / sizeof(cudaEvent_t)), "one event per range");
+
+// Everything a plan holds (partially built plans included).
+void release(moe_plan_s* p) {
+  if (p->timing)
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i)
+      if (p->ev[i]) cudaEventDestroy(p->ev[i]);
+  for (int r = 0; r < HOST_RANGES; ++r)
+    if (p->ev_range[r]) cudaEventDestroy(p->ev_range[r]);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->st_aux) cudaStreamDestroy(p->st_aux);
+  if (p->base) cudaFree(p->base);
+  if (p->bias) cudaFree(p->bias);
+  if (p->trace) cudaFree(p->trace);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -145,123 +168,11 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-const char* moe_status_string(moe_status_t s) {
-  switch (s) {
-    case MOE_OK: return "ok";
-    case MOE_ERR_INVALID_ARG: return "invalid argument";
-    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
-    case MOE_ERR_CUDA: return "CUDA error";
-    case MOE_ERR_OOM: return "out of device memory";
-    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
-    case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
-  }
-  return "unknown status";
-}
-
-moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes) {
-  moe_status_t st = validate_cfg(cfg);
-  if (st != MOE_OK) return st;
-  if (!bytes) return MOE_ERR_INVALID_ARG;
-  const int64_t R = (int64_t)cfg->T_max * cfg->top_k;
-  const int64_t max_mt = max_mtiles(R, cfg->E);
-  const int64_t max_tiles = max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
-  *bytes = layout_of(*cfg, R, max_mt, max_tiles).total;
-  return MOE_OK;
-}
-
-moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
-  if (!out) return MOE_ERR_INVALID_ARG;
-  *out = nullptr;
-  moe_status_t st = validate_cfg(cfg);
-  if (st != MOE_OK) return st;
-  if (!get_encode()) return MOE_ERR_CUDA;
-  int cur = 0;
-  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_INVALID_ARG;
-  moe_plan_s* p = new (std::nothrow) moe_plan_s();
-  if (!p) return MOE_ERR_OOM;
-  p->cfg = *cfg;
-  p->cfg.router_bias = nullptr;
-  if (p->cfg.timeout_ns == 0) p->cfg.timeout_ns = 1000000000ll;
-  if (p->cfg.lead_waves == 0) p->cfg.lead_waves = 1;
-  p->device = device;
-  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device);
-  p->R_max = (int64_t)cfg->T_max * cfg->top_k;
-  p->max_mt = max_mtiles(p->R_max, cfg->E);
-  p->max_tiles = p->max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
-  p->R_pad_max = p->max_mt * UNIT_ROWS;
-  Layout L = layout_of(*cfg, p->R_max, p->max_mt, p->max_tiles);
-  p->bytes = L.total;
-  auto fail = [&](moe_status_t s) {
-    if (p->trace) cudaFree(p->trace);
-    if (p->base) cudaFree(p->base);
-    if (p->bias) cudaFree(p->bias);
-    delete p;
-    cudaSetDevice(cur);
-    return s;
-  };
-  if (cudaMalloc(&p->base, L.total) != cudaSuccess) {
-    cudaGetLastError();
-    p->base = nullptr;
-    return fail(MOE_ERR_OOM);
-  }
-  char* b = static_cast<char*>(p->base);
-  auto at = [&](Buf i) { return b + L.off[i]; };
-  p->ws.ids = reinterpret_cast<int32_t*>(at(B_IDS));
-  p->ws.w = reinterpret_cast<float*>(at(B_W));
-  p->ws.counts = reinterpret_cast<int32_t*>(at(B_COUNTS));
-  p->ws.chist = p->ws.counts + cfg->E;
-  p->ws.offsets = reinterpret_cast<int32_t*>(at(B_OFFSETS));
-  p->ws.row_pair = reinterpret_cast<int32_t*>(at(B_ROW_PAIR));
-  p->ws.row_of = reinterpret_cast<int32_t*>(at(B_ROW_OF));
-  p->ws.prow_of = reinterpret_cast<int32_t*>(at(B_PROW_OF));
-  p->ws.prow_w = reinterpret_cast<float*>(at(B_PROW_W));
-  p->ws.x_pad = reinterpret_cast<uint16_t*>(at(B_X_PAD));
-  p->ws.h_pad = reinterpret_cast<uint16_t*>(at(B_H_PAD));
-  p->ws.P_pad = reinterpret_cast<uint16_t*>(at(B_P_PAD));
-  p->ws.S_pad = reinterpret_cast<float*>(at(B_S_PAD));
-  p->ws.tiles = reinterpret_cast<int32_t*>(at(B_TILES));
-  p->ws.sched = reinterpret_cast<int32_t*>(at(B_SCHED));
-  p->ws.ready = reinterpret_cast<int32_t*>(at(B_READY));
-  p->ws.err = reinterpret_cast<uint32_t*>(at(B_ERR));
-  p->x_stage = at(B_X_STAGE);
-  p->y_stage = at(B_Y_STAGE);
-  p->rw.WrT = reinterpret_cast<uint16_t*>(at(B_WRT));
-  p->rw.nw = reinterpret_cast<float*>(at(B_NW));
-  p->rw.part = reinterpret_cast<float*>(at(B_PART));
-  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
-  if (cfg->router_bias) {
-    if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
-      cudaGetLastError();
-      p->bias = nullptr;
-      return fail(MOE_ERR_OOM);
-    }
-    if (cudaMemcpy(p->bias, cfg->router_bias, sizeof(float) * cfg->E, cudaMemcpyHostToDevice) != cudaSuccess)
-      return fail(MOE_ERR_CUDA);
-  }
-  if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess ||
-      router_tc_prepare() != cudaSuccess)
-    return fail(MOE_ERR_CUDA);
-  if (cfg->flags & MOE_FLAG_TRACE) {
-    if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid) != cudaSuccess) {
-      cudaGetLastError();
-      p->trace = nullptr;
-      return fail(MOE_ERR_OOM);
-    }
-  }
-  p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
-  if (p->timing)
-    for (int i = 0; i <= MOE_NUM_STAGES; ++i)
-      if (cudaEventCreate(&p->ev[i]) != cudaSuccess) return fail(MOE_ERR_CUDA);
-  cudaSetDevice(cur);
-  *out = p;
-  return MOE_OK;
-}
-
-moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_logits, const void* W_router,
-                         const void* W1, const void* W2, void* y, void* stream) {
+// Argument checks of moe_forward (before anything is enqueued).
+moe_status_t check_forward_args(moe_plan_t p, int32_t T, const void* x, const float* router_logits,
+                                const void* W_router, const void* W1, const void* W2, const void* y) {
   if (!p) return MOE_ERR_INVALID_ARG;
   const moe_config_t& c = p->cfg;
   if (T < 0 || T > c.T_max) return MOE_ERR_INVALID_ARG;
@@ -272,9 +183,18 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
   if (cur != p->device) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// One forward, enqueued on st.  x_src, when not null, is page-locked host memory mapped into
+// the device's address space: the layer's input is copied from it into x (the plan's staging
+// buffer) inside this call, in HOST_RANGES token ranges on st_aux, and the tensor-core router
+// starts on each range as soon as it has landed.
+moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_src, float* router_logits,
+                          const void* W_router, const void* W1, const void* W2, void* y, cudaStream_t st) {
+  const moe_config_t& c = p->cfg;
   p->last_launches = 0;
   if (T == 0) return MOE_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int k = c.top_k, E = c.E, H = c.H, I = c.I;
   int nl = 0;
   auto rec = [&](int i) {
@@ -290,17 +210,51 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   rec(0);
   const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
   MOE_CK(cudaMemsetAsync(p->ws.counts, 0, sizeof(int32_t) * E * (1 + chunks), st));   // counts and chist
-  if (W_router && !(c.flags & MOE_FLAG_EXACT_LOGITS)) {
-    CUtensorMap tX, tW;
+  const bool tc_router = W_router && !(c.flags & MOE_FLAG_EXACT_LOGITS);
+  if (x_src && !tc_router) {   // whole copy first
+    MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
+    ++nl;
+  }
+  if (tc_router) {
+    // split plan of the whole forward, whatever the ranges: the same logits either way
+    const RouterSplit sp = router_split(T, H, E, p->num_sms);
+    CUtensorMap tW;
     const int n_pad = ((E + 15) / 16) * 16;
-    if (!make_tmap(&tX, x, H, (uint64_t)T, 128) || !make_tmap(&tW, p->rw.WrT, H, (uint64_t)E, n_pad)) {
+    if (!make_tmap(&tW, p->rw.WrT, H, (uint64_t)E, n_pad)) {
       p->last_launches = nl;
       return MOE_ERR_CUDA;
     }
-    MOE_CK(launch_router_tc(tX, tW, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
-                            p->bias, p->rw, T, H, E, k, p->num_sms, router_logits, p->ws.ids, p->ws.w,
-                            p->ws.counts, p->ws.chist, p->ws.err, c.timeout_ns, st));
-    nl += 3;
+    // token ranges of whole 128-token chunks: one, or up to HOST_RANGES while x streams in
+    const int nr = x_src ? std::min(HOST_RANGES, chunks) : 1;
+    const int per = ((chunks + nr - 1) / nr) * DS_CHUNK_TOK;
+    if (x_src) {
+      MOE_CK(cudaEventRecord(p->ev_fork, st));   // the previous forward no longer reads x_stage
+      MOE_CK(cudaStreamWaitEvent(p->st_aux, p->ev_fork, 0));
+      for (int r = 0; r * per < T; ++r) {
+        const size_t off = (size_t)r * per * H * 2, n = (size_t)std::min(per, T - r * per) * H * 2;
+        MOE_CK(launch_stage_copy(static_cast<const char*>(x_src) + off, static_cast<char*>(p->x_stage) + off, n,
+                                 p->num_sms, p->st_aux));
+        MOE_CK(cudaEventRecord(p->ev_range[r], p->st_aux));
+        ++nl;
+      }
+    }
+    MOE_CK(launch_router_prep(static_cast<const uint16_t*>(W_router), H, E, p->rw, st));
+    ++nl;
+    for (int r = 0; r * per < T; ++r) {
+      const int t0 = r * per, tn = std::min(per, T - t0);
+      if (x_src) MOE_CK(cudaStreamWaitEvent(st, p->ev_range[r], 0));
+      const uint16_t* xr = static_cast<const uint16_t*>(x) + (size_t)t0 * H;
+      CUtensorMap tX;
+      if (!make_tmap(&tX, xr, H, (uint64_t)tn, 128)) {
+        p->last_launches = nl;
+        return MOE_ERR_CUDA;
+      }
+      MOE_CK(launch_router_tc(tX, tW, xr, p->bias, p->rw, sp, tn, H, E, k, p->num_sms,
+                              router_logits + (size_t)t0 * E, p->ws.ids + (size_t)t0 * k, p->ws.w + (size_t)t0 * k,
+                              p->ws.counts, p->ws.chist + (size_t)(t0 / DS_CHUNK_TOK) * E, p->ws.err, c.timeout_ns,
+                              st));
+      nl += 2;
+    }
   } else {
     if (W_router) {
       MOE_CK(launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
@@ -371,33 +325,153 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
   return MOE_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes) {
+  moe_status_t st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const int64_t R = (int64_t)cfg->T_max * cfg->top_k;
+  const int64_t max_mt = max_mtiles(R, cfg->E);
+  const int64_t max_tiles = max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  *bytes = layout_of(*cfg, R, max_mt, max_tiles).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status_t st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!get_encode()) return MOE_ERR_CUDA;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_INVALID_ARG;
+  moe_plan_s* p = new (std::nothrow) moe_plan_s();
+  if (!p) return MOE_ERR_OOM;
+  p->cfg = *cfg;
+  p->cfg.router_bias = nullptr;
+  if (p->cfg.timeout_ns == 0) p->cfg.timeout_ns = 1000000000ll;
+  if (p->cfg.lead_waves == 0) p->cfg.lead_waves = 1;
+  p->device = device;
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device);
+  p->R_max = (int64_t)cfg->T_max * cfg->top_k;
+  p->max_mt = max_mtiles(p->R_max, cfg->E);
+  p->max_tiles = p->max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  p->R_pad_max = p->max_mt * UNIT_ROWS;
+  Layout L = layout_of(*cfg, p->R_max, p->max_mt, p->max_tiles);
+  p->bytes = L.total;
+  auto fail = [&](moe_status_t s) {
+    release(p);
+    delete p;
+    cudaSetDevice(cur);
+    return s;
+  };
+  if (cudaMalloc(&p->base, L.total) != cudaSuccess) {
+    cudaGetLastError();
+    p->base = nullptr;
+    return fail(MOE_ERR_OOM);
+  }
+  char* b = static_cast<char*>(p->base);
+  auto at = [&](Buf i) { return b + L.off[i]; };
+  p->ws.ids = reinterpret_cast<int32_t*>(at(B_IDS));
+  p->ws.w = reinterpret_cast<float*>(at(B_W));
+  p->ws.counts = reinterpret_cast<int32_t*>(at(B_COUNTS));
+  p->ws.chist = p->ws.counts + cfg->E;
+  p->ws.offsets = reinterpret_cast<int32_t*>(at(B_OFFSETS));
+  p->ws.row_pair = reinterpret_cast<int32_t*>(at(B_ROW_PAIR));
+  p->ws.row_of = reinterpret_cast<int32_t*>(at(B_ROW_OF));
+  p->ws.prow_of = reinterpret_cast<int32_t*>(at(B_PROW_OF));
+  p->ws.prow_w = reinterpret_cast<float*>(at(B_PROW_W));
+  p->ws.x_pad = reinterpret_cast<uint16_t*>(at(B_X_PAD));
+  p->ws.h_pad = reinterpret_cast<uint16_t*>(at(B_H_PAD));
+  p->ws.P_pad = reinterpret_cast<uint16_t*>(at(B_P_PAD));
+  p->ws.S_pad = reinterpret_cast<float*>(at(B_S_PAD));
+  p->ws.tiles = reinterpret_cast<int32_t*>(at(B_TILES));
+  p->ws.sched = reinterpret_cast<int32_t*>(at(B_SCHED));
+  p->ws.ready = reinterpret_cast<int32_t*>(at(B_READY));
+  p->ws.err = reinterpret_cast<uint32_t*>(at(B_ERR));
+  p->x_stage = at(B_X_STAGE);
+  p->y_stage = at(B_Y_STAGE);
+  p->rw.WrT = reinterpret_cast<uint16_t*>(at(B_WRT));
+  p->rw.nw = reinterpret_cast<float*>(at(B_NW));
+  p->rw.part = reinterpret_cast<float*>(at(B_PART));
+  if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (cfg->router_bias) {
+    if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
+      cudaGetLastError();
+      p->bias = nullptr;
+      return fail(MOE_ERR_OOM);
+    }
+    if (cudaMemcpy(p->bias, cfg->router_bias, sizeof(float) * cfg->E, cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(MOE_ERR_CUDA);
+  }
+  if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess ||
+      router_tc_prepare() != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
+  if (cfg->flags & MOE_FLAG_TRACE) {
+    if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid) != cudaSuccess) {
+      cudaGetLastError();
+      p->trace = nullptr;
+      return fail(MOE_ERR_OOM);
+    }
+  }
+  p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
+  if (p->timing)
+    for (int i = 0; i <= MOE_NUM_STAGES; ++i)
+      if (cudaEventCreate(&p->ev[i]) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (cudaStreamCreateWithFlags(&p->st_aux, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
+  for (int r = 0; r < HOST_RANGES; ++r)
+    if (cudaEventCreateWithFlags(&p->ev_range[r], cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  cudaSetDevice(cur);
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_logits, const void* W_router,
+                         const void* W1, const void* W2, void* y, void* stream) {
+  const moe_status_t v = check_forward_args(p, T, x, router_logits, W_router, W1, W2, y);
+  if (v != MOE_OK) return v;
+  return forward_impl(p, T, x, nullptr, router_logits, W_router, W1, W2, y, static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float* router_logits,
                               const void* W_router, const void* W1, const void* W2, void* y_host, void* stream) {
-  if (!p) return MOE_ERR_INVALID_ARG;
-  if (T < 0 || T > p->cfg.T_max || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if (!p || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  // Page-locked buffers are reached from the kernels directly: x streams in through copy
+  // kernels (overlapping the router), Combine writes y in place.  Pageable ones go through
+  // the copy engines and the staging buffers.
+  const void* x_dev = mapped_host(x_host);
+  void* y_dev = mapped_host(y_host);
+  void* y = y_dev ? y_dev : p->y_stage;
+  const moe_status_t v = check_forward_args(p, T, p->x_stage, router_logits, W_router, W1, W2, y);
+  if (v != MOE_OK) return v;
   if (T == 0) {
     p->last_launches = 0;
     return MOE_OK;
   }
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cur != p->device) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)T * p->cfg.H * 2;
-  // Page-locked buffers are reached from the kernels directly: a copy kernel pulls x
-  // and Combine writes y in place.  Pageable ones go through the copy engines.
-  const void* x_dev = mapped_host(x_host);
-  void* y_dev = mapped_host(y_host);
-  int nl = 0;
-  if (x_dev) {
-    if (launch_stage_copy(x_dev, p->x_stage, bytes, p->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-    nl = 1;
-  } else if (cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+  if (!x_dev && cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  }
-  moe_status_t s = moe_forward(p, T, p->x_stage, router_logits, W_router, W1, W2, y_dev ? y_dev : p->y_stage,
-                               stream);
-  p->last_launches += nl;
+  const moe_status_t s = forward_impl(p, T, p->x_stage, x_dev, router_logits, W_router, W1, W2, y, st);
   if (s != MOE_OK) return s;
   if (!y_dev && cudaMemcpyAsync(y_host, p->y_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -482,11 +556,7 @@ moe_status_t moe_plan_destroy(moe_plan_t p) {
   cudaGetDevice(&cur);
   cudaSetDevice(p->device);
   cudaDeviceSynchronize();
-  if (p->timing)
-    for (int i = 0; i <= MOE_NUM_STAGES; ++i) cudaEventDestroy(p->ev[i]);
-  if (p->base) cudaFree(p->base);
-  if (p->bias) cudaFree(p->bias);
-  if (p->trace) cudaFree(p->trace);
+  release(p);
   cudaSetDevice(cur);
   delete p;
   return MOE_OK;

@@ -110,8 +110,14 @@ inline int64_t router_part_rows(int64_t T_max) {
 cudaError_t router_tc_prepare();
 RouterSplit router_split(int T, int H, int E, int num_sms);
 float router_bound_coef(int H, const RouterSplit& r);
-cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const uint16_t* Wr,
-                             const float* bias, const RouterWs& rw, int T, int H, int E, int k, int num_sms,
+// WrT = Wr^T (once per forward, before any launch_router_tc).
+cudaError_t launch_router_prep(const uint16_t* Wr, int H, int E, const RouterWs& rw, cudaStream_t st);
+// Tensor-core estimates + certified selection for T tokens starting at x (tmX covers those T
+// rows; logits, ids, w and chist point at the range's first token, which starts a 128-token
+// chunk), with the split plan sp - planned for the whole forward, so that a forward routed in
+// several ranges writes the same logits as one routed in a single call.
+cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const float* bias,
+                             const RouterWs& rw, const RouterSplit& sp, int T, int H, int E, int k, int num_sms,
                              float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* chist,
                              uint32_t* err, int64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits, int T,

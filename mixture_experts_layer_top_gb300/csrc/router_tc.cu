@@ -525,16 +525,19 @@ float router_bound_coef(int H, const RouterSplit& r) {
   return (float)(r.chain_steps + 1) * 0x1p-17f + (float)(r.n_chain * r.splits + H / 32 + 8) * 0x1p-22f;
 }
 
-cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const uint16_t* Wr,
-                             const float* bias, const RouterWs& rw, int T, int H, int E, int k, int num_sms,
+cudaError_t launch_router_prep(const uint16_t* Wr, int H, int E, const RouterWs& rw, cudaStream_t st) {
+  return launch_pdl(router_prep_kernel, dim3((E + 31) / 32, H / RP_H), dim3(256), 0, st, Wr, H, E, rw.WrT);
+}
+
+cudaError_t launch_router_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const uint16_t* x, const float* bias,
+                             const RouterWs& rw, const RouterSplit& sp, int T, int H, int E, int k, int num_sms,
                              float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* chist,
                              uint32_t* err, int64_t timeout_ns, cudaStream_t st) {
-  const RouterSplit sp = router_split(T, H, E, num_sms);
-  cudaError_t e = launch_pdl(router_prep_kernel, dim3((E + 31) / 32, H / RP_H), dim3(256), 0, st, Wr, H, E, rw.WrT);
-  if (e != cudaSuccess) return e;
   const int n_pad = ((E + 15) / 16) * 16;
-  e = launch_pdl(router_tc_kernel, dim3(sp.m_tiles, sp.splits), dim3(RTC_THREADS), RTC_SMEM, st, tmX, tmW, rw.WrT, T,
-                 H, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, rw.nw, err, timeout_ns);
+  const int m_tiles = (T + RTC_BM - 1) / RTC_BM;
+  cudaError_t e = launch_pdl(router_tc_kernel, dim3(m_tiles, sp.splits), dim3(RTC_THREADS), RTC_SMEM, st, tmX, tmW,
+                             rw.WrT, T, H, E, n_pad, sp.kb_total, sp.kb_per, sp.n_chain, rw.part, rw.nw, err,
+                             timeout_ns);
   if (e != cudaSuccess) return e;
   // tokens per block: chosen so that a block's (token, candidate) pairs mostly fit one round
   // of SEL_WARPS * 8 four-lane groups (a few more pairs would cost a whole second round).

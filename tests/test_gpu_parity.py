@@ -240,19 +240,23 @@ def test_zero_tokens_is_noop():
     del x
 
 
-@pytest.mark.parametrize("mode", ["pinned", "pinned_view", "pinned_offset8", "pageable"])
-def test_host_buffers_match_device_forward(mode):
-    """The host-buffer entry point against the device one on the same inputs: y and the
-    logits bit for bit.  Page-locked buffers at 16-byte-aligned addresses (a whole buffer,
-    a view starting 3 rows in) are read by a copy kernel and written by Combine in place
-    (one launch more); a page-locked view 8 bytes off alignment and pageable buffers go
-    through the copy engines (no extra launch).  1000 tokens: a ragged last tile."""
-    wl = synth.Workload("host", 1000, 1024, 256, 16, 4)
+@pytest.mark.parametrize("mode,T,flags", [("pinned", 1000, 0), ("pinned_view", 1000, 0), ("pinned_offset8", 1000, 0),
+                                          ("pageable", 1000, 0), ("pinned", 100, 0), ("pinned", 1000, EXACT),
+                                          ("pageable", 100, EXACT)])
+def test_host_buffers_match_device_forward(mode, T, flags):
+    """The host-buffer entry point against the device one on the same inputs: y, the logits
+    and the routing bit for bit.  Page-locked buffers at 16-byte-aligned addresses (a whole
+    buffer, a view starting 3 rows in) are read by copy kernels - in up to 4 ranges of whole
+    128-token chunks, each routed as it lands, with the split plan of the whole batch - and
+    Combine writes y in place; a page-locked view 8 bytes off alignment and pageable buffers
+    go through the copy engines (no extra launch).  The all-canonical router copies x whole."""
+    wl = synth.Workload("host", T, 1024, 256, 16, 4)
     h = synth.host_inputs(wl)
     d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
-    layer = _layer(wl)
+    layer = _layer(wl, flags=flags)
     y_dev, lg_dev = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     n_dev = layer.launch_count()
+    r_dev = {k: v.cpu() for k, v in layer.routing(T).items()}
     n = wl.T * wl.H
     pin = mode != "pageable"
     xb = torch.empty(n + 3 * wl.H, dtype=torch.bfloat16, pin_memory=pin)
@@ -265,8 +269,12 @@ def test_host_buffers_match_device_forward(mode):
     layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host, check=True)
     assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
     assert torch.equal(logits, lg_dev)
+    for k_, v in layer.routing(T).items():
+        assert torch.equal(v.cpu(), r_dev[k_]), k_
     direct = mode in ("pinned", "pinned_view")
-    assert layer.launch_count() == n_dev + (1 if direct else 0)
+    ranges = min(4, -(-T // 128))
+    extra = 0 if not direct else (1 if flags & EXACT else ranges + 2 * (ranges - 1))
+    assert layer.launch_count() == n_dev + extra
     assert torch.isnan(yb[:off]).all() and torch.isnan(yb[off + n:]).all()   # nothing outside y_host
 
 
