@@ -198,9 +198,9 @@ MOE_API const char* moe_status_string(moe_status_t s);
 
 /* Dispatch (the stable counting sort of moe_forward's Dispatch step) for callers that cannot
  * allocate device memory.  The paper has no counterpart: it exists for code that may not call
- * cudaMalloc, e.g. while a stream is being captured into a CUDA graph, under an allocator that
- * owns all device memory or a fixed memory budget, or on paths that must not risk the implicit
- * synchronisation of cudaMalloc/cudaFree.  It allocates nothing: its scratch (one row counter
+ * cudaMalloc, e.g. under an allocator that owns all device memory or a fixed memory budget (a
+ * cudaMalloc behind its back fails or breaks its accounting), or on paths that must not risk
+ * the implicit synchronisation of cudaMalloc/cudaFree.  It allocates nothing: its scratch (one row counter
  * per expert) is a fixed array of 256 counters inside the library, present on every device
  * that loads it until the process exits.
  *   ids      int32 [T,k]  expert of each (token, slot); entries outside [0,E) are not placed

@@ -4,11 +4,10 @@
 // expert e in ascending token order), but its scratch - one row counter per
 // expert - lives in a fixed array in this file instead of a plan's workspace,
 // so callers that may not call cudaMalloc can still use it.  Those are, for
-// example, code that runs while a stream is being captured into a CUDA graph
-// (allocation is not a capturable operation), runtimes whose device memory is
-// entirely owned by another allocator or capped at a fixed budget, and code
-// paths that must not risk the implicit device synchronisation cudaMalloc and
-// cudaFree can cause.
+// example, runtimes whose device memory is entirely owned by another allocator
+// or capped at a fixed budget (a cudaMalloc behind its back would fail or break
+// its accounting), and code paths that must not risk the implicit device
+// synchronisation cudaMalloc and cudaFree can cause.
 #include <cuda_runtime.h>
 
 #include <mutex>

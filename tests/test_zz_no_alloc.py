@@ -1,5 +1,6 @@
 """moe_dispatch_static: the Dispatch sort for callers that cannot allocate device
-memory (graph capture, a foreign allocator owning the pool, no-sync paths).  Its
+memory (a foreign allocator owning the pool or a fixed budget, paths that must not
+take cudaMalloc's implicit synchronisation).  Its
 output must equal the Dispatch of moe_forward exactly (integer work), on two calls
 in a row, the second starting from the first call's leftover scratch."""
 import numpy as np
