@@ -213,6 +213,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           ptx::fence_proxy_async_global();
         }
         const int nk = (ph == 0 ? args.H : args.I) / BK;
+        // a unit whose valid rows all lie in the even CTA's half: the odd CTA's A rows are
+        // padding, whose accumulator rows are never stored, so they are not loaded at all
+        const bool a_odd_empty = (tl.x >> 16) <= BM;
+        const bool load_a = !(rank == 1 && a_odd_empty);
+        const uint32_t stage_tx = PAIR * PSTAGE_BYTES - (a_odd_empty ? A_STAGE_BYTES : 0);
         const CUtensorMap* tA = ph == 0 ? &tmA1 : &tmA2;
         const CUtensorMap* tB = ph == 0 ? &tmB1 : &tmB2;
         const int brow0 = e * (ph == 0 ? args.H : args.I);
@@ -225,10 +230,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           uint8_t* sA = smem + stage * PSTAGE_BYTES;
           uint8_t* sB = sA + A_STAGE_BYTES;
           const uint32_t full_pair = ptx::mapa_shared(&ctl->full[stage], 0);
-          if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], PAIR * PSTAGE_BYTES);
+          if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], stage_tx);
           // the whole 128-row box even when some rows are padding: skipping the padding
           // rows' 32-row quadrants measured slower (fine workload 0.483 -> 0.512 ms)
-          ptx::tma_load_2d_pair(tA, full_pair, sA, kb * BK, row0, pol_a);
+          if (load_a) ptx::tma_load_2d_pair(tA, full_pair, sA, kb * BK, row0, pol_a);
           ptx::tma_load_2d_pair(tB, full_pair, sB, c0, brow0 + kb * BK, pol_w);
           ptx::tma_load_2d_pair(tB, full_pair, sB + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
           filled_mask |= 1u << stage;
