@@ -15,6 +15,15 @@ outputs of a bf16-intermediate computation:
   cores vs sequential); ~5e-4 of h elements round to a neighbouring bf16 value,
   and one such flip of a large |h| moves an output by ~0.5% of RMS, which is
   >3e-2 relative on the rare output near 0.1 * RMS that the top-k sum cancels.
+* explained outliers (check_y_explained): where the GPU's h is available, elements
+  beyond that allowance pass only if h explains them - every GPU h element within
+  2e-2 * RMS(h) + ulp of the oracle's (the absolute rule of y, applied to h: near
+  g = 0 the accumulation order alone moves silu(g) * u by many ulps, harmlessly),
+  at most 2e-3 of them different at all, and y within the same tolerance of the
+  oracle's Linear-2 and Combine applied to the GPU's h.
+  With k = 1 nothing dilutes a flip: one flipped h element of a token moves its
+  whole output row (measured: 7 of 127,037 elements at 3-4.5% relative, all in
+  the row of the one token with a flipped element).
 
 Routing (ids, counts, offsets, row_pair, row_of) must be bit-exact; router
 weights within 1e-6 relative (the GPU's exp is not the host's).  Logits: with
@@ -66,6 +75,39 @@ def check_y(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: str = "y"):
     assert rel.size == 0 or rel.max() <= 6e-2, f"{what}: max rel err {rel.max():.3e} > 6e-2"
     return dict(max_abs=float(d.max()), rms=rms, max_rel=float(rel.max()) if rel.size else 0.0,
                 n_rel_over=n_over)
+
+
+def check_y_explained(y_gpu_bits: np.ndarray, ref: dict, h_gpu_bits: np.ndarray, W2_bits: np.ndarray,
+                      what: str = "y"):
+    """check_y against the oracle; outliers beyond its relative allowance are accepted only
+    when the GPU's bf16 intermediate h explains them (see the module docstring).
+    ref: the oracle's result with intermediates; h_gpu_bits: [T*k, I] in compact row order;
+    W2_bits: [E, I, H]."""
+    try:
+        check_y(y_gpu_bits, ref["y"], what)
+        return
+    except AssertionError as first:
+        failure = first
+    T, k, I = ref["a"].shape
+    row_of = ref["row_of"].reshape(T, k)
+    hg = f64(h_gpu_bits)[row_of]                        # [T, k, I]
+    ha = f64(ref["a"])
+    dh = np.abs(hg - ha)
+    rms_h = float(np.sqrt(np.mean(ha ** 2)))
+    assert np.all(dh <= 2e-2 * rms_h + bf16_ulp(ha)), \
+        f"{what}: h differs from the oracle's beyond 2e-2 * RMS(h) + ulp ({failure})"
+    frac = float((dh != 0).mean())
+    assert frac <= 2e-3, f"{what}: {frac:.2e} of h elements differ from the oracle's ({failure})"
+    E, _, H = W2_bits.shape
+    y_alt = np.zeros((T, H), dtype=np.float64)
+    for e in np.unique(ref["ids"]):
+        W2e = f64(W2_bits[e])                           # [I, H]
+        for j in range(k):
+            sel = np.nonzero(ref["ids"][:, j] == e)[0]
+            if sel.size:
+                y_alt[sel] += ref["w"][sel, j].astype(np.float64)[:, None] * (hg[sel, j, :] @ W2e)
+    y_alt_bits = oracle.f32_to_bf16(y_alt.astype(np.float32))
+    check_y(y_gpu_bits, y_alt_bits, what + " (from the GPU's h)")
 
 
 def routing_equal(gpu: dict, ref: dict, T: int):

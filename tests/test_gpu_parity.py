@@ -10,7 +10,8 @@ import torch
 import mixture_experts_layer_top_gb300 as moe
 import oracle
 import synth
-from helpers import bits, check_logits, check_y, f64, from_bits, oracle_for, routing_equal, sample_tokens
+from helpers import (bits, check_logits, check_y, check_y_explained, f64, from_bits, oracle_for, routing_equal,
+                     sample_tokens)
 
 EXACT = moe.MOE_FLAG_EXACT_LOGITS
 
@@ -229,6 +230,43 @@ def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
         check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
     routing_equal(layer.routing(T), ref, T)
     check_y(bits(y), ref["y"])
+
+
+def _random_cases(n: int, seed: int = 20261202):
+    """Seeded layer shapes within the library's limits: H a multiple of 256, I of 128, E up
+    to 64, k up to min(8, E), T up to 300 with a larger T_max, any schedule, the default or
+    all-canonical router or the compute ring split, a Zipf router bias on some."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        E = int(rng.integers(1, 65))
+        out.append(dict(T=int(rng.integers(1, 301)), H=int(rng.choice([256, 512, 768, 1024])),
+                        I=int(rng.choice([128, 256, 384, 512])), E=E, k=int(rng.integers(1, min(8, E) + 1)),
+                        sched=int(rng.integers(0, 4)), extra=int(rng.integers(0, 200)),
+                        flags=[0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE][int(rng.integers(0, 3))],
+                        zipf=float(rng.choice([0.0, 1.2]))))
+    return out
+
+
+@pytest.mark.parametrize("c", _random_cases(10), ids=lambda c: "T{T}-H{H}-I{I}-E{E}-k{k}-s{sched}-f{flags}-z{zipf}".format(**c))
+def test_random_shapes_full_oracle(c):
+    """Routing (bit-exact) and y (stated tolerance) against the full oracle on seeded random
+    shapes, schedules and kernel variants, with the plan sized above the batch."""
+    wl = synth.Workload("rand", c["T"], c["H"], c["I"], c["E"], c["k"], zipf_s=c["zipf"])
+    h = synth.host_inputs(wl)
+    bias = _bias(wl)
+    ref = oracle_for(wl, h["x"], h["Wr"], bias, None, full_weights=(h["W1"], h["W2"]), want_intermediates=True)
+    layer = _layer(wl, c["sched"], flags=c["flags"], T_max=c["T"] + c["extra"], bias=bias)
+    d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    if c["flags"] & EXACT:
+        assert np.array_equal(logits.cpu().numpy(), ref["logits"])
+    else:
+        check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(c["T"]), bias)
+    routing_equal(layer.routing(c["T"]), ref, c["T"])
+    h_gpu, _ = layer.intermediates(c["T"], want_P=False)
+    check_y_explained(bits(y), ref, bits(h_gpu), h["W2"])
+    layer.close()
 
 
 def test_zero_tokens_is_noop():
