@@ -19,8 +19,11 @@ outputs of a bf16-intermediate computation:
   beyond that allowance pass only if h explains them - every GPU h element within
   2e-2 * RMS(h) + ulp of the oracle's (the absolute rule of y, applied to h: near
   g = 0 the accumulation order alone moves silu(g) * u by many ulps, harmlessly),
-  at most 2e-3 of them different at all, and y within the same tolerance of the
-  oracle's Linear-2 and Combine applied to the GPU's h.
+  at most H * 2^-18 of them different at all (the share of fp32 sums close enough
+  to a bf16 rounding boundary for the summation order to matter grows with the
+  reduction length H: measured 5e-4 at H = 512 and 2.1e-3 at H = 2048, caps 2e-3
+  and 7.8e-3), and y within the same tolerance of the oracle's Linear-2 and
+  Combine applied to the GPU's h.
   With k = 1 nothing dilutes a flip: one flipped h element of a token moves its
   whole output row (measured: 7 of 127,037 elements at 3-4.5% relative, all in
   the row of the one token with a flipped element).
@@ -97,7 +100,9 @@ def check_y_explained(y_gpu_bits: np.ndarray, ref: dict, h_gpu_bits: np.ndarray,
     assert np.all(dh <= 2e-2 * rms_h + bf16_ulp(ha)), \
         f"{what}: h differs from the oracle's beyond 2e-2 * RMS(h) + ulp ({failure})"
     frac = float((dh != 0).mean())
-    assert frac <= 2e-3, f"{what}: {frac:.2e} of h elements differ from the oracle's ({failure})"
+    H = W2_bits.shape[2]
+    cap = H * 2.0 ** -18          # grows with Linear-1's reduction length H (see the module docstring)
+    assert frac <= cap, f"{what}: {frac:.2e} of h elements differ from the oracle's, above {cap:.2e} ({failure})"
     E, _, H = W2_bits.shape
     y_alt = np.zeros((T, H), dtype=np.float64)
     for e in np.unique(ref["ids"]):

@@ -239,26 +239,34 @@ def _random_cases(n: int, seed: int = 20261202):
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(n):
-        E = int(rng.integers(1, 65))
-        out.append(dict(T=int(rng.integers(1, 301)), H=int(rng.choice([256, 512, 768, 1024])),
+        E = int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(65, 257))]))
+        out.append(dict(T=int(rng.integers(1, 301)), H=int(rng.choice([256, 512, 768, 1024, 2048])),
                         I=int(rng.choice([128, 256, 384, 512])), E=E, k=int(rng.integers(1, min(8, E) + 1)),
                         sched=int(rng.integers(0, 4)), extra=int(rng.integers(0, 200)),
                         flags=[0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE][int(rng.integers(0, 3))],
-                        zipf=float(rng.choice([0.0, 1.2]))))
+                        zipf=float(rng.choice([0.0, 1.2])), host=bool(rng.integers(0, 3) == 0)))
     return out
 
 
-@pytest.mark.parametrize("c", _random_cases(10), ids=lambda c: "T{T}-H{H}-I{I}-E{E}-k{k}-s{sched}-f{flags}-z{zipf}".format(**c))
+@pytest.mark.parametrize("c", _random_cases(24),
+                         ids=lambda c: "T{T}-H{H}-I{I}-E{E}-k{k}-s{sched}-f{flags}-z{zipf}-h{host:d}".format(**c))
 def test_random_shapes_full_oracle(c):
     """Routing (bit-exact) and y (stated tolerance) against the full oracle on seeded random
-    shapes, schedules and kernel variants, with the plan sized above the batch."""
+    shapes, schedules and kernel variants, with the plan sized above the batch; a third of
+    the cases through the host-buffer entry point (page-locked x and y)."""
     wl = synth.Workload("rand", c["T"], c["H"], c["I"], c["E"], c["k"], zipf_s=c["zipf"])
     h = synth.host_inputs(wl)
     bias = _bias(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], bias, None, full_weights=(h["W1"], h["W2"]), want_intermediates=True)
     layer = _layer(wl, c["sched"], flags=c["flags"], T_max=c["T"] + c["extra"], bias=bias)
     d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
-    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    if c["host"]:
+        x_host = d["x"].cpu().pin_memory()
+        y = torch.empty((c["T"], c["H"]), dtype=torch.bfloat16).pin_memory()
+        logits = torch.empty((c["T"], c["E"]), dtype=torch.float32, device="cuda")
+        layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y, check=True)
+    else:
+        y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     if c["flags"] & EXACT:
         assert np.array_equal(logits.cpu().numpy(), ref["logits"])
     else:
