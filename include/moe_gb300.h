@@ -34,6 +34,15 @@
  * no kernel of this library traps or spins without a time limit.
  *
  * Threading: a plan may be used by one stream at a time.
+ *
+ * Concurrency between plans: the grouped GEMM is one persistent launch sized to the SMs,
+ * and with MOE_SCHED_WAVE_SERIAL, MOE_SCHED_INTERLEAVED and MOE_SCHED_AUTO its Linear-2 tiles
+ * wait for Linear-1 tiles that other CTAs of the same launch compute, so all its CTAs must
+ * be resident together.  Forwards of different plans on one device may overlap (different
+ * streams, no ordering) only if every overlapping plan uses MOE_SCHED_PHASED, whose two
+ * launches never wait on other CTAs; otherwise order them (one stream, or events): two such
+ * GEMMs that each got part of the SMs can wait on each other until timeout_ns expires and
+ * the forward reports MOE_ERR_TIMEOUT.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

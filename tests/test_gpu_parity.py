@@ -277,6 +277,33 @@ def test_random_shapes_full_oracle(c):
     layer.close()
 
 
+def test_phased_plans_overlap_on_two_streams():
+    """Two plans with the phased schedule, forwards enqueued on two streams without ordering
+    (the overlap the header allows): each result bitwise equal to the plan's solo forward."""
+    wls = [synth.Workload("ovA", 2048, 1024, 512, 32, 4), synth.Workload("ovB", 1500, 768, 384, 20, 6)]
+    ins = [synth.device_inputs(wl) for wl in wls]
+    layers = [_layer(wl, moe.MOE_SCHED_PHASED) for wl in wls]
+    solo = []
+    for layer, d in zip(layers, ins):
+        y, _ = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+        solo.append(y.view(torch.int16).clone())
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = [[], []]
+    for _ in range(3):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                y, _ = layers[i].forward(ins[i]["x"], ins[i]["Wr"], ins[i]["W1"], ins[i]["W2"])
+                outs[i].append(y)
+    torch.cuda.synchronize()
+    for i in range(2):
+        with torch.cuda.stream(streams[i]):
+            layers[i].check()
+        for y in outs[i]:
+            assert torch.equal(y.view(torch.int16), solo[i]), f"plan {i} differs when overlapped"
+        layers[i].close()
+
+
 def test_zero_tokens_is_noop():
     wl = synth.WORKLOADS["tiny"]
     layer = _layer(wl)
