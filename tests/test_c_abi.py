@@ -1,0 +1,32 @@
+"""The C ABI from plain C: tests/c_abi_check.c is compiled as C99 against include/moe_gb300.h,
+linked to the built libmoe_gb300.so and run; it exercises the calls that need no GPU
+(workspace sizing and validation, status strings, the host schedule)."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import mixture_experts_layer_top_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib_dir():
+    moe.build()
+    return os.path.dirname(moe.LIB_PATH)
+
+
+def test_plain_c_caller_compiles_links_and_runs(lib_dir, tmp_path):
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "c_abi_check")
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c_abi_check.c"), "-L", lib_dir, "-lmoe_gb300",
+           "-Wl,-rpath," + lib_dir, "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
