@@ -231,8 +231,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
           uint8_t* sB = sA + A_STAGE_BYTES;
           const uint32_t full_pair = ptx::mapa_shared(&ctl->full[stage], 0);
           if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], stage_tx);
-          // the whole 128-row box even when some rows are padding: skipping the padding
-          // rows' 32-row quadrants measured slower (fine workload 0.483 -> 0.512 ms)
+          // the whole 128-row box even when some rows are padding: loading only the valid
+          // rows' 32-row quadrants measured slower (fine workload 0.483 -> 0.512 ms), and so
+          // did one 32-row box for a CTA with at most 32 valid rows (large 3.91 -> 4.03 ms)
           if (load_a) ptx::tma_load_2d_pair(tA, full_pair, sA, kb * BK, row0, pol_a);
           ptx::tma_load_2d_pair(tB, full_pair, sB, c0, brow0 + kb * BK, pol_w);
           ptx::tma_load_2d_pair(tB, full_pair, sB + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
