@@ -106,6 +106,9 @@ typedef enum {
  *   cH from moe_router_bound (at most (H/16 + 1) 2^-17 + (H/32 + 8 + 64) 2^-22).
  * MOE_FLAG_EXACT_LOGITS evaluates every logit in the canonical order on the CUDA cores. */
 #define MOE_FLAG_EXACT_LOGITS (1u << 5)
+#define MOE_FLAG_TEST_BAD_ID (1u << 9)  /* test only: Dispatch sees the first (token, slot) pair's expert
+                                          id out of range; the pair is dropped, no access leaves the
+                                          workspace, and moe_get_status reports MOE_ERR_DEVICE_CHECK */
 #define MOE_FLAG_TEST_STALL (1u << 8)   /* test only: Linear-2 tiles wait for a readiness count that
                                            is never reached, so the bounded wait expires and
                                            moe_get_status reports MOE_ERR_TIMEOUT (no GPU fault)   */

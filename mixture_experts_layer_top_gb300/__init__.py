@@ -43,6 +43,7 @@ MOE_FLAG_EXACT_LOGITS = 1 << 5
 TRACE_FIELDS = ("prod_wait_empty_ns", "prod_wait_ready_ns", "mma_wait_tempty_ns", "mma_wait_full_ns",
                 "epi_wait_tfull_ns", "cta_ns", "tiles_l1", "tiles_l2")
 MOE_FLAG_TEST_STALL = 1 << 8
+MOE_FLAG_TEST_BAD_ID = 1 << 9
 
 MOE_NUM_STAGES = 5
 STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")

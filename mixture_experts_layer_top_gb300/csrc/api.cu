@@ -133,7 +133,9 @@ struct Layout {
 };
 
 Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_tiles) {
-  const int64_t Rp = max_mt * UNIT_ROWS;   // padded rows
+  // padded rows, plus the dead row (index max_mt * UNIT_ROWS: no unit reaches it; P and its
+  // scale are zero there) that Dispatch gives a pair it cannot place
+  const int64_t Rp = max_mt * UNIT_ROWS + 1;
   size_t sizes[N_BUFS] = {};
   sizes[B_IDS] = (size_t)R * 4;
   sizes[B_W] = (size_t)R * 4;
@@ -268,7 +270,8 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   // schedule actually run: MOE_SCHED_AUTO resolves to wave-serial with one wave of all experts
   const int sched_mode = (c.schedule == MOE_SCHED_AUTO) ? MOE_SCHED_WAVE_SERIAL : c.schedule;
   const int sched_we = (c.schedule == MOE_SCHED_AUTO) ? E : c.wave_experts;
-  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, sched_mode, sched_we, c.lead_waves, st));
+  MOE_CK(launch_dispatch(p->ws, T, E, k, H, I, p->gemm_grid / PAIR, sched_mode, sched_we, c.lead_waves,
+                         (int)p->R_pad_max, (c.flags & MOE_FLAG_TEST_BAD_ID) != 0, st));
   ++nl;
   rec(2);
   MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.prow_of, T, H, k, p->ws.x_pad, st));
@@ -412,6 +415,12 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->rw.nw = reinterpret_cast<float*>(at(B_NW));
   p->rw.part = reinterpret_cast<float*>(at(B_PART));
   if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  {   // the dead row: P and its scales zero, so a pair sent there adds nothing in Combine
+    const size_t dead = (size_t)p->R_pad_max, nS = (size_t)(cfg->H / P_SCALE_COLS);
+    if (cudaMemset(p->ws.P_pad + dead * cfg->H, 0, (size_t)cfg->H * 2) != cudaSuccess ||
+        cudaMemset(p->ws.S_pad + dead * nS, 0, nS * 4) != cudaSuccess)
+      return fail(MOE_ERR_CUDA);
+  }
   if (cfg->router_bias) {
     if (cudaMalloc(&p->bias, sizeof(float) * cfg->E) != cudaSuccess) {
       cudaGetLastError();
@@ -511,7 +520,8 @@ moe_status_t moe_debug_intermediates(moe_plan_t p, int32_t T, void* h, float* P,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t R = (size_t)T * p->cfg.top_k;
   if (R && (h || P) &&
-      launch_compact_intermediates(p->ws.row_pair, p->ws.prow_of, (int)R, p->cfg.H, p->cfg.I, p->ws.h_pad,
+      launch_compact_intermediates(p->ws.row_pair, p->ws.prow_of, (int)R, (int)p->R_pad_max + 1, p->cfg.H, p->cfg.I,
+                                   p->ws.h_pad,
                                    p->ws.P_pad, p->ws.S_pad, static_cast<uint16_t*>(h), P, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;

@@ -38,7 +38,8 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
                 const int32_t* __restrict__ chist, int T, int E, int k, int nL1, int nL2, int workers, int mode,
                 int wave_experts, int lead, int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair,
                 int32_t* __restrict__ row_of, int32_t* __restrict__ prow_of, float* __restrict__ prow_w,
-                int32_t* __restrict__ tiles, int32_t* __restrict__ sched, int32_t* __restrict__ ready) {
+                int32_t* __restrict__ tiles, int32_t* __restrict__ sched, int32_t* __restrict__ ready,
+                uint32_t* __restrict__ err, int dead_row, int test_bad_id) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int R = T * k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -254,7 +255,14 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
   for (int r0 = f_lo; r0 < f_hi; r0 += DS_THREADS) {
     const int f = r0 + tid;
     int e = f < f_hi ? ids[f] : -1;
-    if ((unsigned)e >= (unsigned)E) e = -1;   // ids come from the router, always in range; kept safe regardless
+    if (test_bad_id && f == 0) e = E;         // test only: one pair's expert id out of range
+    if (f < f_hi && (unsigned)e >= (unsigned)E) {
+      // ids come from the router and are always in range; an inconsistent one is reported,
+      // and its pair gets the dead row (zero P, no tile: Combine adds nothing for it)
+      atomicOr(err, ERR_CHECK);
+      prow_of[f] = dead_row;
+      e = -1;
+    }
     const bool valid = e >= 0;
     const float wf = valid ? w[f] : 0.0f;
     __syncthreads();   // s_part free (previous round's rows read)
@@ -282,6 +290,9 @@ dispatch_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, co
       row_of[f] = pos;
       prow_of[f] = prow;
       prow_w[prow] = wf;
+    } else if (valid) {                   // more pairs of e than the router counted: reported
+      atomicOr(err, ERR_CHECK);
+      prow_of[f] = dead_row;
     }
   }
 }
@@ -334,13 +345,21 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ p
 // (P as fp32: the stored fp16 value times its block's power-of-two scale, exact).
 __global__ void __launch_bounds__(256)
 compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t* __restrict__ prow_of, int R,
-                             int H, int I, const uint16_t* __restrict__ h_pad, const uint16_t* __restrict__ P_pad,
-                             const float* __restrict__ S_pad, uint16_t* __restrict__ h, float* __restrict__ P) {
+                             int R_pad, int H, int I, const uint16_t* __restrict__ h_pad,
+                             const uint16_t* __restrict__ P_pad, const float* __restrict__ S_pad,
+                             uint16_t* __restrict__ h, float* __restrict__ P) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
   const int f = row_pair[row];
-  const size_t pr = (size_t)prow_of[f];
+  // after inconsistent routing (reported by Dispatch) a compact row may hold no pair: zeros
+  const int32_t prr = ((unsigned)f < (unsigned)R) ? prow_of[f] : -1;
+  if ((unsigned)prr >= (unsigned)R_pad) {
+    if (h)
+      for (int i = lane; i < I / 8; i += 32) reinterpret_cast<uint4*>(h + (size_t)row * I)[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const size_t pr = (size_t)prr;
   if (h)
     for (int i = lane; i < I / 8; i += 32)
       reinterpret_cast<uint4*>(h + (size_t)row * I)[i] = reinterpret_cast<const uint4*>(h_pad + pr * I)[i];
@@ -383,11 +402,12 @@ cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, int num_
 }
 
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
-                            int wave_experts, int lead, cudaStream_t st) {
+                            int wave_experts, int lead, int dead_row, bool test_bad_id, cudaStream_t st) {
   const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
   return launch_pdl(dispatch_kernel, dim3(DS_SCHED_CTAS + chunks), dim3(DS_THREADS), 0, st, ws.ids, ws.w, ws.counts,
                     ws.chist, T, E, k, I / L1_COLS, H / L2_COLS, num_sms, mode, wave_experts, lead, ws.offsets,
-                    ws.row_pair, ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready);
+                    ws.row_pair, ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready, ws.err, dead_row,
+                    test_bad_id ? 1 : 0);
 }
 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int H, int k, uint16_t* x_pad,
@@ -396,10 +416,11 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int 
   return launch_pdl(gather_rows_kernel, dim3((T * nch + 7) / 8), dim3(256), 0, st, x, prow_of, T, H, k, x_pad);
 }
 
-cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,
-                                         const uint16_t* h_pad, const uint16_t* P_pad, const float* S_pad,
+cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int R_pad, int H,
+                                         int I, const uint16_t* h_pad, const uint16_t* P_pad, const float* S_pad,
                                          uint16_t* h, float* P, cudaStream_t st) {
-  compact_intermediates_kernel<<<(R + 7) / 8, 256, 0, st>>>(row_pair, prow_of, R, H, I, h_pad, P_pad, S_pad, h, P);
+  compact_intermediates_kernel<<<(R + 7) / 8, 256, 0, st>>>(row_pair, prow_of, R, R_pad, H, I, h_pad, P_pad, S_pad, h,
+                                                             P);
   return cudaGetLastError();
 }
 

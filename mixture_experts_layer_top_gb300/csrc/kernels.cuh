@@ -124,13 +124,17 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* Wr, const fl
                                  int H, int E, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
                         int32_t* chist, int num_sms, cudaStream_t st);
+// A pair that inconsistent routing leaves without a row (reported as ERR_CHECK) gets dead_row:
+// a padded row past every unit whose P and scale are zero.  test_bad_id (test only): Dispatch
+// sees pair 0's expert id out of range.
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
-                            int wave_experts, int lead, cudaStream_t st);
+                            int wave_experts, int lead, int dead_row, bool test_bad_id, cudaStream_t st);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int H, int k, uint16_t* x_pad,
                           cudaStream_t st);
 // bytes a multiple of 16, both pointers 16-byte aligned; src may be mapped host memory.
 cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st);
-cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int H, int I,
+cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int R_pad, int H,
+                                         int I,
                                          const uint16_t* h_pad, const uint16_t* P_pad, const float* S_pad,
                                          uint16_t* h, float* P,
                                          cudaStream_t st);

@@ -304,6 +304,31 @@ def test_phased_plans_overlap_on_two_streams():
         layers[i].close()
 
 
+def test_inconsistent_routing_reported_and_contained():
+    """A test-only flag makes Dispatch see the first (token, slot) pair with an out-of-range
+    expert id: moe_get_status reports MOE_ERR_DEVICE_CHECK, that pair is dropped without any
+    access outside the workspace, every other token's y is bitwise the clean forward's, and
+    the context stays usable (a clean forward afterwards matches the oracle)."""
+    wl = synth.WORKLOADS["tiny"]
+    h = synth.host_inputs(wl)
+    d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
+    good = _layer(wl)
+    y_good, _ = good.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    bad = _layer(wl, flags=moe.MOE_FLAG_TEST_BAD_ID)
+    y_bad, _ = bad.forward(d["x"], d["Wr"], d["W1"], d["W2"])
+    assert moe.moe_get_status(bad.plan, bad._stream()) == moe.MOE_ERR_DEVICE_CHECK
+    assert moe.moe_get_status(bad.plan, bad._stream()) == moe.MOE_OK          # the word is cleared
+    assert torch.equal(y_bad[1:].view(torch.int16), y_good[1:].view(torch.int16))
+    assert torch.isfinite(y_bad[0].float()).all()
+    h_bad, P_bad = bad.intermediates(wl.T)                                      # debug copies stay in bounds
+    torch.cuda.synchronize()
+    bad.close()
+    y2, _ = good.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    check_y(bits(y2), ref["y"])
+    good.close()
+
+
 def test_zero_tokens_is_noop():
     wl = synth.WORKLOADS["tiny"]
     layer = _layer(wl)
