@@ -256,3 +256,19 @@ def test_identity_experts_closed_form(scaled):
     expect = 4.0 * xf ** 2 * cw[:, None]
     y = bits_to_f64(res["y"])
     assert np.all(np.abs(y / expect - 1.0) <= 3 * 2.0 ** -8)
+
+
+def test_oracle_matches_its_regression_record():
+    """The oracle on the seeded tiny workload equals the record tests/golden/make_golden.py
+    wrote (a change detector for the oracle and the generator, not a pin: see the README
+    there).  A deliberate change to the oracle's arithmetic is rerecorded with that script."""
+    import importlib.util
+    import json
+    import os
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_golden", os.path.join(here, "make_golden.py"))
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    with open(os.path.join(here, "oracle_tiny.json")) as f:
+        want = json.load(f)
+    assert mg.record() == want
