@@ -59,3 +59,30 @@ def test_clock_summary_flags_throttling():
 def test_workload_flops():
     wl = bench.synth.WORKLOADS["fine"]
     assert wl.useful_flops() == pytest.approx(6 * 2048 * 768 * 8192 * 8 + 2 * 2048 * 128 * 8192)
+
+
+def _reference_arm(rank: int):
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="2", RANK=str(rank), LOCAL_RANK=str(rank))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                           "--steps", "1", "--warmup", "0"], cwd=ROOT, env=env, capture_output=True, text=True,
+                          timeout=600)
+
+
+def test_reference_arm_rank0_prints_one_line_other_ranks_exit_quietly():
+    """The reference arm (the oracle timed on the host cores): under a launcher only rank 0
+    works and prints one JSON line with the contract's keys; any other rank exits 0 silently."""
+    import json
+    r1 = _reference_arm(1)
+    assert r1.returncode == 0 and r1.stdout.strip() == "", r1.stderr[-2000:]
+    r0 = _reference_arm(0)
+    assert r0.returncode == 0, r0.stderr[-2000:]
+    lines = [ln for ln in r0.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["higher_is_better"] is True and d["steps"] == 1 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("tiny")
