@@ -106,7 +106,7 @@ def test_bilinear_integer_exact():
 
 @pytest.mark.parametrize("exp2", [20, -30])
 def test_expert_outputs_far_outside_fp16_range(exp2):
-    """P is stored as fp16 times a power-of-two scale per (row, 256 columns): W2 scaled by
+    """P is stored as fp16 times a power-of-two scale per (row, 128 columns): W2 scaled by
     2^20 (|P| far above 65504) or 2^-30 (|P| far below fp16's normal range) must give the
     oracle's y within the usual tolerance, with no overflow to inf and no flush to zero."""
     wl = synth.Workload("range", 512, 512, 256, 8, 2)
@@ -209,6 +209,33 @@ def test_ragged_token_counts(T, flags):
     check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
     routing_equal(layer.routing(T), ref, T)
     check_y(bits(y), ref["y"])
+
+
+@pytest.mark.parametrize("schedule", [moe.MOE_SCHED_AUTO, moe.MOE_SCHED_INTERLEAVED, moe.MOE_SCHED_PHASED])
+def test_plan_reused_across_batches(schedule):
+    """One plan, five forwards with different token counts and different inputs (weights
+    included), one of them through the host-buffer entry point: each against the full
+    oracle, so that nothing a forward leaves in the workspace (counts, chunk histograms,
+    readiness counters, padded rows, the staging buffers) reaches the next one."""
+    layer = None
+    for T, seed, host in [(1000, 11, False), (37, 12, False), (513, 13, False), (200, 14, True), (1000, 15, False)]:
+        wl = synth.Workload("reuse", T, 512, 256, 16, 4, seed=seed)
+        if layer is None:
+            layer = _layer(wl, schedule, T_max=1024)
+        h = synth.host_inputs(wl)
+        ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]), want_intermediates=True)
+        d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
+        if host:
+            y = torch.empty((T, wl.H), dtype=torch.bfloat16).pin_memory()
+            logits = torch.empty((T, wl.E), dtype=torch.float32, device="cuda")
+            layer.forward_host(d["x"].cpu().pin_memory(), d["Wr"], d["W1"], d["W2"], logits, y, check=True)
+        else:
+            y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+        check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
+        routing_equal(layer.routing(T), ref, T)
+        h_gpu, _ = layer.intermediates(T, want_P=False)
+        check_y_explained(bits(y), ref, bits(h_gpu), h["W2"])
+    layer.close()
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(100, 256, 128, 6, 2), (64, 256, 128, 1, 1), (50, 512, 128, 40, 8),
