@@ -212,21 +212,26 @@ MOE_API const char* moe_status_string(moe_status_t s);
  * allocate device memory.  The paper has no counterpart: it exists for code that may not call
  * cudaMalloc, e.g. under an allocator that owns all device memory or a fixed memory budget (a
  * cudaMalloc behind its back fails or breaks its accounting), or on paths that must not risk
- * the implicit synchronisation of cudaMalloc/cudaFree.  It allocates nothing: its scratch (one row counter
- * per expert) is a fixed array of 256 counters inside the library, present on every device
- * that loads it until the process exits.
- *   ids      int32 [T,k]  expert of each (token, slot); entries outside [0,E) are not placed
+ * the implicit synchronisation of cudaMalloc/cudaFree.  It allocates nothing: its scratch (one
+ * row counter per expert) is a fixed array of 256 counters inside the library, present on every
+ * device that loads it until the process exits.
+ *   ids      int32 [T,k]  expert of each (token, slot)
  *   w        fp32  [T,k]  router weights, or NULL (then row_w must be NULL)
  *   offsets  int32 [E+1]  OUTPUT: rows of expert e are offsets[e] .. offsets[e+1]-1
  *   row_pair int32 [T*k]  OUTPUT: row -> t*k+j, ascending t within an expert
  *   row_of   int32 [T*k]  OUTPUT: t*k+j -> row
  *   row_w    fp32  [T*k]  OUTPUT: w of each row, or NULL
- * Device pointers, enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
- * Limits: E <= 256 and T*k < 2^30, else MOE_ERR_UNSUPPORTED.  The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress) and should happen before any stream
- * capture; later calls only enqueue a memset of the counters and two kernels.  All calls share
- * the one array: calls whose work overlaps on the GPU (different streams without ordering) race
- * and give wrong rows; calls ordered on one stream are safe, each clears the counters first. */
+ * Device pointers (ids needs only 4-byte alignment), enqueued on `stream` (a cudaStream_t;
+ * NULL = legacy default stream).  T = 0 writes offsets = 0 and nothing else.
+ * A pair whose id lies outside [0, E) gets no row: row_of[t*k+j] = -1, and offsets[E] counts
+ * only the placed pairs, so offsets[E] < T*k tells the caller that some id was out of range
+ * (rows offsets[E] .. T*k-1 of row_pair and row_w are then not written).
+ * Limits: E <= 256 and T*k < 2^30, else MOE_ERR_UNSUPPORTED.  The first call on a device (and
+ * the first after its context was replaced, e.g. by cudaDeviceReset) looks up the array's
+ * device address (cudaGetSymbolAddress) and should happen before any stream capture; later
+ * calls only enqueue a memset of the counters and two kernels.  All calls share the one
+ * array: calls whose work overlaps on the GPU (different streams without ordering) race and
+ * give wrong rows; calls ordered on one stream are safe, each clears the counters first. */
 MOE_API moe_status_t moe_dispatch_static(int32_t T, int32_t E, int32_t k, const int32_t* ids, const float* w,
                                  int32_t* offsets, int32_t* row_pair, int32_t* row_of, float* row_w,
                                  void* stream);

@@ -8,6 +8,7 @@
 // or capped at a fixed budget (a cudaMalloc behind its back would fail or break
 // its accounting), and code paths that must not risk the implicit device
 // synchronisation cudaMalloc and cudaFree can cause.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,17 +26,52 @@ static __device__ __align__(256) int32_t g_static_counts[STATIC_MAX_EXPERTS];
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_setup_mu;
+// Per device: the array's address and the id of the context it was looked up in.  A context
+// id is unique for the life of the process, so after cudaDeviceReset (a new primary context,
+// the module loaded again, possibly elsewhere) the address is looked up anew.
 int32_t* g_counts_ptr[MAX_DEVICES] = {};
+unsigned long long g_counts_ctx[MAX_DEVICES] = {};
 
-// Device address of g_static_counts on the current device (looked up once per device).
+typedef CUresult (*PFN_ctx_get_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long*);
+PFN_ctx_get_current g_ctx_get_current = nullptr;
+PFN_ctx_get_id g_ctx_get_id = nullptr;
+
+// Id of the context current on this thread (0 if there is none yet or the lookup fails).
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PFN_ctx_get_current>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<PFN_ctx_get_id>(f);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!g_ctx_get_current || !g_ctx_get_id || g_ctx_get_current(&c) != CUDA_SUCCESS || !c ||
+      g_ctx_get_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_static_counts on the current device: looked up once per device and
+// context (host code must not pass the symbol itself to a kernel: that is a host-side
+// stand-in, not a device address).
 cudaError_t static_counts_address(int dev, int32_t** out) {
   if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_counts_ptr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_counts_ptr[dev] || ctx == 0 || ctx != g_counts_ctx[dev]) {
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_static_counts);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_counts);   // binds the primary context if needed
     if (e != cudaSuccess) return e;
     g_counts_ptr[dev] = static_cast<int32_t*>(p);
+    g_counts_ctx[dev] = current_context_id();
   }
   *out = g_counts_ptr[dev];
   return cudaSuccess;
@@ -45,15 +81,18 @@ constexpr int SS_THREADS = 1024;
 constexpr int SS_PER_THREAD = 16;
 
 // counts[e] += #{f : ids[f] == e}; a block histogram in shared memory, then one
-// global atomic per non-empty bin.  Entries outside [0, E) are not counted.
+// global atomic per non-empty bin.  Entries outside [0, E) are not counted; their
+// row_of is set to -1 here (no row holds them).
 __global__ void __launch_bounds__(256)
-static_histogram_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ counts) {
+static_histogram_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ counts,
+                        int32_t* __restrict__ row_of) {
   __shared__ int32_t bins[STATIC_MAX_EXPERTS];
   for (int i = threadIdx.x; i < E; i += blockDim.x) bins[i] = 0;
   __syncthreads();
   for (int f = blockIdx.x * blockDim.x + threadIdx.x; f < R; f += gridDim.x * blockDim.x) {
     const int e = ids[f];
     if (e >= 0 && e < E) atomicAdd(&bins[e], 1);
+    else row_of[f] = -1;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
@@ -172,7 +211,7 @@ extern "C" moe_status_t moe_dispatch_static(int32_t T, int32_t E, int32_t k, con
   }
   int blocks = (R + 255) / 256;
   if (blocks > 1024) blocks = 1024;
-  static_histogram_kernel<<<blocks, 256, 0, st>>>(ids, R, E, counts);
+  static_histogram_kernel<<<blocks, 256, 0, st>>>(ids, R, E, counts, row_of);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   static_sort_kernel<<<E, SS_THREADS, 0, st>>>(ids, w, counts, R, E, offsets, row_pair, row_of, row_w);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;

@@ -94,17 +94,6 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* m, uint64_t* bar,
       : "memory");
 }
 
-// The same load delivered to the same shared-memory offset of every CTA in
-// `cta_mask` of the cluster, completing bytes on each CTA's barrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap* m, uint64_t* bar, void* dst, int32_t c0, int32_t c1,
-                                               uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // L2 eviction-priority policies (createpolicy); evict_first for streamed
 // operands, evict_last for operands other CTAs will re-read soon.
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -11,7 +11,15 @@ arrays.  bf16 tensors are passed as ``uint16`` bit patterns.
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py``
 (library routines, closed forms, brute-force dense evaluation, exact integer
-cases); none is "parity unpinned".
+cases, hand-built rounding-boundary cases, brute-force enumeration of the
+intermediate's rounding alternatives); none is "parity unpinned".
+
+Besides the layer's result, ``forward(..., bounds=True)`` reports what the
+comparison with another implementation needs: y before its final rounding
+(``y32``) and the interval [``ylo``, ``yhi``] that y can take when the
+intermediates that lie within the stated accumulation-error bound of a bf16
+rounding boundary (``moe_oracle.c``, "Rounding flags") round to their other
+neighbour.
 """
 from __future__ import annotations
 
@@ -54,8 +62,12 @@ def _load():
         L.oracle_forward_tokens.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp,
                                             vp, vp, vp]
         L.oracle_forward_tokens.restype = ctypes.c_int
+        L.oracle_expert_h_range.argtypes = [i32, i32, vp, vp, i32, vp, vp, vp, vp]
+        L.oracle_expert_rows.argtypes = [i32, i32, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.oracle_combine.argtypes = [i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, vp]
         for f in ("oracle_f32_to_bf16_array", "oracle_router_logits", "oracle_topk",
-                  "oracle_dispatch", "oracle_expert_ffn"):
+                  "oracle_dispatch", "oracle_expert_ffn", "oracle_expert_h_range", "oracle_expert_rows",
+                  "oracle_combine"):
             getattr(L, f).restype = None
         _lib = L
     return _lib
@@ -174,11 +186,110 @@ def forward_tokens(x, ids, w, tokens, W1_of, W2_of, E: int, act: int = ACT_SWIGL
     return y
 
 
+def expert_h_range(x_row, W1e, act: int = ACT_SWIGLU):
+    """The bf16 values the intermediate of one token through one expert can take under the
+    stated accumulation-error bound: a_lo, a_hi (bf16 bits [I]), plus the exact g|u [2I]
+    and their radius [2I] (both float64)."""
+    x_row, px = _c(x_row, np.uint16)
+    W1e, p1 = _c(W1e, np.uint16)
+    H, I2 = W1e.shape
+    I = I2 // 2
+    lo = np.empty(I, np.uint16)
+    hi = np.empty(I, np.uint16)
+    g = np.empty(2 * I, np.float64)
+    rad = np.empty(2 * I, np.float64)
+    _load().oracle_expert_h_range(H, I, px, p1, act, lo.ctypes.data, hi.ctypes.data, g.ctypes.data,
+                                  rad.ctypes.data)
+    return lo, hi, g, rad
+
+
+def _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_intermediates,
+                       experts_per_batch: int = 16):
+    """y of the sampled tokens, driven expert by expert: the weights of each expert the
+    sample touches are requested once, a batch of experts at a time (host memory stays
+    bounded), and every (token, slot) row of those experts is evaluated by
+    oracle_expert_rows; then oracle_combine sums the slots.  Same arithmetic as
+    forward_tokens."""
+    x, px = _c(x, np.uint16)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+    ns, k = len(tokens), ids.shape[1]
+    H = x.shape[1]
+    sel = ids[tokens]                                      # [ns, k]
+    experts = sorted({int(e) for e in sel.ravel()})
+    L = _load()
+    o = a = dlo = dhi = nflag = None
+    I = None
+    for b0 in range(0, len(experts), experts_per_batch):
+        batch = experts[b0:b0 + experts_per_batch]
+        mats = {e: (np.ascontiguousarray(W1_of(e), dtype=np.uint16), np.ascontiguousarray(W2_of(e), dtype=np.uint16))
+                for e in batch}
+        if I is None:
+            I = mats[batch[0]][1].shape[0]
+            o = np.empty((ns, k, H), np.float32)
+            a = np.empty((ns, k, I), np.uint16)
+            if bounds:
+                dlo = np.empty((ns, k, H), np.float64)
+                dhi = np.empty((ns, k, H), np.float64)
+                nflag = np.zeros((ns, k), np.int32)
+                a_lo = np.empty((ns, k, I), np.uint16)
+                a_hi = np.empty((ns, k, I), np.uint16)
+        rows = [(s, j) for s in range(ns) for j in range(k) if int(sel[s, j]) in mats]
+        n = len(rows)
+        toks = np.array([tokens[s] for s, _ in rows], np.int64)
+        P1 = (ctypes.c_void_p * n)(*[mats[int(sel[s, j])][0].ctypes.data for s, j in rows])
+        P2 = (ctypes.c_void_p * n)(*[mats[int(sel[s, j])][1].ctypes.data for s, j in rows])
+        a_b = np.empty((n, I), np.uint16)
+        o_b = np.empty((n, H), np.float32)
+        dl_b = np.empty((n, H), np.float64) if bounds else None
+        dh_b = np.empty((n, H), np.float64) if bounds else None
+        nf_b = np.zeros(n, np.int32) if bounds else None
+        lo_b = np.empty((n, I), np.uint16) if bounds else None
+        hi_b = np.empty((n, I), np.uint16) if bounds else None
+        L.oracle_expert_rows(H, I, act, px, n, toks.ctypes.data, P1, P2, a_b.ctypes.data, o_b.ctypes.data,
+                             dl_b.ctypes.data if bounds else None, dh_b.ctypes.data if bounds else None,
+                             nf_b.ctypes.data if bounds else None, lo_b.ctypes.data if bounds else None,
+                             hi_b.ctypes.data if bounds else None)
+        ss = np.array([r[0] for r in rows], np.int64)
+        jj = np.array([r[1] for r in rows], np.int64)
+        o[ss, jj] = o_b
+        a[ss, jj] = a_b
+        if bounds:
+            dlo[ss, jj] = dl_b
+            dhi[ss, jj] = dh_b
+            nflag[ss, jj] = nf_b
+            a_lo[ss, jj] = lo_b
+            a_hi[ss, jj] = hi_b
+        del mats
+    if I is None:   # no tokens sampled
+        I = 0
+        o = np.empty((0, k, H), np.float32)
+        a = np.empty((0, k, 0), np.uint16)
+    ws = np.ascontiguousarray(w[tokens], dtype=np.float32)
+    y = np.empty((ns, H), np.uint16)
+    out = {}
+    if bounds:
+        y32 = np.empty((ns, H), np.float32)
+        ylo = np.empty((ns, H), np.float64)
+        yhi = np.empty((ns, H), np.float64)
+        L.oracle_combine(H, k, ns, ws.ctypes.data, o.ctypes.data, dlo.ctypes.data, dhi.ctypes.data, y.ctypes.data,
+                         y32.ctypes.data, ylo.ctypes.data, yhi.ctypes.data)
+        out.update(y32=y32, ylo=ylo, yhi=yhi, nflag=nflag, a_lo=a_lo, a_hi=a_hi)
+    else:
+        L.oracle_combine(H, k, ns, ws.ctypes.data, o.ctypes.data, None, None, y.ctypes.data, None, None, None)
+    out["y"] = y
+    if want_intermediates:
+        out["a"], out["o"] = a, o
+    return out
+
+
 def forward(x, Wr, bias, W1, W2, k: int, act: int = ACT_SWIGLU, tokens=None,
-            logits=None, want_intermediates: bool = False) -> dict:
+            logits=None, want_intermediates: bool = False, bounds: bool = False,
+            experts_per_batch: int = 16) -> dict:
     """The whole layer on host arrays.  ``W1``/``W2`` are [E,H,2I]/[E,I,H] arrays or
-    callables e -> per-expert matrix.  ``logits`` given: used instead of x*Wr.
-    ``tokens``: which tokens get y (default all)."""
+    callables e -> per-expert matrix (each called once per expert the sample touches,
+    ``experts_per_batch`` experts held at a time).  ``logits`` given: used instead of x*Wr.
+    ``tokens``: which tokens get y (default all).  ``bounds``: also y32, ylo, yhi, nflag
+    (see the module docstring)."""
     if logits is None:
         logits = router_logits(x, Wr, bias)
     E = logits.shape[1]
@@ -189,11 +300,9 @@ def forward(x, Wr, bias, W1, W2, k: int, act: int = ACT_SWIGLU, tokens=None,
         tokens = np.arange(T, dtype=np.int64)
     W1_of = W1 if callable(W1) else (lambda e: W1[e])
     W2_of = W2 if callable(W2) else (lambda e: W2[e])
-    res = forward_tokens(x, ids, w, tokens, W1_of, W2_of, E, act, want_intermediates)
+    res = _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_intermediates,
+                             experts_per_batch)
     out = dict(logits=logits, ids=ids, w=w, counts=counts, offsets=offsets,
                row_pair=row_pair, row_of=row_of, tokens=np.asarray(tokens, np.int64))
-    if want_intermediates:
-        out["y"], out["a"], out["o"] = res
-    else:
-        out["y"] = res
+    out.update(res)
     return out

@@ -215,3 +215,194 @@ int oracle_forward_tokens(int H, int I, int E, int k, int act, const uint16_t* x
   }
   return bad ? -2 : 0;
 }
+
+/* ============================================================================
+ * Rounding flags of the intermediate and the interval of y they allow.
+ *
+ * Why: the intermediate a = bf16(silu(g) * u) is a discrete decision taken on
+ * fp32 accumulations g, u.  An implementation that accumulates in another
+ * order (the page fixes none) gets g, u that differ in the last bits, and
+ * where silu(g) * u lies that close to a bf16 rounding boundary it rounds to
+ * the neighbouring bf16 value.  The oracle reports, for every element, the
+ * bf16 values a_lo <= a <= a_hi that such an accumulation can produce, and
+ * carries them through Linear-2 and Combine as an interval of y.
+ *
+ * Stated bound.  g* = sum_h x_h W_hn, the exact value, is taken as the double
+ * sum of the exact products (each bf16 x bf16 product is exact in double; the
+ * double sum errs by at most H 2^-53 sum_h |x_h W_hn|, added to the radius).
+ * The implementation under test accumulates in ascending h in steps of
+ * O_STEP products (the tensor-core instruction depth for bf16), each step
+ * D_s = D_{s-1} + (its products) rounded with an error of at most
+ * O_STEP_ULPS units in the last place of the larger of |D_{s-1}| and the
+ * step's sum of |products|; so its fp32 result lies within
+ *     r = O_STEP_ULPS 2^-23 (sum_s |D_{s-1}| + sum_h |x_h W_hn|)
+ * of g*.  (A sum rounded to nearest once per product, in any order, is
+ * covered whenever the step error dominates; the oracle's own fmaf sum is
+ * not assumed to lie in the range - its a is added to it explicitly.)
+ * silu and the product are evaluated over [g* - r, g* + r] x [u* - r_u,
+ * u* + r_u] in double, widened by (|g| + r + 8) 2^-22 relative for the
+ * evaluation of exp, the division and the product on either side, and the
+ * extremes rounded outward to bf16.
+ * ========================================================================== */
+#define O_STEP 16
+#define O_STEP_ULPS 2.0
+#define O_SILU_XMIN (-1.2784645427610738)       /* the minimum of x / (1 + e^-x) */
+
+static double o_silu_d(double g) { return g / (1.0 + exp(-g)); }
+
+/* bf16 value (bits) at or below v / at or above v: v to float rounded outward, then RNE. */
+static uint16_t o_bf16_at_or_below(double v) {
+  float f = (float)v;
+  if ((double)f > v) f = nextafterf(f, -INFINITY);
+  return o_f32_to_bf16(f);
+}
+static uint16_t o_bf16_at_or_above(double v) {
+  float f = (float)v;
+  if ((double)f < v) f = nextafterf(f, INFINITY);
+  return o_f32_to_bf16(f);
+}
+
+/* For one token and one expert: a_lo[n], a_hi[n] (bf16 bits), the extreme bf16 values the
+ * intermediate can take under the stated bound (always bracketing the oracle's own a);
+ * g_out [2I] / rad_out [2I] (optional): the exact g (n < I) and u (n >= I) as doubles and
+ * their radius r. */
+void oracle_expert_h_range(int H, int I, const uint16_t* xrow, const uint16_t* W1e, int act,
+                           uint16_t* a_lo, uint16_t* a_hi, double* g_out, double* rad_out) {
+  double* acc = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+  double* sd = (double*)malloc(sizeof(double) * (size_t)(2 * I));    /* sum_s |D_{s-1}| */
+  double* sp = (double*)malloc(sizeof(double) * (size_t)(2 * I));    /* sum_h |products| */
+  float* facc = (float*)malloc(sizeof(float) * (size_t)(2 * I));     /* the oracle's own fp32 sums */
+  for (int n = 0; n < 2 * I; ++n) { acc[n] = sd[n] = sp[n] = 0.0; facc[n] = 0.0f; }
+  for (int h = 0; h < H; ++h) {
+    if (h % O_STEP == 0)
+      for (int n = 0; n < 2 * I; ++n) sd[n] += fabs(acc[n]);
+    float xv = o_bf16_to_f32(xrow[h]);
+    const uint16_t* wrow = W1e + (int64_t)h * 2 * I;
+    for (int n = 0; n < 2 * I; ++n) {
+      float wv = o_bf16_to_f32(wrow[n]);
+      double p = (double)xv * (double)wv;
+      acc[n] += p;
+      sp[n] += fabs(p);
+      facc[n] = fmaf(xv, wv, facc[n]);       /* the same steps as oracle_expert_ffn */
+    }
+  }
+  for (int n = 0; n < 2 * I; ++n) {
+    double r = O_STEP_ULPS * 0x1p-23 * (sd[n] + sp[n]) + (double)H * 0x1p-53 * sp[n];
+    if (g_out) g_out[n] = acc[n];
+    if (rad_out) rad_out[n] = r;
+    sd[n] = r;
+  }
+  for (int n = 0; n < I; ++n) {
+    float gf = facc[n], uf = facc[I + n];
+    float v = (act == 0) ? (gf / (1.0f + expf(-gf))) * uf : gf * uf;   /* exactly the oracle's a */
+    uint16_t a = o_f32_to_bf16(v);
+    a_lo[n] = a_hi[n] = a;
+    double g = acc[n], u = acc[I + n], rg = sd[n], ru = sd[I + n];
+    if (!isfinite(g) || !isfinite(u) || !isfinite(v)) continue;
+    double glo = g - rg, ghi = g + rg, ulo = u - ru, uhi = u + ru;
+    double smin, smax, slack;
+    if (act == 0) {
+      double s1 = o_silu_d(glo), s2 = o_silu_d(ghi);
+      smin = s1 < s2 ? s1 : s2;
+      smax = s1 < s2 ? s2 : s1;
+      if (glo < O_SILU_XMIN && O_SILU_XMIN < ghi) smin = o_silu_d(O_SILU_XMIN);
+      slack = (fabs(g) + rg + 8.0) * 0x1p-22;
+    } else {
+      smin = glo;
+      smax = ghi;
+      slack = 0x1p-22;
+    }
+    double pr[4] = {smin * ulo, smin * uhi, smax * ulo, smax * uhi};
+    double vlo = pr[0], vhi = pr[0];
+    for (int i = 1; i < 4; ++i) {
+      if (pr[i] < vlo) vlo = pr[i];
+      if (pr[i] > vhi) vhi = pr[i];
+    }
+    double mag = fabs(vlo) > fabs(vhi) ? fabs(vlo) : fabs(vhi);
+    vlo -= slack * mag;
+    vhi += slack * mag;
+    uint16_t lo = o_bf16_at_or_below(vlo), hi = o_bf16_at_or_above(vhi);
+    if (o_bf16_to_f32(lo) < o_bf16_to_f32(a)) a_lo[n] = lo;
+    if (o_bf16_to_f32(hi) > o_bf16_to_f32(a)) a_hi[n] = hi;
+  }
+  free(acc);
+  free(sd);
+  free(sp);
+  free(facc);
+}
+
+/* Rows of several (token, expert) pairs, each with its own expert's weights: row i is token
+ * toks[i] through expert W1p[i] / W2p[i] (oracle_expert_ffn: a_out [n][I] bf16 bits, o_out
+ * [n][H] fp32).  With dlo/dhi [n][H] (double, may be NULL): the change of o that the flagged
+ * intermediates can cause - for each flagged element, (a_lo - a) and (a_hi - a) times its
+ * row of W2, the smaller and the larger summed separately; nflag[i] counts row i's flagged
+ * elements, and a_lo_out / a_hi_out [n][I] (may be NULL) receive the ranges themselves. */
+void oracle_expert_rows(int H, int I, int act, const uint16_t* x, int64_t n, const int64_t* toks,
+                        const uint16_t* const* W1p, const uint16_t* const* W2p, uint16_t* a_out,
+                        float* o_out, double* dlo, double* dhi, int32_t* nflag, uint16_t* a_lo_out,
+                        uint16_t* a_hi_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    const uint16_t* xrow = x + toks[i] * H;
+    float* scratch = (float*)malloc(sizeof(float) * (size_t)(2 * I));
+    oracle_expert_ffn(H, I, xrow, W1p[i], W2p[i], act, a_out + i * I, o_out + i * H, scratch);
+    free(scratch);
+    if (!dlo) continue;
+    uint16_t* lo = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    uint16_t* hi = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+    oracle_expert_h_range(H, I, xrow, W1p[i], act, lo, hi, NULL, NULL);
+    if (a_lo_out) memcpy(a_lo_out + i * I, lo, sizeof(uint16_t) * (size_t)I);
+    if (a_hi_out) memcpy(a_hi_out + i * I, hi, sizeof(uint16_t) * (size_t)I);
+    double* dl = dlo + i * H;
+    double* dh = dhi + i * H;
+    for (int m = 0; m < H; ++m) dl[m] = dh[m] = 0.0;
+    int32_t cnt = 0;
+    const uint16_t* a = a_out + i * I;
+    for (int nn = 0; nn < I; ++nn) {
+      if (lo[nn] == a[nn] && hi[nn] == a[nn]) continue;
+      ++cnt;
+      double d1 = (double)o_bf16_to_f32(lo[nn]) - (double)o_bf16_to_f32(a[nn]);
+      double d2 = (double)o_bf16_to_f32(hi[nn]) - (double)o_bf16_to_f32(a[nn]);
+      const uint16_t* wrow = W2p[i] + (int64_t)nn * H;
+      for (int m = 0; m < H; ++m) {
+        double wv = (double)o_bf16_to_f32(wrow[m]);
+        double c1 = d1 * wv, c2 = d2 * wv;
+        dl[m] += c1 < c2 ? c1 : c2;
+        dh[m] += c1 < c2 ? c2 : c1;
+      }
+    }
+    if (nflag) nflag[i] = cnt;
+    free(lo);
+    free(hi);
+  }
+}
+
+/* Combine of ns tokens from their k slot outputs o [ns][k][H] and weights w [ns][k]: the same
+ * fp32 slot-order sum as oracle_forward_tokens; y [ns][H] bf16 bits and y32 (the sum before
+ * rounding).  With dlo/dhi [ns][k][H]: ylo/yhi = y32 + the smallest / largest change the
+ * flagged intermediates of the k slots can cause, in double. */
+void oracle_combine(int H, int k, int64_t ns, const float* w, const float* o, const double* dlo,
+                    const double* dhi, uint16_t* y, float* y32, double* ylo, double* yhi) {
+#pragma omp parallel for schedule(static)
+  for (int64_t s = 0; s < ns; ++s) {
+    const float* os = o + s * k * H;
+    const float* ws = w + s * k;
+    for (int m = 0; m < H; ++m) {
+      float acc = ws[0] * os[m];
+      for (int j = 1; j < k; ++j) acc = acc + ws[j] * os[(int64_t)j * H + m];
+      y[s * H + m] = o_f32_to_bf16(acc);
+      if (y32) y32[s * H + m] = acc;
+      if (dlo) {
+        double lo = (double)acc, hi = (double)acc;
+        for (int j = 0; j < k; ++j) {
+          double wj = (double)ws[j];
+          double c1 = wj * dlo[(s * k + j) * H + m], c2 = wj * dhi[(s * k + j) * H + m];
+          lo += c1 < c2 ? c1 : c2;
+          hi += c1 < c2 ? c2 : c1;
+        }
+        ylo[s * H + m] = lo;
+        yhi[s * H + m] = hi;
+      }
+    }
+  }
+}

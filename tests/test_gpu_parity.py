@@ -10,7 +10,7 @@ import torch
 import mixture_experts_layer_top_gb300 as moe
 import oracle
 import synth
-from helpers import (bits, check_logits, check_y, check_y_explained, f64, from_bits, oracle_for, routing_equal,
+from helpers import (bits, check_h_in_range, check_logits, check_y, f64, from_bits, oracle_for, routing_equal,
                      sample_tokens)
 
 EXACT = moe.MOE_FLAG_EXACT_LOGITS
@@ -60,7 +60,7 @@ def test_tiny_full_parity(schedule, flags):
     else:
         check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(wl.T))
     routing_equal(layer.routing(wl.T), ref, wl.T)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
     router = 2 if flags & EXACT else 3
     assert layer.launch_count() == router + (5 if schedule == 2 else 4)
 
@@ -118,7 +118,7 @@ def test_expert_outputs_far_outside_fp16_range(exp2):
     y, _ = layer.forward(d["x"], d["Wr"], d["W1"], from_bits(W2), check=True)
     yr = f64(ref["y"])
     assert np.abs(yr).max() > (1e6 if exp2 > 0 else 0) and np.abs(yr).max() < (np.inf if exp2 > 0 else 1e-6)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
 
 
 @pytest.mark.parametrize("name", ["skew", "smallT"])
@@ -162,7 +162,7 @@ def test_schedules_bitwise_identical():
     h = synth.host_inputs(wl, weights=False)
     tok = sample_tokens(wl.T, 48)
     ref = oracle_for(wl, h["x"], h["Wr"], None, tok)
-    check_y(outs[0][tok], ref["y"])
+    check_y(outs[0][tok], ref)
 
 
 # --------------------------------------------------------------------------- full-size workloads
@@ -189,7 +189,7 @@ def test_workload_parity(name, nsample, schedule, flags):
     routing_equal(layer.routing(wl.T), ref, wl.T)
     if name == "skew":
         assert (ref["counts"] == 0).any(), "skewed workload should leave experts idle"
-    check_y(bits(y)[tok], ref["y"], what=name)
+    check_y(bits(y)[tok], ref, what=name)
     del d
     layer.close()
     torch.cuda.empty_cache()
@@ -208,7 +208,7 @@ def test_ragged_token_counts(T, flags):
     y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
     routing_equal(layer.routing(T), ref, T)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
 
 
 @pytest.mark.parametrize("schedule", [moe.MOE_SCHED_AUTO, moe.MOE_SCHED_INTERLEAVED, moe.MOE_SCHED_PHASED])
@@ -234,7 +234,8 @@ def test_plan_reused_across_batches(schedule):
         check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
         routing_equal(layer.routing(T), ref, T)
         h_gpu, _ = layer.intermediates(T, want_P=False)
-        check_y_explained(bits(y), ref, bits(h_gpu), h["W2"])
+        check_y(bits(y), ref)
+        check_h_in_range(bits(h_gpu), ref)
     layer.close()
 
 
@@ -256,7 +257,7 @@ def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
     else:
         check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
     routing_equal(layer.routing(T), ref, T)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
 
 
 def _random_cases(n: int, seed: int = 20261202):
@@ -299,8 +300,10 @@ def test_random_shapes_full_oracle(c):
     else:
         check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(c["T"]), bias)
     routing_equal(layer.routing(c["T"]), ref, c["T"])
+    st = check_y(bits(y), ref)
     h_gpu, _ = layer.intermediates(c["T"], want_P=False)
-    check_y_explained(bits(y), ref, bits(h_gpu), h["W2"])
+    hs = check_h_in_range(bits(h_gpu), ref)
+    print(f"y: {st}; h: {hs}")
     layer.close()
 
 
@@ -352,7 +355,7 @@ def test_inconsistent_routing_reported_and_contained():
     bad.close()
     y2, _ = good.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
-    check_y(bits(y2), ref["y"])
+    check_y(bits(y2), ref)
     good.close()
 
 
@@ -420,7 +423,7 @@ def test_router_certified_selection_on_ties_and_infinities():
     y, logits = layer.forward(from_bits(x), from_bits(Wr), W1, W2, check=True)
     st = check_logits(logits.cpu().numpy(), ref, x, Wr, layer.router_bound(T))
     routing_equal(layer.routing(T), ref, T)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
     assert st["exact_frac"] > 0.1     # ties force many candidates
     Wr_inf = Wr.copy()
     Wr_inf[3, 5] = 0x7F80              # bf16 +inf
@@ -440,14 +443,14 @@ def test_logits_as_input_and_one_hot_expert():
     h = synth.host_inputs(wl)
     logits = np.full((wl.T, wl.E), -5.0, np.float32)
     logits[:, 6] = 3.0
-    ref = oracle.forward(h["x"], h["Wr"], None, h["W1"], h["W2"], wl.k, logits=logits)
+    ref = oracle.forward(h["x"], h["Wr"], None, h["W1"], h["W2"], wl.k, logits=logits, bounds=True)
     assert ref["counts"][6] == wl.T and ref["counts"].sum() == wl.T
     layer = _layer(wl)
     d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
     lg = torch.from_numpy(logits).cuda()
     y, _ = layer.forward(d["x"], None, d["W1"], d["W2"], logits=lg, check=True)
     routing_equal(layer.routing(wl.T), ref, wl.T)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
 
 
 def test_router_weights_wide_logits():
@@ -461,12 +464,12 @@ def test_router_weights_wide_logits():
     logits[::5] = np.round(logits[::5] / 10.0)                       # many exact ties
     few = np.arange(3, wl.T, 11)
     logits[few, 3:] = -np.inf                                        # only 3 finite logits
-    ref = oracle.forward(h["x"], h["Wr"], None, h["W1"], h["W2"], wl.k, logits=logits)
+    ref = oracle.forward(h["x"], h["Wr"], None, h["W1"], h["W2"], wl.k, logits=logits, bounds=True)
     layer = _layer(wl)
     d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
     y, _ = layer.forward(d["x"], None, d["W1"], d["W2"], logits=torch.from_numpy(logits).cuda(), check=True)
     routing_equal(layer.routing(wl.T), ref, wl.T)
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
 
 
 def test_nan_token_stays_local():
@@ -483,7 +486,7 @@ def test_nan_token_stays_local():
     others = np.arange(wl.T) != 5
     assert np.all(np.isfinite(yg[others]))
     assert np.array_equal(layer.routing(wl.T)["ids"].cpu().numpy(), ref["ids"])
-    check_y(bits(y)[others], ref["y"][others])
+    check_y(bits(y)[others], ref, rows=others)
 
 
 def test_timeout_reports_status_and_context_survives():
@@ -501,7 +504,7 @@ def test_timeout_reports_status_and_context_survives():
     y, _ = good.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     h = synth.host_inputs(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
-    check_y(bits(y), ref["y"])
+    check_y(bits(y), ref)
 
 
 def test_invalid_arguments_rejected_before_launch():

@@ -272,3 +272,137 @@ def test_oracle_matches_its_regression_record():
     with open(os.path.join(here, "oracle_tiny.json")) as f:
         want = json.load(f)
     assert mg.record() == want
+
+
+# --------------------------------------------------------------------------- rounding flags of h
+def _one_expert(x_vals, gate, up, H=32):
+    """One token through one expert with I = 1: x[:len(x_vals)] = x_vals (rest 0), the gate
+    and up columns given (rest 0).  Returns x row, W1e [H, 2] (bf16 bits)."""
+    x = np.zeros(H, np.float32)
+    x[:len(x_vals)] = x_vals
+    W1 = np.zeros((H, 2), np.float32)
+    W1[:len(gate), 0] = gate
+    W1[:len(up), 1] = up
+    xb, wb = bf16_bits(x), bf16_bits(W1)
+    assert np.array_equal(bits_to_f64(xb), x) and np.array_equal(bits_to_f64(wb), W1)   # exact in bf16
+    return xb, wb
+
+
+@pytest.mark.parametrize("delta,flagged", [(0.0, True), (2.0 ** -23, True), (-(2.0 ** -23), True),
+                                           (2.0 ** -16, False), (-(2.0 ** -16), False)])
+def test_h_range_on_a_rounding_boundary(delta, flagged):
+    """Bilinear g * u with u = 1 and g = 1 + 2^-8 + delta.  delta = 0 is exactly halfway between
+    the bf16 values 1 and 1 + 2^-7 (round-to-even gives 1): any other accumulation order may
+    give either, so both are in the range.  2^-23 away is inside the stated radius (about
+    2^-22 here), 2^-16 away is far outside it: only the nearest value remains."""
+    terms = [1.0, 2.0 ** -8] + ([abs(delta)] if delta else [])
+    gate = [1.0, 1.0] + ([np.sign(delta)] if delta else [])
+    xb, wb = _one_expert(terms, gate, [1.0])
+    lo, hi, g, rad = oracle.expert_h_range(xb, wb, act=oracle.ACT_BILINEAR)
+    a, _ = oracle.expert_ffn(xb, wb, np.zeros((1, 32), np.uint16), act=oracle.ACT_BILINEAR)
+    assert g[0] == 1.0 + 2.0 ** -8 + delta and g[1] == 1.0              # exact sums
+    assert 2.0 ** -23 < rad[0] < 2.0 ** -20
+    one, up1 = 0x3F80, 0x3F81                                            # bf16 1.0 and 1 + 2^-7
+    nearest = one if delta <= 0 else up1
+    assert a[0] == nearest
+    if flagged:
+        assert (lo[0], hi[0]) == (one, up1)
+    else:
+        assert lo[0] == hi[0] == nearest
+
+
+def test_h_range_brackets_every_evaluation_within_the_radius():
+    """SwiGLU on random inputs: for every element, silu(g') * u' evaluated in float64 at g', u'
+    anywhere in the stated radius (endpoints and random interior points) rounds to a bf16 value
+    inside [a_lo, a_hi], and the range always holds the oracle's own a."""
+    H, I = 512, 64
+    rng = np.random.default_rng(77)
+    x = bf16_bits(rng.standard_normal(H).astype(np.float32))
+    W1 = bf16_bits((rng.standard_normal((H, 2 * I)) / np.sqrt(H)).astype(np.float32))
+    W2 = np.zeros((I, H), np.uint16)
+    lo, hi, g, rad = oracle.expert_h_range(x, W1)
+    a, _ = oracle.expert_ffn(x, W1, W2)
+    flo, fhi, fa = bits_to_f64(lo), bits_to_f64(hi), bits_to_f64(a)
+    assert np.all(flo <= fa) and np.all(fa <= fhi)
+    gg, uu = g[:I], g[I:]
+    rg, ru = rad[:I], rad[I:]
+    for t in np.concatenate([[-1.0, 1.0], rng.uniform(-1, 1, 30)]):
+        for s in (-1.0, 1.0, rng.uniform(-1, 1)):
+            gv = gg + t * rg
+            uv = uu + s * ru
+            v = gv / (1.0 + np.exp(-gv)) * uv
+            b = bits_to_f64(bf16_bits(v.astype(np.float32)))
+            assert np.all((flo <= b) & (b <= fhi))
+
+
+def test_h_range_exact_sums_and_silu_minimum():
+    """The range's g, u are the exact sums (checked with rational arithmetic) and the constant
+    minimum of silu the range uses is silu's minimum (scipy)."""
+    from fractions import Fraction
+    from scipy.optimize import minimize_scalar
+    H, I = 64, 3
+    rng = np.random.default_rng(5)
+    x = bf16_bits(rng.standard_normal(H).astype(np.float32) * 3)
+    W1 = bf16_bits(rng.standard_normal((H, 2 * I)).astype(np.float32) * 1e-3)
+    _, _, g, _ = oracle.expert_h_range(x, W1)
+    xf, wf = bits_to_f64(x), bits_to_f64(W1)
+    for n in range(2 * I):
+        exact = sum(Fraction(float(xf[h])) * Fraction(float(wf[h, n])) for h in range(H))
+        assert abs(Fraction(float(g[n])) - exact) <= Fraction(2.0 ** -52) * abs(exact) + Fraction(2.0 ** -80)
+    m = minimize_scalar(lambda z: z / (1 + np.exp(-z)), bracket=(-3, -1, 0), tol=1e-14)
+    src = open(oracle.__file__.replace("__init__.py", "moe_oracle.c")).read()
+    const = float(src.split("#define O_SILU_XMIN (")[1].split(")")[0])
+    assert abs(const - m.x) < 1e-7
+
+
+def test_y_interval_equals_enumeration_of_flips():
+    """The oracle's [ylo, yhi] against brute force: every combination of the flagged intermediates'
+    extreme roundings (plus the oracle's own) carried through Linear-2 and Combine in float64;
+    the interval's ends must be the smallest and largest results."""
+    H, I, E, k = 512, 48, 4, 2
+    rng = np.random.default_rng(9)
+    x = bf16_bits(rng.standard_normal((40, H)).astype(np.float32))
+    W1 = bf16_bits((rng.standard_normal((E, H, 2 * I)) / np.sqrt(H)).astype(np.float32))
+    W2 = bf16_bits((rng.standard_normal((E, I, H)) / np.sqrt(I)).astype(np.float32))
+    Wr = bf16_bits((rng.standard_normal((H, E)) / np.sqrt(H)).astype(np.float32))
+    ref = oracle.forward(x, Wr, None, W1, W2, k, bounds=True, want_intermediates=True)
+    f = ref["nflag"].sum(axis=1)
+    cand = [t for t in range(40) if 2 <= f[t] <= 9]
+    assert cand, "no token with a handful of flagged elements"
+    for t in cand[:3]:
+        slots = []
+        for j in range(k):
+            e = ref["ids"][t, j]
+            a = bits_to_f64(ref["a"][t, j])
+            lo, hi = bits_to_f64(ref["a_lo"][t, j]), bits_to_f64(ref["a_hi"][t, j])
+            fl = np.nonzero((lo != a) | (hi != a))[0]
+            slots += [(j, e, n, lo[n] - a[n], hi[n] - a[n]) for n in fl]
+        dmin = np.full(H, np.inf)
+        dmax = np.full(H, -np.inf)
+        for mask in range(3 ** len(slots)):
+            d = np.zeros(H)
+            mm = mask
+            for (j, e, n, dl, dh) in slots:
+                c = (0.0, dl, dh)[mm % 3]
+                mm //= 3
+                d += float(ref["w"][t, j]) * c * bits_to_f64(W2[e, n])
+            dmin, dmax = np.minimum(dmin, d), np.maximum(dmax, d)
+        y32 = ref["y32"][t].astype(np.float64)
+        assert np.allclose(ref["ylo"][t] - y32, dmin, rtol=1e-12, atol=1e-15)
+        assert np.allclose(ref["yhi"][t] - y32, dmax, rtol=1e-12, atol=1e-15)
+        assert np.array_equal(oracle.f32_to_bf16(ref["y32"][t]), ref["y"][t])
+
+
+def test_expert_driven_forward_equals_token_driven():
+    """oracle.forward (expert by expert, batched) against oracle_forward_tokens (token by token):
+    the same arithmetic, so y, h and o bit for bit."""
+    H, I, E, k, T = 256, 128, 9, 3, 50
+    rng = np.random.default_rng(10)
+    x = bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    W1 = bf16_bits((rng.standard_normal((E, H, 2 * I)) / np.sqrt(H)).astype(np.float32))
+    W2 = bf16_bits((rng.standard_normal((E, I, H)) / np.sqrt(I)).astype(np.float32))
+    Wr = bf16_bits((rng.standard_normal((H, E)) / np.sqrt(H)).astype(np.float32))
+    ref = oracle.forward(x, Wr, None, W1, W2, k, want_intermediates=True, bounds=True, experts_per_batch=2)
+    y, a, o = oracle.forward_tokens(x, ref["ids"], ref["w"], np.arange(T), lambda e: W1[e], lambda e: W2[e], E,
+                                    want_intermediates=True)
+    assert np.array_equal(ref["y"], y) and np.array_equal(ref["a"], a) and np.array_equal(ref["o"], o)
