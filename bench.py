@@ -2,12 +2,14 @@
 """Throughput of the single-GPU MoE layer (router top-k -> Dispatch -> Linear-1 +
 SwiGLU -> Linear-2 -> Combine) on synthetic seeded inputs.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload fine] [--schedule 3]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large] [--also fine,skew,smallT]
     python bench.py --impl reference ...     # the CPU oracle, timed the same way
 
 One step = one moe_forward over the whole batch of T tokens, inputs and weights
 resident in HBM; L2 is flushed (256 MiB write) before every step, outside the
-timed events.  Rank 0 prints one JSON line.  With torchrun (N > 1) every rank
+timed events.  The headline is the large layer (T=4096, H=7168, I=2048, E=256,
+top-8); the fine-grained, skewed and 128-token workloads are timed in the same
+process the same way and reported under "workloads".  Rank 0 prints one JSON line.  With torchrun (N > 1) every rank
 runs an independent replica on its own GPU (the layer is not sharded) and the
 time is the maximum over ranks.
 """
@@ -34,21 +36,28 @@ L2_FLUSH_BYTES = 256 << 20
 
 
 def load_traffic(kernel: str, workload: str, schedule: int):
-    """DRAM bytes per launch of `kernel` from the committed ncu record, only while the
-    kernel's sources are unchanged since the capture (else None)."""
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, only while
+    the kernel's sources are unchanged since the capture (else None), and a note saying how the
+    figure was taken (a record may be a smaller case scaled to the full launch)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[kernel]
-        if rec["workload"] != workload or rec["schedule"] != schedule:
-            return None
-        h = hashlib.sha256()
-        for src in rec["sources"]:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                h.update(f.read())
-        return float(rec["dram_bytes_per_launch"]) if h.hexdigest() == rec["source_sha256"] else None
+            recs = json.load(f)[kernel]
+        if isinstance(recs, dict):
+            recs = [recs]
+        for rec in recs:
+            if rec["workload"] != workload or rec["schedule"] != schedule:
+                continue
+            h = hashlib.sha256()
+            for src in rec["sources"]:
+                with open(os.path.join(ROOT, src), "rb") as f:
+                    h.update(f.read())
+            if h.hexdigest() != rec["source_sha256"]:
+                return None, "sources changed since the capture"
+            return float(rec["dram_bytes_per_launch"]), rec.get("note", "ncu capture of this workload")
+        return None, "no capture of this workload"
     except Exception:
-        return None
+        return None, "no traffic record"
 
 
 def load_peaks():
@@ -118,6 +127,69 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(win), "note": note}
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (ctypes, read-only calls) every
+    `period_ms` on a thread, with host timestamps; a timed region of a few tens of ms still gets
+    samples.  Falls back to ClockSampler (nvidia-smi) when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_ms: float = 5.0):
+        import ctypes
+        self.samples = []
+        self.ok = False
+        self.stop_flag = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return
+        except Exception:
+            return
+        self.lib, self.h, self.period = lib, h, period_ms / 1e3
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+        self.ok = True
+        self.th = threading.Thread(target=self._run, daemon=True)
+        self.th.start()
+
+    def _run(self):
+        import ctypes
+        mhz, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_r = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag:
+            t = time.perf_counter()
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:   # NVML_CLOCK_SM
+                p = float(pw.value) / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw)) == 0 else None
+                r = int(rs.value) if get_r(self.h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((t, float(mhz.value), p, r))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.stop_flag = True
+        if self.ok:
+            self.th.join(timeout=1.0)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": "no NVML sample inside the timed region"}
+        reasons = sorted({n for s in win for bit, n in self.REASONS.items() if s[3] & bit})
+        pw = [s[2] for s in win if s[2] is not None]
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(win), "power_w_max": max(pw) if pw else None,
+                "note": f"NVML every {self.period * 1e3:.0f} ms inside the timed region"}
+
+
+def clock_sampler(index: int):
+    s = NvmlSampler(index)
+    return s if s.ok else ClockSampler(index)
+
+
 # ----------------------------------------------------------------------------- distributed
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -145,19 +217,19 @@ def barrier(group_ready: bool):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-_WCACHE = {}
+def weight_source(wl, d=None):
+    """Expert slices for the oracle: host copies of the device tensors the seeded generator drew
+    (when the GPU holds them: a copy per expert, no host-side regeneration), else the host
+    implementation of the same generator (bit-identical values)."""
+    if d is not None:
+        return lambda which, e: d[which][e].contiguous().view(__import__("torch").int16).cpu().numpy().view("uint16")
+    return lambda which, e: synth.expert_slice_host(wl, which, e)
 
 
-def _expert(wl, which, e):
-    key = (wl.name, which, e)
-    if key not in _WCACHE:
-        _WCACHE[key] = synth.expert_slice_host(wl, which, e)
-    return _WCACHE[key]
-
-
-def oracle_sample(wl, n_tok: int, seed: int = 1):
-    """Time the CPU oracle on n_tok sampled tokens (routing of the sample + their k experts).
-    Returns (seconds, useful FLOPs, threads).  Weight generation is not timed."""
+def oracle_sample(wl, n_tok: int, seed: int, weights_of):
+    """The CPU oracle on n_tok sampled tokens (routing of the sample + their k experts each).
+    Returns (seconds of the oracle's own arithmetic, useful FLOPs, threads, tokens, experts);
+    fetching the expert weights is not timed."""
     import numpy as np
     import oracle
     rng = np.random.default_rng(seed)
@@ -165,37 +237,30 @@ def oracle_sample(wl, n_tok: int, seed: int = 1):
     h = synth.host_inputs(wl, weights=False)
     x = np.ascontiguousarray(h["x"][tok])
     bias = h["bias"] if wl.zipf_s else None
-    logits = oracle.router_logits(x, h["Wr"], bias)
-    ids, _ = oracle.topk(logits, wl.k)
-    experts = sorted({int(e) for e in ids.ravel()})
-    W1 = {e: _expert(wl, "W1", e) for e in experts}
-    W2 = {e: _expert(wl, "W2", e) for e in experts}
-    t0 = time.perf_counter()
-    oracle.forward(x, h["Wr"], bias, W1.get, W2.get, wl.k)
-    dt = time.perf_counter() - t0
+    tm = {}
+    r = oracle.forward(x, h["Wr"], bias, lambda e: weights_of("W1", e), lambda e: weights_of("W2", e), wl.k,
+                       timing=tm)
+    experts = len({int(e) for e in r["ids"].ravel()})
     flops = len(tok) * (2.0 * wl.H * wl.E + wl.k * 6.0 * wl.H * wl.I)
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return dt, flops, threads, len(tok), len(experts)
+    return tm["compute_s"], flops, threads, len(tok), experts
 
 
-def calibrate_tokens(wl, budget_s: float):
-    dt, _, threads, n, _ = oracle_sample(wl, max(2, min(os.cpu_count() or 1, 16)))
-    per_tok = dt / n
-    n_target = int(budget_s / max(per_tok, 1e-9))
-    expert_bytes = 6.0 * wl.H * wl.I                        # W1[e] + W2[e], bf16
-    if wl.E * expert_bytes > 24e9:                          # keep the sample's host weights under ~24 GB
-        n_target = min(n_target, max(2, int(24e9 / (wl.k * expert_bytes))))
-    return max(2, min(n_target, wl.T))
+def calibrate_tokens(wl, budget_s: float, weights_of):
+    n0 = max(2, min(os.cpu_count() or 1, 16))
+    dt, _, _, n, _ = oracle_sample(wl, n0, 0, weights_of)
+    return max(2, min(int(budget_s / max(dt / n, 1e-9)), wl.T))
 
 
-def cpu_baseline(wl, budget_s: float):
+def cpu_baseline(wl, budget_s: float, weights_of):
     import oracle
     oracle.build()
-    n = calibrate_tokens(wl, budget_s)
-    dt, flops, threads, n, ne = oracle_sample(wl, n, seed=2)
+    n = calibrate_tokens(wl, budget_s, weights_of)
+    dt, flops, threads, n, ne = oracle_sample(wl, n, 2, weights_of)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} of {wl.T} tokens (router + their {wl.k} experts each, {ne} experts touched), "
-                      f"{dt:.1f} s; inputs regenerated on the host, generation untimed",
+                      f"{dt:.1f} s of oracle arithmetic; expert weights copied per expert from the seeded "
+                      f"generator's tensors, untimed",
             "tokens_per_s": n / dt}
 
 
@@ -205,14 +270,23 @@ def run_reference(args, wl):
         return 0
     import oracle
     oracle.build()
+    d = None
+    try:
+        import torch
+        if torch.cuda.is_available():        # the seeded generator draws the weights on the device:
+            torch.cuda.set_device(0)         # the oracle only reads host copies of them
+            d = synth.device_inputs(wl)
+    except Exception:
+        d = None
+    weights_of = weight_source(wl, d)
     budget = 150.0 / max(1, args.steps + args.warmup)
-    n = calibrate_tokens(wl, min(budget, 8.0))
+    n = calibrate_tokens(wl, min(budget, 8.0), weights_of)
     for _ in range(args.warmup):
-        oracle_sample(wl, n, seed=3)
+        oracle_sample(wl, n, 3, weights_of)
     times, flops_tot, toks = 0.0, 0.0, 0
     threads = 1
     for i in range(args.steps):
-        dt, fl, threads, nn, _ = oracle_sample(wl, n, seed=10 + i)
+        dt, fl, threads, nn, _ = oracle_sample(wl, n, 10 + i, weights_of)
         times += dt
         flops_tot += fl
         toks += nn
@@ -221,58 +295,56 @@ def run_reference(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * times / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32-accumulate bf16",
             "data": "synthetic (seeded generator)",
-            "config": config_of(wl, args, l2="host CPU run"),
+            "config": config_of(wl, args), "note": "the CPU oracle on the host cores; no GPU work is timed",
             "tokens_per_s": toks / times,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"each step {n} of {wl.T} tokens (router + their experts)"},
+                             "sample": f"each step {n} of {wl.T} tokens (router + their experts); the oracle's "
+                                       f"arithmetic timed, expert weights fetched untimed"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
-def config_of(wl, args, l2):
+def config_of(wl, args):
+    """The workload, the schedule options and the L2 policy of the GPU arm's timed steps: the
+    same dict for both arms (the reference arm runs on the host and says so in "note")."""
     sched = {0: "wave-serial", 1: "interleaved", 2: "phased (L1 launch, L2 launch)",
              3: "auto (wave-serial, one wave of all experts)"}[args.schedule]
     split = "streaming" if args.gemm_split == "auto" else args.gemm_split
     return {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
             "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
-            "wave_experts": args.wave_experts, "lead_waves": args.lead_waves, "l2": l2,
+            "wave_experts": args.wave_experts, "lead_waves": args.lead_waves,
+            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
             "parallelism": f"replicas x{args.gpus} (no sharding)"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_ours(args, wl):
+def _events(n):
+    import torch
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+
+
+def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e2e=True):
+    """One workload: W warm-up steps, K timed steps (CUDA events on the launching stream, L2
+    flushed before each step outside the events), the host-buffer e2e steps, and the per-stage
+    split from a second plan.  Returns the fields of its JSON entry."""
     import torch
     import mixture_experts_layer_top_gb300 as moe
 
-    ws, rank, local = dist_env()
-    group = False
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-        group = True
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    moe.build()
-    peaks, peak_src = load_peaks()
-
     bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
-    d = synth.device_inputs(wl, device=dev)
     flags = {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING, "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
-    layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=args.schedule, flags=flags,
-                                       wave_experts=args.wave_experts, lead_waves=args.lead_waves),
-                         local, router_bias=bias)
+    cfg = dict(schedule=args.schedule, wave_experts=args.wave_experts, lead_waves=args.lead_waves)
+    layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags, **cfg), local, router_bias=bias)
     logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fwd = lambda: layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=logits, y=y)   # noqa: E731
 
-    sampler = ClockSampler(local) if not args.no_clocks else None
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=logits, y=y)
+        fwd()
     layer.check()
-    r = layer.routing(wl.T)
-    counts = r["counts"].cpu()
+    counts = layer.routing(wl.T)["counts"].cpu()
     touched = int((counts > 0).sum())
     launches = layer.launch_count()
 
@@ -280,32 +352,30 @@ def run_ours(args, wl):
     barrier(group)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = _events(args.steps)
     for i in range(args.steps):                # no host synchronisation inside the timed steps
         flush.zero_()
         ev[i][0].record()
-        layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=logits, y=y)
+        fwd()
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(group)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     layer.check()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = reduce_max(sum(step_ms), group)
-    ms_per_step = total_ms / args.steps
+    clocks = sampler.summary(t0, t1) if sampler else None
+    ms_per_step = reduce_max(sum(a.elapsed_time(b) for a, b in ev), group) / args.steps
 
     # ---- e2e: the host-buffer C-ABI call, copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         x_host = d["x"].cpu().pin_memory()
         y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
         for _ in range(2):
             flush.zero_()
             layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
         torch.cuda.synchronize()
-        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+        eev = _events(args.steps)
         for i in range(args.steps):
             flush.zero_()
             eev[i][0].record()
@@ -319,11 +389,11 @@ def run_ours(args, wl):
         e2e = {"value": ws * wl.useful_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
                "ms_per_step": e_ms, "tokens_per_s": ws * wl.T / (e_ms * 1e-3)}
+    layer.close()
     # ---- per-stage breakdown on a second plan whose library records events between stages
-    # (those events serialise the stream, so the headline steps above run without them)
-    layer_t = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=args.schedule,
-                                         flags=flags | moe.MOE_FLAG_STAGE_TIMING, wave_experts=args.wave_experts,
-                                         lead_waves=args.lead_waves), local, router_bias=bias)
+    # (those events serialise the stream, so the timed steps above run without them)
+    layer_t = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags | moe.MOE_FLAG_STAGE_TIMING,
+                                         **cfg), local, router_bias=bias)
     stages = []
     for i in range(3 + min(args.steps, 20)):
         flush.zero_()
@@ -332,12 +402,7 @@ def run_ours(args, wl):
             stages.append(layer_t.stage_times())
     layer_t.check()
     layer_t.close()
-    if sampler:
-        sampler.stop()
-    clocks = sampler.summary(t0, t1) if sampler else None
-
-    if rank != 0:
-        return 0
+    del flush
 
     flops = wl.useful_flops()
     R = wl.T * wl.k
@@ -361,38 +426,107 @@ def run_ours(args, wl):
         ach = g_bytes / (g_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
-    traffic = load_traffic("grouped_gemm_kernel", wl.name, args.schedule)
+    traffic, traffic_note = load_traffic("grouped_gemm_kernel", wl.name, args.schedule)
     roof.update({"traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read+write)",
+                 "traffic_note": traffic_note,
                  "kernel": "grouped_gemm_kernel", "ms_per_launch": g_ms,
                  "launches_per_step": 2 if args.schedule == 2 else 1,
                  "peak_source": f"{peak_src} ({'bf16_tflops burst' if tensor_bound else 'hbm_gbs'})",
                  "algorithmic": (f"{g_flops:.4g} FLOP (6*H*I per routed row x {R} rows)" if tensor_bound
                                  else f"{g_bytes:.4g} B (6*H*I bytes per touched expert x {touched})")})
-
-    cpu = None
-    if not args.no_cpu_baseline and ws == 1:
-        try:
-            cpu = cpu_baseline(wl, args.cpu_budget)
-        except Exception as ex:  # reported, not fatal
-            cpu = {"value": None, "error": str(ex)[:200]}
-
-    line = {
-        "metric": METRIC, "value": ws * flops / t_step / 1e12, "unit": "TFLOP/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator)",
-        "config": config_of(wl, args, l2=f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)"),
+    nominal_tc, nominal_hbm = 2250.0, 7900.0
+    return {
+        "value": ws * flops / t_step / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_per_step,
         "tokens_per_s": ws * wl.T / t_step,
+        "config": config_of(wl, args),
         "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "frac": max(t_tc, t_hbm) / t_step,
+                           "frac_of_nominal": max(flops / (nominal_tc * 1e12),
+                                                  layer_bytes / (nominal_hbm * 1e9)) / t_step,
                            "t_tensor_us": t_tc * 1e6, "t_hbm_us": t_hbm * 1e6,
-                           "compulsory_bytes": layer_bytes, "useful_flops": flops,
-                           "experts_touched": touched},
+                           "compulsory_bytes": layer_bytes, "useful_flops": flops, "experts_touched": touched,
+                           "peaks": "measured (MEASURED_PEAKS); frac_of_nominal against 2.25 PF/s bf16, 7.9 TB/s"},
         "roofline": roof,
         "stages_ms": stage_avg,
         "gpu_launches": launches * args.steps,
         "e2e": e2e,
-        "cpu_baseline": cpu,
         "clocks": clocks,
+    }
+
+
+def _shared_inputs(wl, have: dict, dev):
+    """Device inputs of wl, reusing another workload's weight tensors when the shapes and seed
+    match (the generator gives the same values for the same tensor id, index and seed)."""
+    import torch
+    key = (wl.H, wl.I, wl.E, wl.seed)
+    if key in have:
+        d = dict(have[key])
+        d["x"] = synth.normal_bf16_torch(wl.T * wl.H, 1.0, synth.TID_X, wl.seed, device=dev).view(wl.T, wl.H)
+        d["bias"] = torch.from_numpy(synth.zipf_bias(wl.E, wl.zipf_s)).to(dev)
+        return d
+    d = synth.device_inputs(wl, device=dev)
+    have.clear()                                 # keep one weight set resident at a time
+    have[key] = d
+    return d
+
+
+def run_ours(args, wl):
+    import torch
+    import mixture_experts_layer_top_gb300 as moe
+
+    ws, rank, local = dist_env()
+    group = False
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        group = True
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.build()
+    peaks, peak_src = load_peaks()
+    sampler = None if args.no_clocks else clock_sampler(local)
+
+    have = {}
+    main = measure(wl, _shared_inputs(wl, have, dev), args, dev, local, peaks, peak_src, group, ws, sampler,
+                   with_e2e=not args.no_e2e)
+    extra = {}
+    for name in [n for n in args.also.split(",") if n and n != wl.name]:
+        w2 = synth.WORKLOADS[name]
+        extra[name] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
+                              sampler, with_e2e=not args.no_e2e)
+        extra[name].pop("gpu_launches", None)
+    have.clear()
+    torch.cuda.empty_cache()
+    if sampler:
+        sampler.stop()
+
+    if rank != 0:
+        if group:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        try:
+            cpu = cpu_baseline(wl, args.cpu_budget, weight_source(wl, _shared_inputs(wl, {}, dev)))
+        except Exception as ex:  # reported, not fatal
+            cpu = {"value": None, "error": str(ex)[:200]}
+
+    line = {
+        "metric": METRIC, "value": main["value"], "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator)",
+        "config": main["config"],
+        "tokens_per_s": main["tokens_per_s"],
+        "layer_roofline": main["layer_roofline"],
+        "roofline": main["roofline"],
+        "stages_ms": main["stages_ms"],
+        "gpu_launches": main["gpu_launches"],
+        "e2e": main["e2e"],
+        "cpu_baseline": cpu,
+        "clocks": main["clocks"],
         "peaks": {**peaks, "source": peak_src},
+        "workloads": extra,
     }
     print(json.dumps(line))
     if group:
@@ -407,7 +541,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)   # >= 0.2 s timed, several 50 ms clock samples
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="fine")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="large",
+                    help="the workload of the headline line (default: the large layer)")
+    ap.add_argument("--also", default="fine,skew,smallT",
+                    help="comma-separated workloads also timed in the same run, reported under 'workloads'")
+    ap.add_argument("--shape", default="",
+                    help="T,H,I,E,k[,zipf_s]: a custom workload (same laws and seed) instead of --workload, "
+                         "e.g. a cut-down case for a profiler capture")
     ap.add_argument("--schedule", type=int, choices=(0, 1, 2, 3), default=3,
                     help="0 wave-serial, 1 interleaved, 2 phased, 3 auto (the library's choice)")
     ap.add_argument("--wave-experts", type=int, default=0, help="experts per wave (0: fill the SMs)")
@@ -422,6 +562,12 @@ def main(argv=None):
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     wl = synth.WORKLOADS[args.workload]
+    if args.shape:
+        v = args.shape.split(",")
+        T, H, I, E, k = (int(a) for a in v[:5])
+        z = float(v[5]) if len(v) > 5 else 0.0
+        wl = synth.Workload(f"custom-{T}x{H}x{I}x{E}x{k}" + (f"-z{z}" if z else ""), T, H, I, E, k, zipf_s=z,
+                            description=f"custom T={T} H={H} I={I} E={E} top-{k}" + (f" Zipf({z})" if z else ""))
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -26,6 +26,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
+import time
 
 import numpy as np
 
@@ -204,7 +205,7 @@ def expert_h_range(x_row, W1e, act: int = ACT_SWIGLU):
 
 
 def _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_intermediates,
-                       experts_per_batch: int = 16):
+                       experts_per_batch: int = 16, timing=None):
     """y of the sampled tokens, driven expert by expert: the weights of each expert the
     sample touches are requested once, a batch of experts at a time (host memory stays
     bounded), and every (token, slot) row of those experts is evaluated by
@@ -245,10 +246,13 @@ def _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_interm
         nf_b = np.zeros(n, np.int32) if bounds else None
         lo_b = np.empty((n, I), np.uint16) if bounds else None
         hi_b = np.empty((n, I), np.uint16) if bounds else None
+        tc = time.perf_counter()
         L.oracle_expert_rows(H, I, act, px, n, toks.ctypes.data, P1, P2, a_b.ctypes.data, o_b.ctypes.data,
                              dl_b.ctypes.data if bounds else None, dh_b.ctypes.data if bounds else None,
                              nf_b.ctypes.data if bounds else None, lo_b.ctypes.data if bounds else None,
                              hi_b.ctypes.data if bounds else None)
+        if timing is not None:
+            timing["compute_s"] = timing.get("compute_s", 0.0) + time.perf_counter() - tc
         ss = np.array([r[0] for r in rows], np.int64)
         jj = np.array([r[1] for r in rows], np.int64)
         o[ss, jj] = o_b
@@ -267,6 +271,7 @@ def _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_interm
     ws = np.ascontiguousarray(w[tokens], dtype=np.float32)
     y = np.empty((ns, H), np.uint16)
     out = {}
+    tc = time.perf_counter()
     if bounds:
         y32 = np.empty((ns, H), np.float32)
         ylo = np.empty((ns, H), np.float64)
@@ -276,6 +281,8 @@ def _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_interm
         out.update(y32=y32, ylo=ylo, yhi=yhi, nflag=nflag, a_lo=a_lo, a_hi=a_hi)
     else:
         L.oracle_combine(H, k, ns, ws.ctypes.data, o.ctypes.data, None, None, y.ctypes.data, None, None, None)
+    if timing is not None:
+        timing["compute_s"] = timing.get("compute_s", 0.0) + time.perf_counter() - tc
     out["y"] = y
     if want_intermediates:
         out["a"], out["o"] = a, o
@@ -284,24 +291,28 @@ def _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_interm
 
 def forward(x, Wr, bias, W1, W2, k: int, act: int = ACT_SWIGLU, tokens=None,
             logits=None, want_intermediates: bool = False, bounds: bool = False,
-            experts_per_batch: int = 16) -> dict:
+            experts_per_batch: int = 16, timing=None) -> dict:
     """The whole layer on host arrays.  ``W1``/``W2`` are [E,H,2I]/[E,I,H] arrays or
     callables e -> per-expert matrix (each called once per expert the sample touches,
     ``experts_per_batch`` experts held at a time).  ``logits`` given: used instead of x*Wr.
     ``tokens``: which tokens get y (default all).  ``bounds``: also y32, ylo, yhi, nflag
-    (see the module docstring)."""
+    (see the module docstring).  ``timing`` (a dict): receives compute_s, the seconds spent in
+    the oracle's own arithmetic (fetching the expert weights is not counted)."""
+    tc = time.perf_counter()
     if logits is None:
         logits = router_logits(x, Wr, bias)
     E = logits.shape[1]
     ids, w = topk(logits, k)
     counts, offsets, row_pair, row_of = dispatch(ids, E)
+    if timing is not None:
+        timing["compute_s"] = timing.get("compute_s", 0.0) + time.perf_counter() - tc
     T = x.shape[0]
     if tokens is None:
         tokens = np.arange(T, dtype=np.int64)
     W1_of = W1 if callable(W1) else (lambda e: W1[e])
     W2_of = W2 if callable(W2) else (lambda e: W2[e])
     res = _forward_by_expert(x, ids, w, tokens, W1_of, W2_of, act, bounds, want_intermediates,
-                             experts_per_batch)
+                             experts_per_batch, timing)
     out = dict(logits=logits, ids=ids, w=w, counts=counts, offsets=offsets,
                row_pair=row_pair, row_of=row_of, tokens=np.asarray(tokens, np.int64))
     out.update(res)

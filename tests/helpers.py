@@ -162,10 +162,11 @@ def logit_bound(x_bits: np.ndarray, Wr_bits: np.ndarray, bias, est: np.ndarray, 
 
 
 def check_logits(lg_gpu: np.ndarray, ref: dict, x_bits: np.ndarray, Wr_bits: np.ndarray, cH: float, bias=None,
-                 rows=None) -> dict:
+                 rows=None, max_ratio: float = 0.25) -> dict:
     """Default router: every selected expert's logit bit-exact, every other entry exact or
-    within logit_bound; the observed estimate error must stay under a quarter of the bound
-    (the bound carries a wide margin over the tensor-core accumulation error)."""
+    within logit_bound; the observed estimate error must stay under max_ratio of the bound
+    (by default a quarter: the bound carries a wide margin over the tensor-core accumulation
+    error on ordinary inputs)."""
     ref_l = ref["logits"]
     ids = ref["ids"]
     if rows is not None:
@@ -178,5 +179,5 @@ def check_logits(lg_gpu: np.ndarray, ref: dict, x_bits: np.ndarray, Wr_bits: np.
     bound = logit_bound(x_bits, Wr_bits, bias, lg_gpu, cH)
     ratio = np.where(exact, 0.0, d / bound)
     assert np.all(np.isfinite(lg_gpu[~exact])), "non-finite estimate"
-    assert ratio.max() <= 0.25, f"estimate error {ratio.max():.3f} of the stated bound"
+    assert ratio.max() <= max_ratio, f"estimate error {ratio.max():.3f} of the stated bound"
     return dict(exact_frac=float(exact.mean()), max_ratio=float(ratio.max()))

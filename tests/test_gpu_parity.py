@@ -166,20 +166,54 @@ def test_schedules_bitwise_identical():
 
 
 # --------------------------------------------------------------------------- full-size workloads
+def _cover_tokens(ids: np.ndarray, n: int, min_experts: int) -> np.ndarray:
+    """n tokens chosen greedily (by the oracle's routing) so that their experts cover as many
+    distinct experts as possible - at least min_experts - plus the first and last token."""
+    T = ids.shape[0]
+    chosen, seen = [0, T - 1], set(ids[0]) | set(ids[T - 1])
+    order = np.random.default_rng(3).permutation(T)
+    while len(chosen) < n:
+        best, gain = None, -1
+        for t in order[:4096]:
+            if t in chosen:
+                continue
+            g = len(set(ids[t]) - seen)
+            if g > gain:
+                best, gain = int(t), g
+        chosen.append(best)
+        seen |= set(ids[best])
+    assert len(seen) >= min_experts, f"only {len(seen)} experts covered"
+    return np.sort(np.array(chosen, np.int64))
+
+
+def _device_weights(d):
+    """Host copies of the expert slices of the device tensors the synth generator drew (the
+    generator's device and host implementations are bit-identical)."""
+    return lambda which, e: d[which][e].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
 @pytest.mark.parametrize("name,nsample,schedule,flags", [
-    ("fine", 48, 0, 0), ("fine", 16, 1, EXACT), ("skew", 32, 0, 0), ("large", 4, 0, 0), ("smallT", 4, 0, 0),
-    ("smallT", 4, 1, EXACT)])
+    ("fine", 48, 0, 0), ("fine", 16, 1, EXACT), ("skew", 32, 0, 0), ("large", 64, 0, 0), ("smallT", 128, 0, 0),
+    ("smallT", 128, 1, EXACT)])
 def test_workload_parity(name, nsample, schedule, flags):
     """Full-size workloads: routing of every token against the oracle (ids, counts, order
-    bit-exact), logits (bit-exact, or selected-exact and bounded), y on sampled tokens."""
+    bit-exact), logits (bit-exact, or selected-exact and bounded), y on sampled tokens: every
+    token of the 128-token workload, and on the large layer 64 tokens chosen to reach at least
+    200 of its 256 experts."""
     wl = synth.WORKLOADS[name]
     bias = _bias(wl)
     d = synth.device_inputs(wl)
     layer = _layer(wl, schedule, bias=bias, flags=flags)
     y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
     h = synth.host_inputs(wl, weights=False)
-    tok = sample_tokens(wl.T, nsample)
-    ref = oracle_for(wl, h["x"], h["Wr"], bias, tok)
+    lg_ref = oracle.router_logits(h["x"], h["Wr"], bias)
+    if name == "large":
+        tok = _cover_tokens(oracle.topk(lg_ref, wl.k)[0], nsample, 200)
+        assert np.array_equal(synth.expert_slice_host(wl, "W2", 17), _device_weights(d)("W2", 17))
+    else:
+        tok = sample_tokens(wl.T, nsample)
+    ref = oracle.forward(h["x"], h["Wr"], bias, lambda e: _device_weights(d)("W1", e),
+                         lambda e: _device_weights(d)("W2", e), wl.k, tokens=tok, logits=lg_ref, bounds=True)
     if flags & EXACT:
         assert np.array_equal(logits.cpu().numpy(), ref["logits"]), "logits not bit-exact"
     else:
@@ -189,7 +223,9 @@ def test_workload_parity(name, nsample, schedule, flags):
     routing_equal(layer.routing(wl.T), ref, wl.T)
     if name == "skew":
         assert (ref["counts"] == 0).any(), "skewed workload should leave experts idle"
-    check_y(bits(y)[tok], ref, what=name)
+    n_exp = len({int(e) for e in ref["ids"][tok].ravel()})
+    st = check_y(bits(y)[tok], ref, what=name)
+    print(f"{name}: y on {len(tok)} tokens ({n_exp} experts): {st}")
     del d
     layer.close()
     torch.cuda.empty_cache()
@@ -434,6 +470,63 @@ def test_router_certified_selection_on_ties_and_infinities():
     assert nan.any() and np.array_equal(np.isnan(lg), nan), "NaN logits differ"   # 0 * inf
     assert np.array_equal(lg[~nan].view(np.uint32), rl[~nan].view(np.uint32)), "fallback logits not canonical"
     routing_equal(layer.routing(T), ref, T)
+
+
+def _stress_router_inputs(T, H, E, k, mode, seed=21):
+    """Inputs built against the tensor-core router's error model; experts 0..23 are contenders
+    with one shared small positive column, experts 24.. have a strongly negative column (the
+    bound excludes them, so their estimates are written out).
+    mode "align": the first 16 h of every token hold +64 and W_router +1 there, the last 16 h
+    the same x with W_router -1, so every exact logit loses those 1024-sized terms, but the
+    accumulation chain that takes the first K block carries a partial sum of 1024 while it adds
+    the many small products in between (whose low bits an aligning adder drops).
+    mode "ladder": contender pair p adds, at one h, p times one fp32 unit of the logit (x there
+    picks 0, 1 or 2 units per token), so the k-th and (k+1)-th logits tie or differ by 1-2
+    units."""
+    rng = np.random.default_rng(seed)
+    x = (2.0 ** -3 * (1.0 + rng.integers(0, 128, size=(T, H)) / 128.0)).astype(np.float32)
+    Wr = np.empty((H, E), np.float32)
+    base = 2.0 ** -6 * (1.0 + rng.integers(0, 128, size=H) / 128.0)
+    Wr[:, :24] = base[:, None]
+    Wr[:, 24:] = -4.0 * 2.0 ** -6 * (1.0 + rng.integers(0, 128, size=(H, E - 24)) / 128.0)
+    if mode == "align":
+        x[:, :16] = 64.0
+        x[:, H - 16:] = 64.0
+        Wr[:16] = 1.0
+        Wr[H - 16:] = -1.0
+    else:
+        hz = 20
+        x[:, hz] = rng.choice([0.0, 2.0 ** -3, 2.0 ** -2], size=T)
+        Wr[hz, :24] = (np.arange(24) // 2) * 2.0 ** -18
+    xb, wb = oracle.f32_to_bf16(x), oracle.f32_to_bf16(Wr)
+    assert np.array_equal(oracle.bf16_to_f32(xb), x) and np.array_equal(oracle.bf16_to_f32(wb), Wr)
+    return xb, wb
+
+
+@pytest.mark.parametrize("mode", ["align", "ladder"])
+def test_router_certificate_under_stress(mode):
+    """Default router on inputs built to push the tensor-core estimate error toward its bound
+    ("align") or to put the k-th place on exact ties and 1-2 unit gaps ("ladder"): routing
+    bit-exact, selected logits canonical, every written estimate within the bound; the
+    largest observed error/bound ratio is printed."""
+    T, H, I, E, k = 512, 1024, 256, 64, 8
+    xb, wb = _stress_router_inputs(T, H, E, k, mode)
+    wl = synth.Workload("rstress", T, H, I, E, k)
+    hw = synth.host_inputs(wl)
+    ref = oracle_for(wl, xb, wb, None, None, full_weights=(hw["W1"], hw["W2"]))
+    lg = ref["logits"]
+    srt = np.sort(lg, axis=1)[:, ::-1]
+    gap_ulp = (srt[:, k - 1] - srt[:, k]) / np.spacing(np.abs(srt[:, k - 1]))
+    if mode == "ladder":
+        assert set(np.unique(gap_ulp)) >= {0.0, 1.0, 2.0}, "ties and 1-2 unit gaps at the k-th place expected"
+    layer = _layer(wl)
+    y, logits = layer.forward(from_bits(xb), from_bits(wb), from_bits(hw["W1"]), from_bits(hw["W2"]), check=True)
+    routing_equal(layer.routing(T), ref, T)
+    st = check_logits(logits.cpu().numpy(), ref, xb, wb, layer.router_bound(T), max_ratio=1.0)
+    print(f"router stress ({mode}): k-th gaps (ulp) {np.unique(gap_ulp, return_counts=True)}; estimates written for "
+          f"{1 - st['exact_frac']:.2f} of the logits; largest error/bound {st['max_ratio']:.3e}")
+    assert st["exact_frac"] < 0.9, "the losers' estimates should be written out"
+    check_y(bits(y), ref)
 
 
 def test_logits_as_input_and_one_hot_expert():
