@@ -489,7 +489,7 @@ def run_ours(args, wl):
     main = measure(wl, _shared_inputs(wl, have, dev), args, dev, local, peaks, peak_src, group, ws, sampler,
                    with_e2e=not args.no_e2e)
     extra = {}
-    for name in [n for n in args.also.split(",") if n and n != wl.name]:
+    for name in [n for n in args.also.split(",") if n and n != "none" and n != wl.name]:
         w2 = synth.WORKLOADS[name]
         extra[name] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
                               sampler, with_e2e=not args.no_e2e)
@@ -535,6 +535,67 @@ def run_ours(args, wl):
     return 0
 
 
+# ----------------------------------------------------------------------------- schedule sweep
+SWEEP_SCHEDULES = [("auto", 3, 0, 1), ("wave-serial, waves fill the SMs", 0, 0, 1), ("wave-serial, 32 experts", 0, 32, 1),
+                   ("interleaved lead 1", 1, 0, 1), ("interleaved lead 2", 1, 0, 2), ("interleaved lead 3", 1, 0, 3),
+                   ("interleaved 32 experts lead 1", 1, 32, 1), ("phased", 2, 0, 1)]
+
+
+def sweep_points():
+    for s in (0.0, 0.6, 1.2, 2.0):
+        for T in (512, 2048, 8192, 16384):
+            yield synth.Workload(f"fine-shape T={T} zipf={s}", T, 2048, 768, 128, 8, zipf_s=s)
+    for s in (0.0, 1.2):
+        for T in (128, 1024, 4096):
+            yield synth.Workload(f"large-shape T={T} zipf={s}", T, 7168, 2048, 256, 8, zipf_s=s)
+
+
+def run_schedule_sweep(args):
+    """Every tile schedule on every sweep point, in alternating rounds (same process, same
+    inputs), with the L2 flushed before each step: one JSON line per (point, schedule) with the
+    median step and grouped-GEMM times (CUDA events; the stage events of the library)."""
+    import torch
+    import mixture_experts_layer_top_gb300 as moe
+    moe.build()
+    torch.cuda.set_device(0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    have = {}
+    for wl in sweep_points():
+        d = _shared_inputs(wl, have, torch.device("cuda", 0))
+        bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
+        layers = {name: moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, schedule=sc, wave_experts=we,
+                                                   lead_waves=lead, flags=moe.MOE_FLAG_STAGE_TIMING), 0,
+                                     router_bias=bias)
+                  for name, sc, we, lead in SWEEP_SCHEDULES}
+        lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+        y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+        res = {n: ([], []) for n in layers}
+        for layer in layers.values():
+            for _ in range(3):
+                layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=lg, y=y)
+            layer.check()
+        counts = layers["auto"].routing(wl.T)["counts"].cpu()
+        for _ in range(3):
+            for name, layer in layers.items():
+                for _ in range(10):
+                    flush.zero_()
+                    a, b = _events(1)[0]
+                    a.record()
+                    layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=lg, y=y)
+                    b.record()
+                    b.synchronize()
+                    res[name][0].append(a.elapsed_time(b))
+                    res[name][1].append(layer.stage_times()["grouped_gemm"])
+        for name, layer in layers.items():
+            layer.check()
+            layer.close()
+            print(json.dumps({"point": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "zipf_s": wl.zipf_s,
+                              "experts_touched": int((counts > 0).sum()), "max_rows": int(counts.max()),
+                              "schedule": name, "step_ms": statistics.median(res[name][0]),
+                              "gemm_ms": statistics.median(res[name][1])}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -544,7 +605,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="large",
                     help="the workload of the headline line (default: the large layer)")
     ap.add_argument("--also", default="fine,skew,smallT",
-                    help="comma-separated workloads also timed in the same run, reported under 'workloads'")
+                    help="comma-separated workloads also timed in the same run, reported under 'workloads' "
+                         "('none': only the headline workload)")
     ap.add_argument("--shape", default="",
                     help="T,H,I,E,k[,zipf_s]: a custom workload (same laws and seed) instead of --workload, "
                          "e.g. a cut-down case for a profiler capture")
@@ -554,6 +616,8 @@ def main(argv=None):
     ap.add_argument("--lead-waves", type=int, default=1, help="interleave lead D (interleaved schedule)")
     ap.add_argument("--gemm-split", choices=("auto", "streaming", "compute"), default="auto",
                     help="shared-memory split of the grouped GEMM (auto: the library default, streaming)")
+    ap.add_argument("--schedule-sweep", action="store_true",
+                    help="time every tile schedule over a sweep of routing skew and token counts (JSON lines)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -568,6 +632,8 @@ def main(argv=None):
         z = float(v[5]) if len(v) > 5 else 0.0
         wl = synth.Workload(f"custom-{T}x{H}x{I}x{E}x{k}" + (f"-z{z}" if z else ""), T, H, I, E, k, zipf_s=z,
                             description=f"custom T={T} H={H} I={I} E={E} top-{k}" + (f" Zipf({z})" if z else ""))
+    if args.schedule_sweep:
+        return run_schedule_sweep(args)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
