@@ -324,7 +324,7 @@ def _events(n):
     return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
 
 
-def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e2e=True):
+def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e2e=True, extra_flags=0):
     """One workload: W warm-up steps, K timed steps (CUDA events on the launching stream, L2
     flushed before each step outside the events), the host-buffer e2e steps, and the per-stage
     split from a second plan.  Returns the fields of its JSON entry."""
@@ -333,6 +333,7 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
 
     bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
     flags = {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING, "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
+    flags |= extra_flags
     cfg = dict(schedule=args.schedule, wave_experts=args.wave_experts, lead_waves=args.lead_waves)
     layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags, **cfg), local, router_bias=bias)
     logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=dev)
@@ -494,6 +495,12 @@ def run_ours(args, wl):
         extra[name] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
                               sampler, with_e2e=not args.no_e2e)
         extra[name].pop("gpu_launches", None)
+    for name in [n for n in args.also_single.split(",") if n and n != "none"]:
+        w2 = synth.WORKLOADS[name]
+        key = f"{name} (single launch)"
+        extra[key] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
+                             sampler, with_e2e=False, extra_flags=moe.MOE_FLAG_SINGLE_LAUNCH)
+        extra[key]["launches_per_step"] = extra[key].pop("gpu_launches") // args.steps
     have.clear()
     torch.cuda.empty_cache()
     if sampler:
@@ -604,7 +611,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="large",
                     help="the workload of the headline line (default: the large layer)")
-    ap.add_argument("--also", default="fine,skew,smallT",
+    ap.add_argument("--also-single", default="tiny,smallT",
+                    help="comma-separated workloads also timed with the whole layer in one launch "
+                         "(MOE_FLAG_SINGLE_LAUNCH), reported under 'workloads' as '<name> (single launch)'")
+    ap.add_argument("--also", default="fine,skew,smallT,tiny",
                     help="comma-separated workloads also timed in the same run, reported under 'workloads' "
                          "('none': only the headline workload)")
     ap.add_argument("--shape", default="",

@@ -106,6 +106,19 @@ typedef enum {
  *   cH from moe_router_bound (at most (H/16 + 1) 2^-17 + (H/32 + 8 + 64) 2^-22).
  * MOE_FLAG_EXACT_LOGITS evaluates every logit in the canonical order on the CUDA cores. */
 #define MOE_FLAG_EXACT_LOGITS (1u << 5)
+/* The whole layer as ONE kernel launch (after the per-forward memset of the expert counts):
+ * the MegaMoE design of the X-Stage paper's introduction - one persistent kernel for routing,
+ * Dispatch, Linear-1, the activation, Linear-2 and Combine.  The kernel runs on the grouped
+ * GEMM's grid and goes through the steps as phases separated by grid-wide barriers (each
+ * bounded by timeout_ns; on expiry MOE_ERR_TIMEOUT as for any device wait).  The router is
+ * the all-canonical one (as MOE_FLAG_EXACT_LOGITS: every logit written is canonical), and y,
+ * the logits and the routing are bitwise those of the multi-launch path with
+ * MOE_FLAG_EXACT_LOGITS.  It removes the launch gaps between the steps, which dominate when a
+ * forward holds few tokens; with many tokens the multi-launch path (tensor-core router)
+ * is faster.  MOE_SCHED_PHASED runs its tile list in the one launch; MOE_FLAG_GEMM_COMPUTE is
+ * ignored (the default ring split); with MOE_FLAG_STAGE_TIMING the whole launch is reported
+ * as stage 3 (the grouped GEMM) and the other stages as 0. */
+#define MOE_FLAG_SINGLE_LAUNCH (1u << 6)
 #define MOE_FLAG_TEST_BAD_ID (1u << 9)  /* test only: Dispatch sees the first (token, slot) pair's expert
                                           id out of range; the pair is dropped, no access leaves the
                                           workspace, and moe_get_status reports MOE_ERR_DEVICE_CHECK */
@@ -188,7 +201,10 @@ MOE_API moe_status_t moe_debug_intermediates(moe_plan_t plan, int32_t T, void* h
 MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
 
 /* Wait-time trace of the last forward's grouped GEMM (needs MOE_FLAG_TRACE; synchronises the
- * device).  Writes n = CTAs x 8 uint64 values to host_buf (cap = capacity in values); per CTA:
+ * device).  Writes n = (CTAs + 1) x 8 uint64 values to host_buf (CTAs: the larger of the two
+ * launch paths' grids; a CTA the last launch did not have reads zero; the last row holds the
+ * %globaltimer stamps of a MOE_FLAG_SINGLE_LAUNCH forward - start, end of router logits, top-k,
+ * Dispatch, gather, grouped GEMM, Combine - and zeros otherwise) (cap = capacity in values); per CTA:
  * {producer waiting for a free stage, producer waiting for Linear-1 readiness, MMA issuer waiting
  * for a free accumulator, MMA issuer waiting for operands, epilogue waiting for an accumulator,
  * CTA lifetime} in nanoseconds, then {Linear-1 tiles, Linear-2 tiles}. */

@@ -40,6 +40,7 @@ MOE_FLAG_TRACE = 1 << 2
 MOE_FLAG_GEMM_STREAMING = 1 << 3
 MOE_FLAG_GEMM_COMPUTE = 1 << 4
 MOE_FLAG_EXACT_LOGITS = 1 << 5
+MOE_FLAG_SINGLE_LAUNCH = 1 << 6
 TRACE_FIELDS = ("prod_wait_empty_ns", "prod_wait_ready_ns", "mma_wait_tempty_ns", "mma_wait_full_ns",
                 "epi_wait_tfull_ns", "cta_ns", "tiles_l1", "tiles_l2")
 MOE_FLAG_TEST_STALL = 1 << 8
@@ -181,8 +182,9 @@ def moe_last_launch_count(plan: int) -> int:
 
 
 def moe_trace_read(plan: int) -> np.ndarray:
-    """Per-CTA wait-time counters of the last forward's grouped GEMM: [CTAs, 8] uint64
-    (fields in TRACE_FIELDS).  Needs MOE_FLAG_TRACE."""
+    """Per-CTA wait-time counters of the last forward's grouped GEMM: [CTAs + 1, 8] uint64
+    (fields in TRACE_FIELDS; the last row: the phase stamps of a single-launch forward).
+    Needs MOE_FLAG_TRACE."""
     n = ctypes.c_size_t(0)
     L = load()
     st = L.moe_trace_read(plan, None, 0, ctypes.byref(n))

@@ -1,6 +1,7 @@
 // C ABI of the MoE layer (include/moe_gb300.h): plan, forward, status, debug
 // hooks.  Host code only; every step of the layer runs in this library's
-// kernels (router.cu, dispatch.cu, gemm.cu, combine.cu).
+// kernels (router_tc.cu, router.cu, dispatch.cu, gemm.cu, combine.cu, and fused.cu for
+// the single-launch layer).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -21,6 +22,7 @@ struct moe_plan_s {
   int device;
   int num_sms;
   int gemm_grid;   // CTAs of the grouped GEMM (all 2-CTA clusters co-resident)
+  int fused_grid;  // CTAs of the single-launch layer (all 2-CTA clusters co-resident)
   int64_t R_max, max_mt, max_tiles, R_pad_max;
   void* base;
   size_t bytes;
@@ -37,7 +39,7 @@ struct moe_plan_s {
   cudaEvent_t ev_fork;
   cudaEvent_t ev_range[4];
   int last_launches;
-  unsigned long long* trace;   // [gemm_grid][TRACE_SLOTS] when MOE_FLAG_TRACE
+  unsigned long long* trace;   // [max(gemm_grid, fused_grid) + 1][TRACE_SLOTS] when MOE_FLAG_TRACE
 };
 
 namespace {
@@ -139,7 +141,7 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
   size_t sizes[N_BUFS] = {};
   sizes[B_IDS] = (size_t)R * 4;
   sizes[B_W] = (size_t)R * 4;
-  sizes[B_COUNTS] = (size_t)c.E * 4 * (1 + (c.T_max + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK);   // counts, chist
+  sizes[B_COUNTS] = 16 + (size_t)c.E * 4 * (1 + (c.T_max + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK);   // gbar, counts, chist
   sizes[B_OFFSETS] = (size_t)(c.E + 1) * 4;
   sizes[B_ROW_PAIR] = (size_t)R * 4;
   sizes[B_ROW_OF] = (size_t)R * 4;
@@ -188,6 +190,36 @@ moe_status_t check_forward_args(moe_plan_t p, int32_t T, const void* x, const fl
   return MOE_OK;
 }
 
+// CTA rows of the trace buffer (the larger grid of the two launch paths); one more row of
+// TRACE_SLOTS values follows them: the phase stamps of a single-launch forward.
+int trace_ctas(const moe_plan_s* p) { return p->gemm_grid > p->fused_grid ? p->gemm_grid : p->fused_grid; }
+
+// Arguments of the grouped GEMM (both launch paths) other than the tile range.
+GemmArgs gemm_args(const moe_plan_s* p) {
+  const moe_config_t& c = p->cfg;
+  GemmArgs ga;
+  ga.tiles = reinterpret_cast<const int4*>(p->ws.tiles);
+  ga.sched = p->ws.sched;
+  ga.counts = p->ws.counts;
+  ga.prow_w = p->ws.prow_w;
+  ga.h_pad = p->ws.h_pad;
+  ga.P_pad = p->ws.P_pad;
+  ga.S_pad = p->ws.S_pad;
+  ga.ready = p->ws.ready;
+  ga.err = p->ws.err;
+  ga.trace = p->trace;
+  ga.range_sel = 2;
+  ga.H = c.H;
+  ga.I = c.I;
+  ga.E = c.E;
+  ga.R_pad = (int)p->R_pad_max;
+  ga.nL1 = c.I / L1_COLS;
+  ga.nL2 = c.H / L2_COLS;
+  ga.flags = c.flags;
+  ga.timeout_ns = c.timeout_ns;
+  return ga;
+}
+
 // One forward, enqueued on st.  x_src, when not null, is page-locked host memory mapped into
 // the device's address space: the layer's input is copied from it into x (the plan's staging
 // buffer) inside this call, in HOST_RANGES token ranges on st_aux, and the tensor-core router
@@ -211,7 +243,40 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   } while (0)
   rec(0);
   const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
-  MOE_CK(cudaMemsetAsync(p->ws.counts, 0, sizeof(int32_t) * E * (1 + chunks), st));   // counts and chist
+  // grid-barrier word, counts and chist (one contiguous range)
+  MOE_CK(cudaMemsetAsync(p->ws.gbar, 0, 16 + sizeof(int32_t) * E * (1 + chunks), st));
+  if (c.flags & MOE_FLAG_SINGLE_LAUNCH) {
+    if (x_src) {   // the input lands whole before the one launch
+      MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
+      ++nl;
+    }
+    rec(1);
+    rec(2);
+    rec(3);
+    CUtensorMap tA1, tB1, tA2, tB2, tH, tP;
+    const uint64_t Rp = (uint64_t)p->R_pad_max;
+    if (!make_tmap(&tA1, p->ws.x_pad, H, Rp, BM) || !make_tmap(&tB1, W1, 2 * I, (uint64_t)E * H, BK) ||
+        !make_tmap(&tA2, p->ws.h_pad, I, Rp, BM) || !make_tmap(&tB2, W2, H, (uint64_t)E * I, BK) ||
+        !make_tmap(&tH, p->ws.h_pad, I, Rp, 32) || !make_tmap(&tP, p->ws.P_pad, H, Rp, 32)) {
+      p->last_launches = nl;
+      return MOE_ERR_CUDA;
+    }
+    GemmArgs ga = gemm_args(p);
+    if (p->trace)
+      MOE_CK(cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1), st));
+    const int sched_mode = (c.schedule == MOE_SCHED_AUTO) ? MOE_SCHED_WAVE_SERIAL : c.schedule;
+    const int sched_we = (c.schedule == MOE_SCHED_AUTO) ? E : c.wave_experts;
+    MOE_CK(launch_fused_layer(tA1, tB1, tA2, tB2, tH, tP, p->ws, p->ws.gbar, static_cast<const uint16_t*>(x),
+                              static_cast<const uint16_t*>(W_router), p->bias, router_logits,
+                              static_cast<uint16_t*>(y), T, H, I, E, k, p->fused_grid, sched_mode, sched_we,
+                              c.lead_waves, (int)p->R_pad_max, (c.flags & MOE_FLAG_TEST_BAD_ID) != 0, ga,
+                              trace_ctas(p), st));
+    ++nl;
+    rec(4);
+    rec(5);
+    p->last_launches = nl;
+    return MOE_OK;
+  }
   const bool tc_router = W_router && !(c.flags & MOE_FLAG_EXACT_LOGITS);
   if (x_src && !tc_router) {   // whole copy first
     MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
@@ -285,27 +350,9 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     p->last_launches = nl;
     return MOE_ERR_CUDA;
   }
-  GemmArgs ga;
-  ga.tiles = reinterpret_cast<const int4*>(p->ws.tiles);
-  ga.sched = p->ws.sched;
-  ga.counts = p->ws.counts;
-  ga.prow_w = p->ws.prow_w;
-  ga.h_pad = p->ws.h_pad;
-  ga.P_pad = p->ws.P_pad;
-  ga.S_pad = p->ws.S_pad;
-  ga.ready = p->ws.ready;
-  ga.err = p->ws.err;
-  ga.trace = p->trace;
+  GemmArgs ga = gemm_args(p);
   if (p->trace)
-    MOE_CK(cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid, st));
-  ga.H = H;
-  ga.I = I;
-  ga.E = E;
-  ga.R_pad = (int)p->R_pad_max;
-  ga.nL1 = I / L1_COLS;
-  ga.nL2 = H / L2_COLS;
-  ga.flags = c.flags;
-  ga.timeout_ns = c.timeout_ns;
+    MOE_CK(cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1), st));
   const bool streaming = !(c.flags & MOE_FLAG_GEMM_COMPUTE);   // the deeper operand ring by default
   if (c.schedule == MOE_SCHED_PHASED) {
     ga.range_sel = 0;
@@ -394,7 +441,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   auto at = [&](Buf i) { return b + L.off[i]; };
   p->ws.ids = reinterpret_cast<int32_t*>(at(B_IDS));
   p->ws.w = reinterpret_cast<float*>(at(B_W));
-  p->ws.counts = reinterpret_cast<int32_t*>(at(B_COUNTS));
+  p->ws.gbar = reinterpret_cast<unsigned int*>(at(B_COUNTS));
+  p->ws.counts = reinterpret_cast<int32_t*>(at(B_COUNTS) + 16);
   p->ws.chist = p->ws.counts + cfg->E;
   p->ws.offsets = reinterpret_cast<int32_t*>(at(B_OFFSETS));
   p->ws.row_pair = reinterpret_cast<int32_t*>(at(B_ROW_PAIR));
@@ -431,10 +479,10 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
       return fail(MOE_ERR_CUDA);
   }
   if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess ||
-      router_tc_prepare() != cudaSuccess)
+      router_tc_prepare() != cudaSuccess || fused_prepare(device, &p->fused_grid) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   if (cfg->flags & MOE_FLAG_TRACE) {
-    if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * p->gemm_grid) != cudaSuccess) {
+    if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1)) != cudaSuccess) {
       cudaGetLastError();
       p->trace = nullptr;
       return fail(MOE_ERR_OOM);
@@ -538,7 +586,7 @@ moe_status_t moe_stage_times(moe_plan_t p, float* ms) {
 
 moe_status_t moe_trace_read(moe_plan_t p, uint64_t* host_buf, size_t cap, size_t* n) {
   if (!p || !n || !p->trace) return MOE_ERR_INVALID_ARG;
-  const size_t cnt = (size_t)TRACE_SLOTS * p->gemm_grid;
+  const size_t cnt = (size_t)TRACE_SLOTS * (trace_ctas(p) + 1);
   *n = cnt;
   if (!host_buf) return MOE_OK;
   if (cap < cnt) return MOE_ERR_INVALID_ARG;
@@ -581,7 +629,7 @@ moe_status_t moe_debug_schedule(moe_plan_t p, int32_t* tiles_out, int64_t cap, i
     return MOE_ERR_CUDA;
   n_out[0] = sc[0];
   n_out[1] = sc[1];
-  n_out[2] = p->gemm_grid / PAIR;
+  n_out[2] = ((p->cfg.flags & MOE_FLAG_SINGLE_LAUNCH) ? p->fused_grid : p->gemm_grid) / PAIR;
   if (tiles_out && sc[1] > 0) {
     if (cap < sc[1]) return MOE_ERR_INVALID_ARG;
     if (cudaMemcpy(tiles_out, p->ws.tiles, sizeof(int32_t) * 4 * (size_t)sc[1], cudaMemcpyDeviceToHost) != cudaSuccess)

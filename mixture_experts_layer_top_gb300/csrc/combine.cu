@@ -9,52 +9,21 @@
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "layer_parts.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 namespace {
 
-// One thread per 8 consecutive outputs: k 16-byte loads of fp16 P from the slots'
-// rows (padded row space, found through prow_of), each widened and multiplied by
-// its block's power-of-two scale (exact), fixed-order fp32 sum, 16-byte store.
+// One thread per 8 consecutive outputs (combine_item), grid-stride.
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint16_t* __restrict__ P_pad, const float* __restrict__ S_pad, const int32_t* __restrict__ prow_of,
                int T, int H, int k, uint16_t* __restrict__ y) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int64_t n8 = (int64_t)T * H / 8;
-  const int nS = H / P_SCALE_COLS;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = (i * 8) / H;
-    const int64_t c = (i * 8) % H;
-    const int32_t* pr = prow_of + t * k;
-    float s[8];
-    for (int j = 0; j < k; ++j) {
-      const int64_t row = pr[j];
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(P_pad + row * H + c));
-      const float sc = S_pad[row * nS + c / P_SCALE_COLS];
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
-        const float a = f.x * sc, b = f.y * sc;
-        if (j == 0) {
-          s[2 * q] = a;
-          s[2 * q + 1] = b;
-        } else {
-          s[2 * q] = s[2 * q] + a;
-          s[2 * q + 1] = s[2 * q + 1] + b;
-        }
-      }
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(s[2 * q], s[2 * q + 1]);
-      o[q] = *reinterpret_cast<uint32_t*>(&b2);
-    }
-    *reinterpret_cast<uint4*>(y + t * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x)
+    combine_item(P_pad, S_pad, prow_of, H, k, y, i);
 }
 
 }  // namespace

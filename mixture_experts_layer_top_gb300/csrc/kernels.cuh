@@ -55,6 +55,7 @@ struct Workspace {
   int32_t* ready;     // [max_units]
   uint32_t* err;      // [1]
   unsigned long long* trace;   // [gemm grid][TRACE_SLOTS] wait-time counters (MOE_FLAG_TRACE)
+  unsigned int* gbar; // [4] grid-barrier arrivals of the single-launch layer (just before counts; zeroed with them)
 };
 
 // Per-CTA counters of the grouped GEMM under MOE_FLAG_TRACE (nanoseconds unless noted).
@@ -81,7 +82,7 @@ struct GemmArgs {
   int32_t* ready;
   uint32_t* err;
   unsigned long long* trace;
-  int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all
+  int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all, 3: none
   int H, I, E, R_pad, nL1, nL2;
   uint32_t flags;
   int64_t timeout_ns;
@@ -142,6 +143,14 @@ cudaError_t gemm_prepare(int device, int* grid);   // grid: CTAs of the co-resid
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
                                 const GemmArgs& a, int grid, bool streaming, cudaStream_t st);
+// The whole layer as one launch (fused.cu): grid = the co-resident 2-CTA clusters of that kernel.
+cudaError_t fused_prepare(int device, int* grid);
+cudaError_t launch_fused_layer(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
+                               const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP, const Workspace& ws,
+                               unsigned int* gbar, const uint16_t* x, const uint16_t* Wr, const float* bias,
+                               float* logits, uint16_t* y, int T, int H, int I, int E, int k, int grid, int mode,
+                               int wave_experts, int lead, int dead_row, bool test_bad_id, const GemmArgs& ga,
+                               int trace_ctas, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* P_pad, const float* S_pad, const int32_t* prow_of, int T, int H, int k,
                            uint16_t* y, int num_sms,
                            cudaStream_t st);

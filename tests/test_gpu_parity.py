@@ -618,3 +618,88 @@ def test_invalid_arguments_rejected_before_launch():
     bad[3] = None
     assert moe.moe_forward(layer.plan, wl.T, *bad, s) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_get_status(layer.plan, s) == moe.MOE_OK
+
+
+# --------------------------------------------------------------------------- single launch
+SINGLE = moe.MOE_FLAG_SINGLE_LAUNCH
+
+
+@pytest.mark.parametrize("shape,schedule", [((256, 512, 256, 8, 2), 3), ((1000, 512, 256, 16, 4), 0),
+                                            ((1000, 512, 256, 16, 4), 1), ((300, 768, 384, 6, 3), 2),
+                                            ((33, 768, 256, 200, 8), 3), ((1, 256, 128, 1, 1), 3)])
+def test_single_launch_bitwise_equals_multi_launch_and_oracle(shape, schedule):
+    """MOE_FLAG_SINGLE_LAUNCH (the whole layer in one kernel) against the multi-launch path with
+    all-canonical logits: logits, routing and y bit for bit, on several shapes (E not a multiple of
+    8, one expert, one token) and schedules; y against the full oracle; one launch."""
+    T, H, I, E, k = shape
+    wl = synth.Workload("single", T, H, I, E, k)
+    h = synth.host_inputs(wl)
+    d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
+    multi = _layer(wl, schedule, flags=EXACT)
+    y_m, lg_m = multi.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    r_m = {kk: v.cpu() for kk, v in multi.routing(T).items()}
+    one = _layer(wl, schedule, flags=SINGLE)
+    for _ in range(2):                                  # the plan's second forward starts from the first's state
+        y_s, lg_s = one.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+        assert one.launch_count() == 1
+        assert torch.equal(lg_s, lg_m), "logits differ"
+        for kk, v in one.routing(T).items():
+            assert torch.equal(v.cpu(), r_m[kk]), kk
+        assert torch.equal(y_s.view(torch.int16), y_m.view(torch.int16)), "y differs from the multi-launch path"
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    assert np.array_equal(lg_s.cpu().numpy(), ref["logits"])
+    routing_equal(one.routing(T), ref, T)
+    check_y(bits(y_s), ref)
+    multi.close()
+    one.close()
+
+
+def test_single_launch_workloads_and_inputs():
+    """The single launch on the 128-token workload (full oracle on every token), with the
+    caller's logits as input, and through the host-buffer entry point."""
+    wl = synth.WORKLOADS["smallT"]
+    d = synth.device_inputs(wl)
+    one = _layer(wl, flags=SINGLE)
+    y, lg = one.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    multi = _layer(wl, flags=EXACT)
+    y_m, lg_m = multi.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    assert torch.equal(lg, lg_m) and torch.equal(y.view(torch.int16), y_m.view(torch.int16))
+    h = synth.host_inputs(wl, weights=False)
+    ref = oracle.forward(h["x"], h["Wr"], None, lambda e: _device_weights(d)("W1", e),
+                         lambda e: _device_weights(d)("W2", e), wl.k, bounds=True)
+    assert np.array_equal(lg.cpu().numpy(), ref["logits"])
+    routing_equal(one.routing(wl.T), ref, wl.T)
+    check_y(bits(y), ref)
+    y2, _ = one.forward(d["x"], None, d["W1"], d["W2"], logits=lg.clone(), check=True)     # logits as input
+    assert torch.equal(y2.view(torch.int16), y.view(torch.int16))
+    x_host = d["x"].cpu().pin_memory()
+    y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    lg3 = torch.empty_like(lg)
+    one.forward_host(x_host, d["Wr"], d["W1"], d["W2"], lg3, y_host, check=True)
+    assert torch.equal(y_host.view(torch.int16), y.cpu().view(torch.int16)) and torch.equal(lg3, lg)
+    one.close()
+    multi.close()
+    del d
+    torch.cuda.empty_cache()
+
+
+def test_single_launch_reports_timeout_and_bad_id():
+    """Host-made faults in the single launch: a Linear-2 readiness wait that never completes
+    (bounded, MOE_ERR_TIMEOUT) and an out-of-range expert id seen by Dispatch
+    (MOE_ERR_DEVICE_CHECK); the context stays usable and a clean forward matches the oracle."""
+    wl = synth.WORKLOADS["tiny"]
+    h = synth.host_inputs(wl)
+    d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
+    bad = _layer(wl, flags=SINGLE | moe.MOE_FLAG_TEST_STALL, timeout_ns=20_000_000)
+    bad.forward(d["x"], d["Wr"], d["W1"], d["W2"])
+    assert moe.moe_get_status(bad.plan, bad._stream()) == moe.MOE_ERR_TIMEOUT
+    bad.close()
+    bad = _layer(wl, flags=SINGLE | moe.MOE_FLAG_TEST_BAD_ID)
+    bad.forward(d["x"], d["Wr"], d["W1"], d["W2"])
+    assert moe.moe_get_status(bad.plan, bad._stream()) == moe.MOE_ERR_DEVICE_CHECK
+    bad.close()
+    good = _layer(wl, flags=SINGLE)
+    y, _ = good.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
+    check_y(bits(y), ref)
+    good.close()

@@ -152,3 +152,16 @@ def test_merge_positions_proportional(lib):
     assert sum(seg) == 3
     pos = [i for i, v in enumerate(seg) if v == 1]
     assert pos == [1, 5, 9]          # L2 tiles at ~1/6, 1/2, 5/6 of the segment
+
+
+def test_flag_constants_match_header():
+    """The binding's MOE_FLAG_* / MOE_SCHED_* constants are the header's values."""
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                            "moe_gb300.h")).read()
+    found = 0
+    for name, shift, plain in re.findall(r"#define (MOE_(?:FLAG|SCHED)_[A-Z_]+) +(?:\(1u << (\d+)\)|(\d+))", src):
+        v = (1 << int(shift)) if shift else int(plain)
+        assert getattr(moe, name) == v, name
+        found += 1
+    assert found >= 12
