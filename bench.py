@@ -314,6 +314,7 @@ def config_of(wl, args):
     return {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
             "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
             "wave_experts": args.wave_experts, "lead_waves": args.lead_waves,
+            "launch": "single (MOE_FLAG_SINGLE_LAUNCH)" if getattr(args, "single_launch", False) else "multi",
             "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
             "parallelism": f"replicas x{args.gpus} (no sharding)"}
 
@@ -487,13 +488,14 @@ def run_ours(args, wl):
     sampler = None if args.no_clocks else clock_sampler(local)
 
     have = {}
+    main_flags = moe.MOE_FLAG_SINGLE_LAUNCH if args.single_launch else 0
     main = measure(wl, _shared_inputs(wl, have, dev), args, dev, local, peaks, peak_src, group, ws, sampler,
-                   with_e2e=not args.no_e2e)
+                   with_e2e=not args.no_e2e, extra_flags=main_flags)
     extra = {}
     for name in [n for n in args.also.split(",") if n and n != "none" and n != wl.name]:
         w2 = synth.WORKLOADS[name]
         extra[name] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
-                              sampler, with_e2e=not args.no_e2e)
+                              sampler, with_e2e=not args.no_e2e, extra_flags=main_flags)
         extra[name].pop("gpu_launches", None)
     for name in [n for n in args.also_single.split(",") if n and n != "none"]:
         w2 = synth.WORKLOADS[name]
@@ -626,6 +628,8 @@ def main(argv=None):
     ap.add_argument("--lead-waves", type=int, default=1, help="interleave lead D (interleaved schedule)")
     ap.add_argument("--gemm-split", choices=("auto", "streaming", "compute"), default="auto",
                     help="shared-memory split of the grouped GEMM (auto: the library default, streaming)")
+    ap.add_argument("--single-launch", action="store_true",
+                    help="run the headline (and --also) workloads with the whole layer in one launch")
     ap.add_argument("--schedule-sweep", action="store_true",
                     help="time every tile schedule over a sweep of routing skew and token counts (JSON lines)")
     ap.add_argument("--no-e2e", action="store_true")
