@@ -144,24 +144,6 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
         const int4 tl = args.tiles[i];
         const int ph = tl.x & 1, nb = (tl.x >> 1) & 0x7FFF, e = tl.y, g = tl.w;
         const int row0 = g * UNIT_ROWS + rank * BM;     // this CTA's 128 padded rows of the unit
-        if (ph == 1) {
-          // wait for every Linear-1 tile of this unit, from both CTAs (bounded)
-          const int* rp = args.ready + g;
-          const int need = PAIR * args.nL1 + ((args.flags & MOE_FLAG_TEST_STALL) ? 1 : 0);
-          if (ptx::ld_acquire_gpu(rp) < need) {
-            const uint64_t t0 = ptx::globaltimer();
-            bool ok = false;
-            while (true) {
-              if (ptx::ld_acquire_gpu(rp) >= need) { ok = true; break; }
-              if (*abort_flag) break;
-              if ((int64_t)(ptx::globaltimer() - t0) > tmo) break;
-              __nanosleep(64);
-            }
-            tr_b += ptx::globaltimer() - t0;
-            if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
-          }
-          ptx::fence_proxy_async_global();
-        }
         const int nk = (ph == 0 ? args.H : args.I) / BK;
         // a unit whose valid rows all lie in the even CTA's half: the odd CTA's A rows are
         // padding, whose accumulator rows are never stored, so they are not loaded at all
@@ -175,21 +157,69 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
         // Linear-2 columns [128 r, 128 r + 128) of the 256-column block
         const int c0 = (ph == 0) ? (rank == 0 ? nb * L1_COLS : args.I + nb * L1_COLS) : nb * L2_COLS + rank * 128;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, tmo, abort_flag, trp_a)) { ok = false; break; }
-          uint8_t* sA = smem + stage * PSTAGE_BYTES;
-          uint8_t* sB = sA + A_STAGE_BYTES;
-          const uint32_t full_pair = ptx::mapa_shared(&ctl->full[stage], 0);
+        // claim the next stage (bounded wait until the pair MMA released it) and set its
+        // transaction count; returns the stage's operand buffers
+        auto claim = [&](uint8_t*& sA, uint8_t*& sB, uint32_t& full_pair) {
+          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, tmo, abort_flag, trp_a)) return false;
+          sA = smem + stage * PSTAGE_BYTES;
+          sB = sA + A_STAGE_BYTES;
+          full_pair = ptx::mapa_shared(&ctl->full[stage], 0);
           if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], stage_tx);
+          filled_mask |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+          return true;
+        };
+        int kb0 = 0;   // k-blocks already claimed (B issued) before the loop below
+        if (ph == 1) {
+          // wait for every Linear-1 tile of this unit, from both CTAs (bounded)
+          const int* rp = args.ready + g;
+          const int need = PAIR * args.nL1 + ((args.flags & MOE_FLAG_TEST_STALL) ? 1 : 0);
+          if (ptx::ld_acquire_gpu(rp) < need) {
+            // W2 does not depend on Linear-1: the first stages' B halves are loaded while the
+            // unit's Linear-1 tiles finish, their A rows (h) after the wait
+            const int pre = nk < NST ? nk : NST;
+            const int st0 = stage;
+            for (; kb0 < pre; ++kb0) {
+              uint8_t *sA, *sB;
+              uint32_t full_pair;
+              if (!claim(sA, sB, full_pair)) { ok = false; break; }
+              ptx::tma_load_2d_pair(tB, full_pair, sB, c0, brow0 + kb0 * BK, pol_w);
+              ptx::tma_load_2d_pair(tB, full_pair, sB + B_BOX_BYTES, c0 + 64, brow0 + kb0 * BK, pol_w);
+            }
+            if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
+            const uint64_t t0 = ptx::globaltimer();
+            bool ready = false;
+            while (true) {
+              if (ptx::ld_acquire_gpu(rp) >= need) { ready = true; break; }
+              if (*abort_flag) break;
+              if ((int64_t)(ptx::globaltimer() - t0) > tmo) break;
+              __nanosleep(64);
+            }
+            tr_b += ptx::globaltimer() - t0;
+            if (!ready) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
+            ptx::fence_proxy_async_global();
+            if (load_a) {
+              for (int q = 0; q < kb0; ++q) {
+                const int sq = (st0 + q) % NST;
+                uint8_t* sA = smem + sq * PSTAGE_BYTES;
+                ptx::tma_load_2d_pair(tA, ptx::mapa_shared(&ctl->full[sq], 0), sA, q * BK, row0, pol_a);
+              }
+            }
+          } else {
+            ptx::fence_proxy_async_global();
+          }
+        }
+        for (int kb = kb0; kb < nk; ++kb) {
+          uint8_t *sA, *sB;
+          uint32_t full_pair;
+          if (!claim(sA, sB, full_pair)) { ok = false; break; }
           // the whole 128-row box even when some rows are padding: loading only the valid
           // rows' 32-row quadrants measured slower (fine workload 0.483 -> 0.512 ms), and so
           // did one 32-row box for a CTA with at most 32 valid rows (large 3.91 -> 4.03 ms)
           if (load_a) ptx::tma_load_2d_pair(tA, full_pair, sA, kb * BK, row0, pol_a);
           ptx::tma_load_2d_pair(tB, full_pair, sB, c0, brow0 + kb * BK, pol_w);
           ptx::tma_load_2d_pair(tB, full_pair, sB + B_BOX_BYTES, c0 + 64, brow0 + kb * BK, pol_w);
-          filled_mask |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) { set_abort(ctl, args.err, ERR_TIMEOUT); break; }
       }
