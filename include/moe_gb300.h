@@ -146,13 +146,18 @@ typedef struct {
 typedef struct moe_plan_s* moe_plan_t;
 
 /* Validate cfg, allocate the workspace for T_max on `device`, copy the bias.
- * On success *out receives a plan to pass to the calls below. */
+ * On success *out receives a plan to pass to the calls below.  Passage: the layer's shape
+ * (hidden, intermediate, experts, top-k) is the expert layer of the X-Stage paper's
+ * introduction, MegaMoE paragraph; the plan and its workspace have no counterpart there. */
 MOE_API moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out);
 
-/* Bytes of device workspace moe_plan allocates for cfg (no allocation). */
+/* Bytes of device workspace moe_plan allocates for cfg (no allocation).  Library plumbing:
+ * no counterpart in the paper. */
 MOE_API moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
 
 /* One forward of the layer for T tokens (0 <= T <= T_max; T = 0 enqueues nothing), enqueued
+ * [the operation: X-Stage paper, introduction, MegaMoE paragraph - router top-k, Dispatch,
+ * Linear-1, SwiGLU, Linear-2, Combine weighted by the router weights]
  * on `stream` (a cudaStream_t; NULL = the legacy default stream).  Never synchronises.
  *   x             bf16 [T, H]            input tokens
  *   router_logits fp32 [T, E]            OUTPUT when W_router != NULL (see MOE_FLAG_EXACT_LOGITS
@@ -166,7 +171,8 @@ MOE_API moe_status_t moe_forward(moe_plan_t plan, int32_t T, const void* x, floa
                          const void* W_router, const void* W1_gate_up, const void* W2, void* y,
                          void* stream);
 
-/* moe_forward with the token tensors in HOST memory: x_host (bf16 [T, H]) is brought into a
+/* moe_forward with the token tensors in HOST memory (the same operation as moe_forward; the
+ * host transfer has no counterpart in the paper): x_host (bf16 [T, H]) is brought into a
  * plan-owned device buffer, the layer runs, and y (bf16 [T, H]) lands in y_host, all enqueued
  * on `stream`.  A page-locked buffer that is mapped into the device's address space (any
  * cudaHostAlloc / cudaMallocHost buffer under unified addressing) at a 16-byte-aligned address
@@ -179,11 +185,14 @@ MOE_API moe_status_t moe_forward_host(moe_plan_t plan, int32_t T, const void* x_
                               const void* W_router, const void* W1_gate_up, const void* W2, void* y_host,
                               void* stream);
 
-/* Synchronise `stream`, then read and clear the plan's device error word.
+/* Synchronise `stream`, then read and clear the plan's device error word (library plumbing:
+ * no counterpart in the paper).
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */
 MOE_API moe_status_t moe_get_status(moe_plan_t plan, void* stream);
 
 /* Copy the routing of the last forward (T tokens) into caller DEVICE buffers, stream-ordered
+ * [the router's top-k and Dispatch's expert-contiguous row order: X-Stage paper, introduction,
+ * MegaMoE paragraph]
  * (any pointer may be NULL to skip it):
  *   ids int32 [T,k], w fp32 [T,k], counts int32 [E], offsets int32 [E+1],
  *   row_pair int32 [T*k] (row -> t*k+j, rows grouped by expert, ascending t within an expert),
@@ -191,16 +200,21 @@ MOE_API moe_status_t moe_get_status(moe_plan_t plan, void* stream);
 MOE_API moe_status_t moe_debug_routing(moe_plan_t plan, int32_t T, int32_t* ids, float* w, int32_t* counts,
                                int32_t* offsets, int32_t* row_pair, int32_t* row_of, void* stream);
 
-/* Copy the intermediates of the last forward into caller DEVICE buffers (NULL skips):
+/* Copy the intermediates of the last forward into caller DEVICE buffers (NULL skips)
+ * [Linear-1 + SwiGLU output and the router-weighted Linear-2 output: X-Stage paper,
+ * introduction, MegaMoE paragraph]:
  *   h   bf16 [T*k, I]   activation rows in dispatch (row) order
  *   P   fp32 [T*k, H]   router-weighted expert outputs, indexed by t*k+j */
 MOE_API moe_status_t moe_debug_intermediates(moe_plan_t plan, int32_t T, void* h, float* P, void* stream);
 
-/* Durations (ms) of the MOE_NUM_STAGES stages of the last forward; needs MOE_FLAG_STAGE_TIMING.
+/* Durations (ms) of the MOE_NUM_STAGES stages of the last forward (the steps of the X-Stage
+ * paper's MegaMoE paragraph, timed); needs MOE_FLAG_STAGE_TIMING.
  * Synchronises on the recorded events.  ms[3] is the grouped-GEMM launch(es). */
 MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
 
-/* Wait-time trace of the last forward's grouped GEMM (needs MOE_FLAG_TRACE; synchronises the
+/* Wait-time trace of the last forward's grouped GEMM (the producer / tensor-core / epilogue
+ * roles coupled through finite staging that the X-Stage paper's MegaMoE discussion describes;
+ * needs MOE_FLAG_TRACE; synchronises the
  * device).  Writes n = (CTAs + 1) x 8 uint64 values to host_buf (CTAs: the larger of the two
  * launch paths' grids; a CTA the last launch did not have reads zero; the last row holds the
  * %globaltimer stamps of a MOE_FLAG_SINGLE_LAUNCH forward - start, end of router logits, top-k,
@@ -210,18 +224,19 @@ MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
  * CTA lifetime} in nanoseconds, then {Linear-1 tiles, Linear-2 tiles}. */
 MOE_API moe_status_t moe_trace_read(moe_plan_t plan, uint64_t* host_buf, size_t cap, size_t* n);
 
-/* The coefficient cH of the default router's error bound (MOE_FLAG_EXACT_LOGITS) for a forward
+/* The coefficient cH of the default router's error bound (the router used without
+ * MOE_FLAG_EXACT_LOGITS; library numerics, no counterpart in the paper) for a forward
  * of T tokens (1 <= T <= T_max): n = the MMA steps of the longest accumulation chain, A the
  * chains per CTA, S the K splits; cH = (n + 1) 2^-17 + (A S + H/32 + 8) 2^-22.  Host only. */
 MOE_API moe_status_t moe_router_bound(moe_plan_t plan, int32_t T, float* cH);
 
-/* Number of kernels the last moe_forward launched. */
+/* Number of kernels the last moe_forward launched (library plumbing). */
 MOE_API moe_status_t moe_last_launch_count(moe_plan_t plan, int32_t* n);
 
-/* Free the plan and its workspace (synchronises the device first). */
+/* Free the plan and its workspace (synchronises the device first; library plumbing). */
 MOE_API moe_status_t moe_plan_destroy(moe_plan_t plan);
 
-/* Static description of a status code. */
+/* Static description of a status code (library plumbing). */
 MOE_API const char* moe_status_string(moe_status_t s);
 
 /* Dispatch (the stable counting sort of moe_forward's Dispatch step) for callers that cannot
@@ -252,14 +267,17 @@ MOE_API moe_status_t moe_dispatch_static(int32_t T, int32_t E, int32_t k, const 
                                  int32_t* offsets, int32_t* row_pair, int32_t* row_of, float* row_w,
                                  void* stream);
 
-/* The tile list the last forward's Dispatch built on the device (synchronises `stream`):
+/* The tile list the last forward's Dispatch built on the device [the expert-wave schedule and
+ * the cross-wave interleave: X-Stage paper, introduction (expert waves) and its X-Stage-aware
+ * design section] (synchronises `stream`):
  * n_out[3] = {linear-1 tiles, total tiles, tile workers (2-CTA clusters) it was built for};
  * up to cap tiles are copied to HOST memory tiles_out (4 ints each, as moe_schedule_host), which
  * may be NULL to query the counts.  MOE_ERR_INVALID_ARG if cap is smaller than the total. */
 MOE_API moe_status_t moe_debug_schedule(moe_plan_t plan, int32_t* tiles_out, int64_t cap, int64_t* n_out,
                                 void* stream);
 
-/* Host-side evaluation of the tile schedule the device builds (for tests; no GPU needed).
+/* Host-side evaluation of the tile schedule the device builds (the same passages as
+ * moe_debug_schedule; for tests; no GPU needed).
  * counts[E] rows per expert; num_sms = number of tile workers (2-CTA clusters on the GPU);
  * a unit is a pair of 128-row m-tiles of one expert.  Writes up to cap tiles as 4 ints each
  * {phase | n_block << 1, expert, unit within the expert, global unit index} into tiles_out and
