@@ -89,18 +89,18 @@ __device__ bool grid_barrier(unsigned int* ctr, unsigned int n, bool wait, int64
   return *s_ok != 0;
 }
 
-// Top-k of token t by one warp: the selection and weights of routing.cuh, counts by atomics.
-__device__ __forceinline__ void topk_token(const FusedArgs& a, int t, int lane) {
+// Top-k of token t by one warp from its logits row l (global memory, or the CTA's shared copy):
+// the selection and weights of routing.cuh, counts by atomics.
+__device__ __forceinline__ void topk_token(const FusedArgs& a, int t, const float* l, int lane) {
   const int nkey = (a.E + 31) >> 5;
-  const float* l = a.logits + (size_t)t * a.E;
   uint64_t key[MAX_E / 32];
 #pragma unroll
   for (int i = 0; i < MAX_E / 32; ++i) {
     const int e = lane + 32 * i;
-    key[i] = (i < nkey && e < a.E) ? select_key(__ldcg(l + e), e) : 0ull;
+    key[i] = (i < nkey && e < a.E) ? select_key(l[e], e) : 0ull;
   }
   const int my_e = warp_select_topk(key, a.k, lane);
-  const float my_l = (lane < a.k) ? __ldcg(l + my_e) : 0.0f;
+  const float my_l = (lane < a.k) ? l[my_e] : 0.0f;
   const float wt = warp_softmax_weight(my_l, a.k, lane);
   if (lane < a.k) {
     a.ws.ids[(size_t)t * a.k + lane] = my_e;
@@ -112,7 +112,7 @@ __device__ __forceinline__ void topk_token(const FusedArgs& a, int t, int lane) 
 
 // Phase B, one warp per token.
 __device__ void topk_phase(const FusedArgs& a, int gw, int nw, int lane) {
-  for (int t = gw; t < a.T; t += nw) topk_token(a, t, lane);
+  for (int t = gw; t < a.T; t += nw) topk_token(a, t, a.logits + (size_t)t * a.E, lane);
 }
 
 // Phase A: a CTA task is FR_TOK tokens x FR_EXP experts.  x and W_router stream through a
@@ -126,7 +126,7 @@ constexpr int FR_STAGE_X = FR_TOK * FR_XROW;         // elements
 constexpr int FR_STAGE_W = FR_HC * FR_EXP;           // elements: [h][8 experts]
 constexpr int FR_STAGE = FR_STAGE_X + FR_STAGE_W;
 constexpr int FR_CWARPS = FR_TOK / 4;                // compute warps
-static_assert(FR_NS * FR_STAGE * 2 + 1024 <= FZ_BAR_OFF, "router ring overlaps the barrier word");
+static_assert(FR_NS * FR_STAGE * 2 + FR_TOK * FR_EXP * 4 + 1024 <= FZ_BAR_OFF, "router ring overlaps the barrier word");
 static_assert(FR_CWARPS <= FZ_WARPS, "router tile needs more warps than the CTA has");
 
 __device__ __forceinline__ void fr_cp16(uint16_t* dst, const uint16_t* src, bool valid) {
@@ -137,6 +137,7 @@ __device__ __forceinline__ void fr_cp16(uint16_t* dst, const uint16_t* src, bool
 // with_topk (one expert group, E <= FR_EXP): the CTA that wrote a task's logits - every expert
 // of its 32 tokens - selects those tokens' experts right away (a CTA barrier orders the writes).
 __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int warp, bool with_topk) {
+  float* lg = reinterpret_cast<float*>(rs + FR_NS * FR_STAGE);   // [FR_TOK][FR_EXP] logits (with_topk)
   const int nT = (a.T + FR_TOK - 1) / FR_TOK, nE = (a.E + FR_EXP - 1) / FR_EXP;
   const bool wvec = (a.E % FR_EXP) == 0;     // 16-byte rows of W_router (else element copies)
   const int nchunk = a.H / FR_HC;            // H is a multiple of 256
@@ -213,11 +214,17 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
           if (lane == ti * FR_EXP + b) mine = v;
         }
       const int t = t0 + warp * 4 + lane / FR_EXP, e = e0 + lane % FR_EXP;
-      if (t < a.T && e < a.E) a.logits[(size_t)t * a.E + e] = a.bias ? __fadd_rn(mine, a.bias[e]) : mine;
+      const float v = a.bias ? __fadd_rn(mine, a.bias[e < a.E ? e : 0]) : mine;
+      if (t < a.T && e < a.E) {
+        a.logits[(size_t)t * a.E + e] = v;
+        if (with_topk) lg[(t - t0) * FR_EXP + e] = v;   // the CTA's copy for the top-k below
+      }
     }
     __syncthreads();                           // the ring is reused by the next task
-    if (with_topk)
-      for (int tt = warp; tt < FR_TOK && t0 + tt < a.T; tt += FZ_WARPS) topk_token(a, t0 + tt, lane);
+    if (with_topk) {
+      for (int tt = warp; tt < FR_TOK && t0 + tt < a.T; tt += FZ_WARPS) topk_token(a, t0 + tt, lg + tt * FR_EXP, lane);
+      __syncthreads();                         // lg is rewritten by the next task
+    }
   }
 }
 
