@@ -703,3 +703,30 @@ def test_single_launch_reports_timeout_and_bad_id():
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
     check_y(bits(y), ref)
     good.close()
+
+
+def test_single_launch_phase_stamps_and_trace_layout():
+    """MOE_FLAG_TRACE: the trace has one row per CTA of the larger grid plus one row of phase
+    stamps; after a single-launch forward the stamps are non-decreasing and span less than the
+    forward's event time, after a multi-launch forward the stamp row is zero."""
+    wl = synth.WORKLOADS["tiny"]
+    d = synth.device_inputs(wl)
+    for flags, single in [(SINGLE | moe.MOE_FLAG_TRACE, True), (moe.MOE_FLAG_TRACE, False)]:
+        layer = _layer(wl, flags=flags)
+        for _ in range(2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+            b.record()
+            b.synchronize()
+        tr = moe.moe_trace_read(layer.plan)
+        assert tr.shape[1] == 8 and tr.shape[0] >= 2
+        stamps = tr[-1].astype(np.int64)
+        if single:
+            assert np.all(stamps[:7] > 0) and np.all(np.diff(stamps[:7]) >= 0), stamps
+            assert (stamps[6] - stamps[0]) / 1e6 < a.elapsed_time(b)       # ns vs ms
+            assert tr[:-1, 5].max() > 0                                      # the GEMM phase's CTA lifetimes
+        else:
+            assert np.all(stamps == 0)
+            assert tr[:-1, 5].max() > 0
+        layer.close()
