@@ -17,13 +17,14 @@ namespace moe {
 namespace {
 
 // One thread per 8 consecutive outputs (combine_item), grid-stride.
+template <bool ALL_IN_FLIGHT>
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint16_t* __restrict__ P_pad, const float* __restrict__ S_pad, const int32_t* __restrict__ prow_of,
                int T, int H, int k, uint16_t* __restrict__ y) {
   ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
   const int64_t n8 = (int64_t)T * H / 8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x)
-    combine_item(P_pad, S_pad, prow_of, H, k, y, i);
+    combine_item<ALL_IN_FLIGHT>(P_pad, S_pad, prow_of, H, k, y, i);
 }
 
 }  // namespace
@@ -35,7 +36,11 @@ cudaError_t launch_combine(const uint16_t* P_pad, const float* S_pad, const int3
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, st, P_pad, S_pad, prow_of, T, H, k, y);
+  // a batch that one resident wave of threads covers (4 blocks of 256 per SM) is latency-bound:
+  // all slots in flight; larger batches are bandwidth-bound: one slot at a time
+  if (n8 <= (int64_t)sms * 4 * 256)
+    return launch_pdl(combine_kernel<true>, dim3((unsigned)blocks), dim3(256), 0, st, P_pad, S_pad, prow_of, T, H, k, y);
+  return launch_pdl(combine_kernel<false>, dim3((unsigned)blocks), dim3(256), 0, st, P_pad, S_pad, prow_of, T, H, k, y);
 }
 
 }  // namespace moe

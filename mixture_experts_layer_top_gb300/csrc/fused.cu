@@ -291,7 +291,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
   if (ok) {                                                             // F
     const int64_t n8 = (int64_t)a.T * a.H / 8;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x)
-      combine_item(a.ws.P_pad, a.ws.S_pad, a.ws.prow_of, a.H, a.k, a.y, i);
+      combine_item<true>(a.ws.P_pad, a.ws.S_pad, a.ws.prow_of, a.H, a.k, a.y, i);   // small batches: latency-bound
   }
   if (a.ga.trace) {   // the end of Combine: the last CTA to finish writes the stamp
     __syncthreads();

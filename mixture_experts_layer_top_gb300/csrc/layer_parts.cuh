@@ -351,45 +351,57 @@ __device__ __forceinline__ void gather_task(const uint16_t* x, const int32_t* pr
   }
 }
 
-// Combine item i (one thread, 8 consecutive outputs of a token): the k slots' padded rows
-// first, then k 16-byte loads of fp16 P from them (all in flight at once) and their blocks'
-// power-of-two scales, each widened and rescaled exactly, summed in fp32 in slot order
-// j = 0..k-1; one 16-byte store.
+// Combine item i (one thread, 8 consecutive outputs of a token): k 16-byte loads of fp16 P
+// from the slots' padded rows (found through prow_of) and their blocks' power-of-two scales,
+// each widened and rescaled exactly, summed in fp32 in slot order j = 0..k-1; one 16-byte
+// store.  ALL_IN_FLIGHT: the k row indices first, then all k loads at once (for small batches,
+// where a resident wave of threads covers the whole output and latency decides: 128-token
+// workload 12.3 -> 10.2 us); otherwise one slot after another in 32 registers, so that more
+// warps stay resident (large batches are bandwidth-bound: large layer 88 vs 98 us, fine 52 vs
+// 55 us with all slots in flight).  Both give the same bits.
+template <bool ALL_IN_FLIGHT>
 __device__ __forceinline__ void combine_item(const uint16_t* P_pad, const float* S_pad, const int32_t* prow_of, int H,
                                              int k, uint16_t* y, int64_t i) {
   const int nS = H / P_SCALE_COLS;
   const int64_t t = (i * 8) / H;
   const int64_t c = (i * 8) % H;
   const int32_t* pr = prow_of + t * k;
-  int64_t row[MAX_K];
-#pragma unroll
-  for (int j = 0; j < MAX_K; ++j) row[j] = (j < k) ? (int64_t)pr[j] : 0;
-  uint4 v[MAX_K];
-  float sc[MAX_K];
-#pragma unroll
-  for (int j = 0; j < MAX_K; ++j) {
-    if (j < k) {
-      v[j] = __ldcs(reinterpret_cast<const uint4*>(P_pad + row[j] * H + c));
-      sc[j] = S_pad[row[j] * nS + c / P_SCALE_COLS];
-    }
-  }
   float s[8];
+  auto add = [&](int j, const uint4& v, float sc) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int j = 0; j < MAX_K; ++j) {
-    if (j < k) {
-      const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
-        const float a = f.x * sc[j], b = f.y * sc[j];
-        if (j == 0) {
-          s[2 * q] = a;
-          s[2 * q + 1] = b;
-        } else {
-          s[2 * q] = s[2 * q] + a;
-          s[2 * q + 1] = s[2 * q + 1] + b;
-        }
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[q]));
+      const float a = f.x * sc, b = f.y * sc;
+      if (j == 0) {
+        s[2 * q] = a;
+        s[2 * q + 1] = b;
+      } else {
+        s[2 * q] = s[2 * q] + a;
+        s[2 * q + 1] = s[2 * q + 1] + b;
       }
+    }
+  };
+  if (ALL_IN_FLIGHT) {
+    int64_t row[MAX_K];
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j) row[j] = (j < k) ? (int64_t)pr[j] : 0;
+    uint4 v[MAX_K];
+    float sc[MAX_K];
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j) {
+      if (j < k) {
+        v[j] = __ldcs(reinterpret_cast<const uint4*>(P_pad + row[j] * H + c));
+        sc[j] = S_pad[row[j] * nS + c / P_SCALE_COLS];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAX_K; ++j)
+      if (j < k) add(j, v[j], sc[j]);
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = pr[j];
+      add(j, __ldcs(reinterpret_cast<const uint4*>(P_pad + row * H + c)), S_pad[row * nS + c / P_SCALE_COLS]);
     }
   }
   uint32_t o[4];
