@@ -298,8 +298,9 @@ def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
 
 def _random_cases(n: int, seed: int = 20261202):
     """Seeded layer shapes within the library's limits: H a multiple of 256, I of 128, E up
-    to 64, k up to min(8, E), T up to 300 with a larger T_max, any schedule, the default or
-    all-canonical router or the compute ring split, a Zipf router bias on some."""
+    to 256, k up to min(8, E), T up to 300 with a larger T_max, any schedule, the default or
+    all-canonical router, the compute ring split or the single launch, a Zipf router bias on
+    some."""
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(n):
@@ -307,7 +308,7 @@ def _random_cases(n: int, seed: int = 20261202):
         out.append(dict(T=int(rng.integers(1, 301)), H=int(rng.choice([256, 512, 768, 1024, 2048])),
                         I=int(rng.choice([128, 256, 384, 512])), E=E, k=int(rng.integers(1, min(8, E) + 1)),
                         sched=int(rng.integers(0, 4)), extra=int(rng.integers(0, 200)),
-                        flags=[0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE][int(rng.integers(0, 3))],
+                        flags=[0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE, moe.MOE_FLAG_SINGLE_LAUNCH][int(rng.integers(0, 4))],
                         zipf=float(rng.choice([0.0, 1.2])), host=bool(rng.integers(0, 3) == 0)))
     return out
 
@@ -331,7 +332,7 @@ def test_random_shapes_full_oracle(c):
         layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y, check=True)
     else:
         y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
-    if c["flags"] & EXACT:
+    if c["flags"] & (EXACT | moe.MOE_FLAG_SINGLE_LAUNCH):     # the single launch's logits are all canonical
         assert np.array_equal(logits.cpu().numpy(), ref["logits"])
     else:
         check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(c["T"]), bias)
