@@ -332,8 +332,13 @@ __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, 
 // 8 pairs per warp at a time; (3) each warp ranks its token's candidates on the
 // exact values (one pass over them when there are at most 32, k rounds of warp
 // arg-max over all experts otherwise).  E <= 32 NK.
+// Resident blocks per SM: the kernel is latency-bound (memory waits on the canonical
+// re-evaluation's loads), so occupancy helps where the registers allow it: 4 blocks (64
+// registers) for E <= 128 measured faster than 3 (80 registers) - fine workload 68 -> 64 us -
+// while for E = 256 the 64-register build spills in the hot loop and 3 blocks stay faster
+// (large layer 121-128 vs 136-144 us).
 template <int NK>
-__global__ void __launch_bounds__(SEL_WARPS * 32, 3)
+__global__ void __launch_bounds__(SEL_WARPS * 32, (NK <= 4) ? 4 : 3)
 router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ WrT, const float* __restrict__ part,
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
                      float cH, int ntok, float* __restrict__ logits, int32_t* __restrict__ ids,
