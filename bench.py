@@ -305,16 +305,19 @@ def run_reference(args, wl):
     return 0
 
 
-def config_of(wl, args):
+def config_of(wl, args, single=None):
     """The workload, the schedule options and the L2 policy of the GPU arm's timed steps: the
-    same dict for both arms (the reference arm runs on the host and says so in "note")."""
+    same dict for both arms (the reference arm runs on the host and says so in "note").  single:
+    the launch form of this entry (default: the --single-launch option)."""
+    if single is None:
+        single = getattr(args, "single_launch", False)
     sched = {0: "wave-serial", 1: "interleaved", 2: "phased (L1 launch, L2 launch)",
              3: "auto (wave-serial, one wave of all experts)"}[args.schedule]
     split = "streaming" if args.gemm_split == "auto" else args.gemm_split
     return {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
             "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
             "wave_experts": args.wave_experts, "lead_waves": args.lead_waves,
-            "launch": "single (MOE_FLAG_SINGLE_LAUNCH)" if getattr(args, "single_launch", False) else "multi",
+            "launch": "single (MOE_FLAG_SINGLE_LAUNCH)" if single else "multi",
             "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
             "parallelism": f"replicas x{args.gpus} (no sharding)"}
 
@@ -335,6 +338,7 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
     flags = {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING, "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
     flags |= extra_flags
+    single = bool(flags & moe.MOE_FLAG_SINGLE_LAUNCH)
     cfg = dict(schedule=args.schedule, wave_experts=args.wave_experts, lead_waves=args.lead_waves)
     layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags, **cfg), local, router_bias=bias)
     logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device=dev)
@@ -414,9 +418,13 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     t_hbm = layer_bytes / (peaks["hbm_gbs"] * 1e9)
     t_step = ms_per_step * 1e-3
     stage_avg = {k: statistics.mean(s[k] for s in stages) for k in stages[0]}
-
-    # dominant kernel: the persistent grouped GEMM (Linear-1 + SwiGLU, Linear-2 + scale)
-    g_ms = stage_avg["grouped_gemm"]
+    if single:
+        # one kernel: the library's stage events bracket the counts memset and the whole layer
+        stage_avg = {"memset_counts": stage_avg["router_topk"], "fused_layer": stage_avg["grouped_gemm"]}
+        kernel, g_ms = "fused_layer_kernel", stage_avg["fused_layer"]
+    else:
+        # dominant kernel: the persistent grouped GEMM (Linear-1 + SwiGLU, Linear-2 + scale)
+        kernel, g_ms = "grouped_gemm_kernel", stage_avg["grouped_gemm"]
     g_flops = 6.0 * wl.H * wl.I * R
     g_bytes = w_bytes                               # compulsory: each touched expert's weights once
     tensor_bound = g_flops / (peaks["bf16_tflops"] * 1e12) >= g_bytes / (peaks["hbm_gbs"] * 1e9)
@@ -428,11 +436,11 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
         ach = g_bytes / (g_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
-    traffic, traffic_note = load_traffic("grouped_gemm_kernel", wl.name, args.schedule)
+    traffic, traffic_note = load_traffic(kernel, wl.name, args.schedule)
     roof.update({"traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read+write)",
                  "traffic_note": traffic_note,
-                 "kernel": "grouped_gemm_kernel", "ms_per_launch": g_ms,
-                 "launches_per_step": 2 if args.schedule == 2 else 1,
+                 "kernel": kernel, "ms_per_launch": g_ms,
+                 "launches_per_step": 2 if (args.schedule == 2 and not single) else 1,
                  "peak_source": f"{peak_src} ({'bf16_tflops burst' if tensor_bound else 'hbm_gbs'})",
                  "algorithmic": (f"{g_flops:.4g} FLOP (6*H*I per routed row x {R} rows)" if tensor_bound
                                  else f"{g_bytes:.4g} B (6*H*I bytes per touched expert x {touched})")})
@@ -440,7 +448,7 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     return {
         "value": ws * flops / t_step / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_per_step,
         "tokens_per_s": ws * wl.T / t_step,
-        "config": config_of(wl, args),
+        "config": config_of(wl, args, single),
         "layer_roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "frac": max(t_tc, t_hbm) / t_step,
                            "frac_of_nominal": max(flops / (nominal_tc * 1e12),
                                                   layer_bytes / (nominal_hbm * 1e9)) / t_step,
@@ -491,18 +499,22 @@ def run_ours(args, wl):
     main_flags = moe.MOE_FLAG_SINGLE_LAUNCH if args.single_launch else 0
     main = measure(wl, _shared_inputs(wl, have, dev), args, dev, local, peaks, peak_src, group, ws, sampler,
                    with_e2e=not args.no_e2e, extra_flags=main_flags)
+    # the other workloads, those sharing the resident weights' shape first, so that each weight
+    # set is drawn once (22.5 GB for the large shape)
+    jobs = [(n, False) for n in args.also.split(",") if n and n != "none" and n != wl.name]
+    jobs += [(n, True) for n in args.also_single.split(",") if n and n != "none"]
+    shape = lambda n: (synth.WORKLOADS[n].H, synth.WORKLOADS[n].I, synth.WORKLOADS[n].E)   # noqa: E731
+    jobs.sort(key=lambda j: (shape(j[0]) != (wl.H, wl.I, wl.E), shape(j[0])))
     extra = {}
-    for name in [n for n in args.also.split(",") if n and n != "none" and n != wl.name]:
+    for name, single in jobs:
         w2 = synth.WORKLOADS[name]
-        extra[name] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
-                              sampler, with_e2e=not args.no_e2e, extra_flags=main_flags)
-        extra[name].pop("gpu_launches", None)
-    for name in [n for n in args.also_single.split(",") if n and n != "none"]:
-        w2 = synth.WORKLOADS[name]
-        key = f"{name} (single launch)"
-        extra[key] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws,
-                             sampler, with_e2e=False, extra_flags=moe.MOE_FLAG_SINGLE_LAUNCH)
-        extra[key]["launches_per_step"] = extra[key].pop("gpu_launches") // args.steps
+        key = f"{name} (single launch)" if single else name
+        extra[key] = measure(w2, _shared_inputs(w2, have, dev), args, dev, local, peaks, peak_src, group, ws, sampler,
+                             with_e2e=(not args.no_e2e) and not single,
+                             extra_flags=moe.MOE_FLAG_SINGLE_LAUNCH if single else main_flags)
+        launches = extra[key].pop("gpu_launches")
+        if single:
+            extra[key]["launches_per_step"] = launches // args.steps
     have.clear()
     torch.cuda.empty_cache()
     if sampler:
