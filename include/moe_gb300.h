@@ -130,8 +130,8 @@ typedef enum {
 
 typedef struct {
   int32_t T_max;        /* largest token count a forward may use (>= 1)                         */
-  int32_t H;            /* hidden size: multiple of 256                                         */
-  int32_t I;            /* intermediate size per expert: multiple of 128                        */
+  int32_t H;            /* hidden size: multiple of 64 (else MOE_ERR_UNSUPPORTED)               */
+  int32_t I;            /* intermediate size per expert: multiple of 64 (else UNSUPPORTED)      */
   int32_t E;            /* experts: 1 <= E <= 256                                               */
   int32_t top_k;        /* 1 <= top_k <= min(E, 8)                                              */
   int32_t schedule;     /* MOE_SCHED_*                                                          */
@@ -281,7 +281,9 @@ MOE_API moe_status_t moe_debug_schedule(moe_plan_t plan, int32_t* tiles_out, int
  * counts[E] rows per expert; num_sms = number of tile workers (2-CTA clusters on the GPU);
  * a unit is a pair of 128-row m-tiles of one expert.  Writes up to cap tiles as 4 ints each
  * {phase | n_block << 1, expert, unit within the expert, global unit index} into tiles_out and
- * the tile counts {linear-1 tiles, total tiles} into n_out[2]. */
+ * the tile counts {linear-1 tiles, total tiles} into n_out[2].  A unit has ceil(I / 128)
+ * Linear-1 tiles and ceil(H / 256) Linear-2 tiles (the last of each may be partial); H and I
+ * must be positive multiples of 64, else MOE_ERR_INVALID_ARG. */
 MOE_API moe_status_t moe_schedule_host(const int32_t* counts, int32_t E, int32_t H, int32_t I,
                                int32_t num_sms, int32_t schedule, int32_t wave_experts,
                                int32_t lead_waves, int32_t* tiles_out, int64_t cap, int64_t* n_out);

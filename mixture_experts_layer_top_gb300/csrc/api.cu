@@ -114,7 +114,8 @@ moe_status_t validate_cfg(const moe_config_t* c) {
       c->timeout_ns < 0)
     return MOE_ERR_INVALID_ARG;
   if ((c->flags & MOE_FLAG_GEMM_STREAMING) && (c->flags & MOE_FLAG_GEMM_COMPUTE)) return MOE_ERR_INVALID_ARG;
-  if (c->H % L2_COLS != 0 || c->I % L1_COLS != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->H % SHAPE_ALIGN != 0 || c->I % SHAPE_ALIGN != 0) return MOE_ERR_UNSUPPORTED;
+  if (l1_blocks(c->I) >= (1 << 15) || l2_blocks(c->H) >= (1 << 15)) return MOE_ERR_UNSUPPORTED;   // tile field
   if (c->E > MAX_E || c->top_k > MAX_K || c->top_k > c->E) return MOE_ERR_UNSUPPORTED;
   const int64_t R = (int64_t)c->T_max * c->top_k;
   if (R >= (1ll << 30) || (int64_t)c->E * c->H >= (1ll << 31) || (int64_t)c->E * c->I >= (1ll << 31) ||
@@ -150,7 +151,7 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
   sizes[B_X_PAD] = (size_t)Rp * c.H * 2;
   sizes[B_H_PAD] = (size_t)Rp * c.I * 2;
   sizes[B_P_PAD] = (size_t)Rp * c.H * 2;                 // fp16
-  sizes[B_S_PAD] = (size_t)Rp * (c.H / P_SCALE_COLS) * 4;   // per-(row, 128 columns) scale of P_pad
+  sizes[B_S_PAD] = (size_t)Rp * p_scale_blocks(c.H) * 4;   // per-(row, 128 columns) scale of P_pad
   sizes[B_TILES] = (size_t)max_tiles * 16;
   sizes[B_SCHED] = 16;
   sizes[B_READY] = (size_t)max_mt * 4;
@@ -213,8 +214,8 @@ GemmArgs gemm_args(const moe_plan_s* p) {
   ga.I = c.I;
   ga.E = c.E;
   ga.R_pad = (int)p->R_pad_max;
-  ga.nL1 = c.I / L1_COLS;
-  ga.nL2 = c.H / L2_COLS;
+  ga.nL1 = l1_blocks(c.I);
+  ga.nL2 = l2_blocks(c.H);
   ga.flags = c.flags;
   ga.timeout_ns = c.timeout_ns;
   return ga;
@@ -398,7 +399,7 @@ moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes) {
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const int64_t R = (int64_t)cfg->T_max * cfg->top_k;
   const int64_t max_mt = max_mtiles(R, cfg->E);
-  const int64_t max_tiles = max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  const int64_t max_tiles = max_mt * (l1_blocks(cfg->I) + l2_blocks(cfg->H));
   *bytes = layout_of(*cfg, R, max_mt, max_tiles).total;
   return MOE_OK;
 }
@@ -422,7 +423,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device);
   p->R_max = (int64_t)cfg->T_max * cfg->top_k;
   p->max_mt = max_mtiles(p->R_max, cfg->E);
-  p->max_tiles = p->max_mt * (cfg->I / L1_COLS + cfg->H / L2_COLS);
+  p->max_tiles = p->max_mt * (l1_blocks(cfg->I) + l2_blocks(cfg->H));
   p->R_pad_max = p->max_mt * UNIT_ROWS;
   Layout L = layout_of(*cfg, p->R_max, p->max_mt, p->max_tiles);
   p->bytes = L.total;
@@ -464,7 +465,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->rw.part = reinterpret_cast<float*>(at(B_PART));
   if (cudaMemset(p->ws.err, 0, 16) != cudaSuccess) return fail(MOE_ERR_CUDA);
   {   // the dead row: P and its scales zero, so a pair sent there adds nothing in Combine
-    const size_t dead = (size_t)p->R_pad_max, nS = (size_t)(cfg->H / P_SCALE_COLS);
+    const size_t dead = (size_t)p->R_pad_max, nS = (size_t)p_scale_blocks(cfg->H);
     if (cudaMemset(p->ws.P_pad + dead * cfg->H, 0, (size_t)cfg->H * 2) != cudaSuccess ||
         cudaMemset(p->ws.S_pad + dead * nS, 0, nS * 4) != cudaSuccess)
       return fail(MOE_ERR_CUDA);
@@ -641,12 +642,12 @@ moe_status_t moe_debug_schedule(moe_plan_t p, int32_t* tiles_out, int64_t cap, i
 moe_status_t moe_schedule_host(const int32_t* counts, int32_t E, int32_t H, int32_t I, int32_t num_sms,
                                int32_t schedule, int32_t wave_experts, int32_t lead_waves, int32_t* tiles_out,
                                int64_t cap, int64_t* n_out) {
-  if (!counts || !n_out || E < 1 || E > MAX_E || H % L2_COLS || I % L1_COLS || num_sms < 1 || schedule < 0 ||
+  if (!counts || !n_out || E < 1 || E > MAX_E || H < 1 || I < 1 || H % SHAPE_ALIGN || I % SHAPE_ALIGN || num_sms < 1 || schedule < 0 ||
       schedule > 2)
     return MOE_ERR_INVALID_ARG;
   SchedTables* s = new (std::nothrow) SchedTables();
   if (!s) return MOE_ERR_OOM;
-  sched_build(*s, counts, E, I / L1_COLS, H / L2_COLS, num_sms, schedule, wave_experts,
+  sched_build(*s, counts, E, l1_blocks(I), l2_blocks(H), num_sms, schedule, wave_experts,
               lead_waves == 0 ? 1 : lead_waves);
   n_out[0] = s->n1_total;
   n_out[1] = s->total;

@@ -27,6 +27,15 @@ constexpr int UNIT_ROWS = BM * PAIR;
 constexpr int MAX_E = 256;
 constexpr int MAX_K = 8;
 
+// Shapes: H and I are multiples of 64 (one 64-column TMA box).  The last Linear-1 tile of an
+// expert may hold 64 intermediate columns instead of 128, the last Linear-2 tile 64, 128 or 192
+// output columns instead of 256, and the last P scale block 64 columns: the operand loads of
+// the missing columns read zeros (or columns that are never stored) and their stores are skipped.
+constexpr int SHAPE_ALIGN = 64;
+MOE_HD int l1_blocks(int I) { return (I + L1_COLS - 1) / L1_COLS; }        // Linear-1 tiles per unit
+MOE_HD int l2_blocks(int H) { return (H + L2_COLS - 1) / L2_COLS; }        // Linear-2 tiles per unit
+MOE_HD int p_scale_blocks(int H) { return (H + P_SCALE_COLS - 1) / P_SCALE_COLS; }   // scales per P row
+
 constexpr int A_STAGE_BYTES = BM * BK * 2;                 // 16 KB
 constexpr int B_STAGE_BYTES = MMA_N * BK * 2;              // 32 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;                   // one 64-column box, 8 KB

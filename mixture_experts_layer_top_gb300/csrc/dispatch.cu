@@ -67,7 +67,7 @@ compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t
       reinterpret_cast<uint4*>(h + (size_t)row * I)[i] = reinterpret_cast<const uint4*>(h_pad + pr * I)[i];
   if (P)
     for (int c = lane; c < H; c += 32)
-      P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * (H / P_SCALE_COLS) + c / P_SCALE_COLS];
+      P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * p_scale_blocks(H) + c / P_SCALE_COLS];
 }
 
 // Token block from page-locked host memory (mapped into this device's address space)
@@ -107,7 +107,7 @@ cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int
                             int wave_experts, int lead, int dead_row, bool test_bad_id, cudaStream_t st) {
   const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
   return launch_pdl(dispatch_kernel, dim3(DS_SCHED_CTAS + chunks), dim3(DS_THREADS), 0, st, ws.ids, ws.w, ws.counts,
-                    ws.chist, T, E, k, I / L1_COLS, H / L2_COLS, num_sms, mode, wave_experts, lead, ws.offsets,
+                    ws.chist, T, E, k, l1_blocks(I), l2_blocks(H), num_sms, mode, wave_experts, lead, ws.offsets,
                     ws.row_pair, ws.row_of, ws.prow_of, ws.prow_w, ws.tiles, ws.sched, ws.ready, ws.err, dead_row,
                     test_bad_id ? 1 : 0);
 }

@@ -140,7 +140,9 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
   float* lg = reinterpret_cast<float*>(rs + FR_NS * FR_STAGE);   // [FR_TOK][FR_EXP] logits (with_topk)
   const int nT = (a.T + FR_TOK - 1) / FR_TOK, nE = (a.E + FR_EXP - 1) / FR_EXP;
   const bool wvec = (a.E % FR_EXP) == 0;     // 16-byte rows of W_router (else element copies)
-  const int nchunk = a.H / FR_HC;            // H is a multiple of 256
+  // the last chunk of an H that is not a multiple of FR_HC holds zeros past H (a fused
+  // multiply-add of 0 * 0 leaves a partial sum unchanged: the canonical value is the same)
+  const int nchunk = (a.H + FR_HC - 1) / FR_HC;
   for (int task = blockIdx.x; task < nT * nE; task += gridDim.x) {
     const int t0 = (task / nE) * FR_TOK, e0 = (task % nE) * FR_EXP;
     auto issue = [&](int c) {
@@ -149,16 +151,17 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
       const int h0 = c * FR_HC;
       for (int q = threadIdx.x; q < FR_TOK * (FR_HC / 8); q += GEMM_THREADS) {   // x: 16-byte pieces
         const int tok = q / (FR_HC / 8), pc = q % (FR_HC / 8);
-        const bool ok = t0 + tok < a.T;
-        fr_cp16(xs + tok * FR_XROW + pc * 8, a.x + (size_t)(ok ? t0 + tok : 0) * a.H + h0 + pc * 8, ok);
+        const bool ok = t0 + tok < a.T && h0 + pc * 8 < a.H;
+        fr_cp16(xs + tok * FR_XROW + pc * 8, ok ? a.x + (size_t)(t0 + tok) * a.H + h0 + pc * 8 : a.x, ok);
       }
       for (int r = threadIdx.x; r < FR_HC; r += GEMM_THREADS) {                   // W_router rows h0 + r
-        const uint16_t* src = a.Wr + (size_t)(h0 + r) * a.E + e0;
+        const bool h_ok = h0 + r < a.H;
+        const uint16_t* src = a.Wr + (size_t)(h_ok ? h0 + r : 0) * a.E + e0;
         if (wvec) {
-          fr_cp16(ws + r * FR_EXP, src, true);
+          fr_cp16(ws + r * FR_EXP, src, h_ok);
         } else {
 #pragma unroll
-          for (int b = 0; b < FR_EXP; ++b) ws[r * FR_EXP + b] = (e0 + b < a.E) ? src[b] : (uint16_t)0;
+          for (int b = 0; b < FR_EXP; ++b) ws[r * FR_EXP + b] = (e0 + b < a.E && h_ok) ? src[b] : (uint16_t)0;
         }
       }
     };

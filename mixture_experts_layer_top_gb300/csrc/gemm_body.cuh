@@ -317,7 +317,9 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * MMA_N);
       const uint32_t tempty_addr = as ? tempty_pair1 : tempty_pair0;
       if (ph == 0) {
-        // h = silu(gate) * up for columns [64 ch, 64 ch + 64) of the tile
+        // h = silu(gate) * up for columns [64 ch, 64 ch + 64) of the tile; the last tile of an
+        // expert with I = 64 (mod 128) has no second half (its values are computed, not stored)
+        const bool col_ok = nb * L1_COLS + ch * 64 < args.I;
         acquire_stage();
         uint8_t* box = stg + (sb % NBUF) * STG_BYTES + ch * STG_BOX_BYTES;
         uint16_t* hrow = args.h_pad + (size_t)(prow0 + r) * args.I + nb * L1_COLS + ch * 64;
@@ -340,7 +342,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
           for (int j = 0; j < 4; ++j) {
             const uint4 v4 = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
             if (staged) *reinterpret_cast<uint4*>(box + chunk_off(4 * c + j)) = v4;
-            else if (direct) reinterpret_cast<uint4*>(hrow)[4 * c + j] = v4;
+            else if (direct && col_ok) reinterpret_cast<uint4*>(hrow)[4 * c + j] = v4;
           }
         }
         ptx::tc_fence_before();
@@ -350,10 +352,12 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
         if (ep_tid == 0) {
           ptx::mbar_arrive_cluster(tempty_addr);     // accumulator free for the next tile
           uint8_t* buf = stg + (sb % NBUF) * STG_BYTES;
+          const bool half2 = nb * L1_COLS + 64 < args.I;
           for (int gq = 0; gq < nfull; ++gq) {
             ptx::tma_store_2d(tmH, buf + gq * ST_BOX_BYTES, nb * L1_COLS, prow0 + gq * ST_ROWS);
-            ptx::tma_store_2d(tmH, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L1_COLS + 64,
-                              prow0 + gq * ST_ROWS);
+            if (half2)
+              ptx::tma_store_2d(tmH, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L1_COLS + 64,
+                                prow0 + gq * ST_ROWS);
           }
           ptx::bulk_commit();
           ptx::bulk_wait<0>();                       // h rows written: publish them to Linear-2
@@ -392,8 +396,12 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
           se = max(-126, min(127, cl2 - 15));
         }
         const float inv = __uint_as_float((uint32_t)(127 - se) << 23);   // 2^-se, exact
-        const int nS = args.H / P_SCALE_COLS;
-        if (staged || direct)
+        const int nS = p_scale_blocks(args.H);
+        // columns of this warp's block that exist: 128, or 64 for the last block of an H that is
+        // 64 (mod 128), or none past H (the tile's B columns there were read as zeros)
+        const int col0 = nb * L2_COLS + ch * P_SCALE_COLS;
+        const int ncols = max(0, min(P_SCALE_COLS, args.H - col0));
+        if ((staged || direct) && ncols > 0)
           args.S_pad[(size_t)(prow0 + r) * nS + nb * (L2_COLS / P_SCALE_COLS) + ch] =
               __uint_as_float((uint32_t)(127 + se) << 23);
         uint16_t* prow = args.P_pad + (size_t)(prow0 + r) * args.H + nb * L2_COLS + ch * P_SCALE_COLS;
@@ -418,7 +426,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
             for (int j = 0; j < 4; ++j) {
               const uint4 v4 = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
               if (staged) *reinterpret_cast<uint4*>(box + chunk_off(4 * c + j)) = v4;
-              else if (direct) reinterpret_cast<uint4*>(prow + pass * 64)[4 * c + j] = v4;
+              else if (direct && pass * 64 < ncols) reinterpret_cast<uint4*>(prow + pass * 64)[4 * c + j] = v4;
             }
           }
           if (pass == MMA_N / 128 - 1) ptx::tc_fence_before();
@@ -427,10 +435,14 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
           if (ep_tid == 0) {
             if (pass == MMA_N / 128 - 1) ptx::mbar_arrive_cluster(tempty_addr);
             uint8_t* buf = stg + (sb % NBUF) * STG_BYTES;
+            const bool box0 = nb * L2_COLS + pass * 64 < args.H;
+            const bool box1 = nb * L2_COLS + P_SCALE_COLS + pass * 64 < args.H;
             for (int gq = 0; gq < nfull; ++gq) {
-              ptx::tma_store_2d(tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64, prow0 + gq * ST_ROWS);
-              ptx::tma_store_2d(tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES, nb * L2_COLS + P_SCALE_COLS + pass * 64,
-                                prow0 + gq * ST_ROWS);
+              if (box0)
+                ptx::tma_store_2d(tmP, buf + gq * ST_BOX_BYTES, nb * L2_COLS + pass * 64, prow0 + gq * ST_ROWS);
+              if (box1)
+                ptx::tma_store_2d(tmP, buf + STG_BOX_BYTES + gq * ST_BOX_BYTES,
+                                  nb * L2_COLS + P_SCALE_COLS + pass * 64, prow0 + gq * ST_ROWS);
             }
             ptx::bulk_commit();                      // one group per pass, possibly empty
           }

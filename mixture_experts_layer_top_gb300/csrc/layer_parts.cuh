@@ -362,7 +362,7 @@ __device__ __forceinline__ void gather_task(const uint16_t* x, const int32_t* pr
 template <bool ALL_IN_FLIGHT>
 __device__ __forceinline__ void combine_item(const uint16_t* P_pad, const float* S_pad, const int32_t* prow_of, int H,
                                              int k, uint16_t* y, int64_t i) {
-  const int nS = H / P_SCALE_COLS;
+  const int nS = p_scale_blocks(H);
   const int64_t t = (i * 8) / H;
   const int64_t c = (i * 8) % H;
   const int32_t* pr = prow_of + t * k;

@@ -21,7 +21,9 @@ namespace {
 
 constexpr int RT_TOK = 32;      // tokens per CTA
 constexpr int RT_EXP = 32;      // experts per CTA
-constexpr int RT_HC = 256;      // h per pipeline stage (8 x 32); H is a multiple of 256
+constexpr int RT_HC = 256;      // h per pipeline stage (8 x 32); the last stage of an H that is not a
+                                // multiple of 256 holds zeros past H (a fused multiply-add of 0 * 0
+                                // leaves a partial sum unchanged, so the canonical value is the same)
 constexpr int RT_NS = 4;        // pipeline stages
 constexpr int RT_XROW = RT_HC + 8;   // bf16 per staged x row (528 B; 16-B multiple, conflict-free reads)
 constexpr int RT_WROW = RT_EXP + 8;  // bf16 per staged Wr row (80 B; conflict-free 16-B reads)
@@ -86,18 +88,19 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
     for (int j = 0; j < RT_HC / 128; ++j) {
       const int q = tid + RT_THREADS * j;
       const int tok = q / XCH, c = q % XCH;
-      const bool x_ok = (t0 + tok) < T;
-      cp_async16(xs + st * RT_STAGE_X + tok * RT_XROW + c * 8,
-                 x + (size_t)(x_ok ? t0 + tok : 0) * H + h0 + c * 8, x_ok);
+      const bool x_ok = (t0 + tok) < T && h0 + c * 8 < H;
+      cp_async16(xs + st * RT_STAGE_X + tok * RT_XROW + c * 8, x_ok ? x + (size_t)(t0 + tok) * H + h0 + c * 8 : x,
+                 x_ok);
       const int row = q >> 2, part = q & 3;
       const int we = we_base + part * 8;
       uint16_t* wdst = ws + st * RT_STAGE_W + row * RT_WROW + part * 8;
-      const uint16_t* wsrc = Wr + (size_t)(h0 + row) * E + we;
+      const bool h_ok = h0 + row < H;
+      const uint16_t* wsrc = Wr + (size_t)(h_ok ? h0 + row : 0) * E + we;
       if (w_vec) {
-        cp_async16(wdst, (we < E) ? wsrc : Wr, we < E);
+        cp_async16(wdst, (we < E && h_ok) ? wsrc : Wr, we < E && h_ok);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wdst[i] = (we + i < E) ? wsrc[i] : (uint16_t)0;
+        for (int i = 0; i < 8; ++i) wdst[i] = (we + i < E && h_ok) ? wsrc[i] : (uint16_t)0;
       }
     }
   };
@@ -106,7 +109,7 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
 #pragma unroll
   for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-  const int nchunk = H / RT_HC;   // H is a multiple of 256
+  const int nchunk = (H + RT_HC - 1) / RT_HC;
 #pragma unroll
   for (int c = 0; c < RT_NS - 1; ++c) {
     if (c < nchunk) issue(c);

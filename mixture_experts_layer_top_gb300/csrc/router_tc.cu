@@ -284,13 +284,17 @@ __device__ __forceinline__ void fma_bf16x2(uint32_t x, uint32_t w, float& p_lo, 
 // pairs (j, j+16), (j, j+8), (j, j+4), (j, j+2), (j, j+1) - lanes sub^2 and sub^1
 // for the first two levels, inside the lane for the rest.  Every lane of the
 // group returns the same value.
+template <bool H_TAIL>
 __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, const uint16_t* __restrict__ wr,
                                                int H, int sub) {
   float p[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) p[j] = 0.0f;
-  // trips of four 32-wide steps, two trips per iteration (H is a multiple of 256),
-  // the next trip's loads issued before this trip's fused multiply-adds
+  // trips of four 32-wide steps, two trips per iteration over the first H256 = H - H mod 256 h,
+  // the next trip's loads issued before this trip's fused multiply-adds; then (H_TAIL: H not a
+  // multiple of 256, a separate instance so the measured loop above keeps its registers) the
+  // remaining 32-wide steps, still in ascending h
+  const int H256 = H_TAIL ? (H & ~255) : H;
   uint4 xa[4], wa[4], xb[4], wb[4];
   auto load = [&](uint4 (&xv)[4], uint4 (&wv)[4], int h) {
 #pragma unroll
@@ -308,12 +312,24 @@ __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, 
       fma_bf16x2(xv[u].w, wv[u].w, p[6], p[7]);
     }
   };
-  load(xa, wa, 8 * sub);
-  for (int h = 8 * sub; h < H; h += 256) {
-    load(xb, wb, h + 128);
-    fma_trip(xa, wa);
-    if (h + 256 < H) load(xa, wa, h + 256);
-    fma_trip(xb, wb);
+  if (!H_TAIL || H256 > 0) {
+    load(xa, wa, 8 * sub);
+    for (int h = 8 * sub; h < H256; h += 256) {
+      load(xb, wb, h + 128);
+      fma_trip(xa, wa);
+      if (h + 256 < H256) load(xa, wa, h + 256);
+      fma_trip(xb, wb);
+    }
+  }
+  if (H_TAIL) {
+    for (int h = H256 + 8 * sub; h < H; h += 32) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + h));
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + h));
+      fma_bf16x2(xv.x, wv.x, p[0], p[1]);
+      fma_bf16x2(xv.y, wv.y, p[2], p[3]);
+      fma_bf16x2(xv.z, wv.z, p[4], p[5]);
+      fma_bf16x2(xv.w, wv.w, p[6], p[7]);
+    }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xFFFFFFFFu, p[j], 2));
@@ -337,7 +353,7 @@ __device__ __forceinline__ float canonical_dot(const uint16_t* __restrict__ xr, 
 // registers) for E <= 128 measured faster than 3 (80 registers) - fine workload 68 -> 64 us -
 // while for E = 256 the 64-register build spills in the hot loop and 3 blocks stay faster
 // (large layer 121-128 vs 136-144 us).
-template <int NK>
+template <int NK, bool H_TAIL>
 __global__ void __launch_bounds__(SEL_WARPS * 32, (NK <= 4) ? 4 : 3)
 router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ WrT, const float* __restrict__ part,
                      int S, const float* __restrict__ nw, const float* __restrict__ bias, int T, int H, int E, int k,
@@ -453,7 +469,7 @@ router_select_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
     for (int i = 1; i < SEL_WARPS; ++i) slot += (q >= pref[i]) ? 1 : 0;
     const int e = cl[slot][q - pref[slot]];
     const int tt = blockIdx.x * ntok + slot;
-    float l = canonical_dot(x + (size_t)tt * H, WrT + (size_t)e * H, H, sub);
+    float l = canonical_dot<H_TAIL>(x + (size_t)tt * H, WrT + (size_t)e * H, H, sub);
     if (bias) l = __fadd_rn(l, bias[e]);
     if (pi < total && sub == 0) lg[slot][e] = l;
   }
@@ -498,7 +514,8 @@ template <int NK>
 cudaError_t launch_select(dim3 grid, cudaStream_t st, const uint16_t* x, const RouterWs& rw, int S,
                           const float* bias, int T, int H, int E, int k, float cH, int ntok, float* logits,
                           int32_t* ids, float* w, int32_t* counts, int32_t* chist) {
-  return launch_pdl(router_select_kernel<NK>, grid, dim3(SEL_WARPS * 32), 0, st, x, rw.WrT, rw.part, S, rw.nw, bias,
+  auto kern = (H % 256 == 0) ? router_select_kernel<NK, false> : router_select_kernel<NK, true>;
+  return launch_pdl(kern, grid, dim3(SEL_WARPS * 32), 0, st, x, rw.WrT, rw.part, S, rw.nw, bias,
                     T, H, E, k, cH, ntok, logits, ids, w, counts, chist);
 }
 

@@ -276,12 +276,16 @@ def test_plan_reused_across_batches(schedule):
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(100, 256, 128, 6, 2), (64, 256, 128, 1, 1), (50, 512, 128, 40, 8),
-                                       (300, 256, 384, 3, 3), (33, 768, 256, 200, 8)])
+                                       (300, 256, 384, 3, 3), (33, 768, 256, 200, 8),
+                                       (77, 64, 64, 5, 2), (200, 320, 192, 12, 3), (129, 384, 320, 40, 4),
+                                       (300, 448, 128, 9, 4), (60, 2112, 832, 16, 8)])
 @pytest.mark.parametrize("flags", [0, EXACT])
 def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
     """Expert counts that are not multiples of 8 / 16 / 32 (tensor-core router N padding,
-    transpose tiles, selection keys), one expert, k = E, the smallest H and I the layout allows:
-    routing and y against the full oracle, default and all-canonical routers."""
+    transpose tiles, selection keys), one expert, k = E, the smallest H and I the layout allows
+    (64), and H = 64, 128, 192 (mod 256) with I = 64 (mod 128) - partial last Linear-1 and
+    Linear-2 tiles and P scale blocks, router rows not a multiple of 256 h: routing and y
+    against the full oracle, default and all-canonical routers."""
     wl = synth.Workload("odd", T, H, I, E, k)
     h = synth.host_inputs(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
@@ -297,7 +301,7 @@ def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
 
 
 def _random_cases(n: int, seed: int = 20261202):
-    """Seeded layer shapes within the library's limits: H a multiple of 256, I of 128, E up
+    """Seeded layer shapes within the library's limits: H and I multiples of 64, E up
     to 256, k up to min(8, E), T up to 300 with a larger T_max, any schedule, the default or
     all-canonical router, the compute ring split or the single launch, a Zipf router bias on
     some."""
@@ -305,8 +309,8 @@ def _random_cases(n: int, seed: int = 20261202):
     out = []
     for _ in range(n):
         E = int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(65, 257))]))
-        out.append(dict(T=int(rng.integers(1, 301)), H=int(rng.choice([256, 512, 768, 1024, 2048])),
-                        I=int(rng.choice([128, 256, 384, 512])), E=E, k=int(rng.integers(1, min(8, E) + 1)),
+        out.append(dict(T=int(rng.integers(1, 301)), H=int(rng.choice([64, 256, 320, 512, 704, 768, 1024, 2048])),
+                        I=int(rng.choice([64, 128, 192, 256, 384, 448, 512])), E=E, k=int(rng.integers(1, min(8, E) + 1)),
                         sched=int(rng.integers(0, 4)), extra=int(rng.integers(0, 200)),
                         flags=[0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE, moe.MOE_FLAG_SINGLE_LAUNCH][int(rng.integers(0, 4))],
                         zipf=float(rng.choice([0.0, 1.2])), host=bool(rng.integers(0, 3) == 0)))
@@ -627,11 +631,13 @@ SINGLE = moe.MOE_FLAG_SINGLE_LAUNCH
 
 @pytest.mark.parametrize("shape,schedule", [((256, 512, 256, 8, 2), 3), ((1000, 512, 256, 16, 4), 0),
                                             ((1000, 512, 256, 16, 4), 1), ((300, 768, 384, 6, 3), 2),
-                                            ((33, 768, 256, 200, 8), 3), ((1, 256, 128, 1, 1), 3)])
+                                            ((33, 768, 256, 200, 8), 3), ((1, 256, 128, 1, 1), 3),
+                                            ((200, 320, 192, 12, 3), 3), ((77, 64, 64, 5, 2), 0)])
 def test_single_launch_bitwise_equals_multi_launch_and_oracle(shape, schedule):
     """MOE_FLAG_SINGLE_LAUNCH (the whole layer in one kernel) against the multi-launch path with
     all-canonical logits: logits, routing and y bit for bit, on several shapes (E not a multiple of
-    8, one expert, one token) and schedules; y against the full oracle; one launch."""
+    8, one expert, one token, H and I not multiples of 256 and 128) and schedules; y against the
+    full oracle; one launch."""
     T, H, I, E, k = shape
     wl = synth.Workload("single", T, H, I, E, k)
     h = synth.host_inputs(wl)

@@ -34,6 +34,7 @@ def test_config_struct_layout():
 
 @pytest.mark.parametrize("kw,status", [
     (dict(H=100), moe.MOE_ERR_UNSUPPORTED), (dict(I=96), moe.MOE_ERR_UNSUPPORTED),
+    (dict(H=32), moe.MOE_ERR_UNSUPPORTED), (dict(I=160), moe.MOE_ERR_UNSUPPORTED),
     (dict(E=300), moe.MOE_ERR_UNSUPPORTED), (dict(top_k=9), moe.MOE_ERR_UNSUPPORTED),
     (dict(top_k=0), moe.MOE_ERR_INVALID_ARG), (dict(T_max=0), moe.MOE_ERR_INVALID_ARG),
     (dict(schedule=4), moe.MOE_ERR_INVALID_ARG), (dict(E=4, top_k=5), moe.MOE_ERR_UNSUPPORTED),
@@ -45,6 +46,14 @@ def test_config_validation(lib, kw, status):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_workspace_bytes(moe.MoEConfig(**base).c())
     assert ei.value.status == status
+
+
+@pytest.mark.parametrize("H,I", [(64, 64), (320, 192), (448, 64), (2048 + 64, 768 + 64)])
+def test_config_accepts_multiples_of_64(lib, H, I):
+    """H and I need only be multiples of 64 (one 64-column TMA box): the last Linear-1 tile of an
+    expert may hold 64 intermediate columns, the last Linear-2 tile 64, 128 or 192 outputs."""
+    b = moe.moe_workspace_bytes(moe.MoEConfig(256, H, I, 8, 2).c())
+    assert b >= 256 * 2 * (2 * H + 2 * I + 4 * H)
 
 
 def test_workspace_bytes_padded_layout(lib):
@@ -74,7 +83,7 @@ def test_plan_without_device_fails_cleanly(lib):
 
 def _check_schedule(counts, H, I, sms, mode, wave_experts=0, lead=1):
     tiles, n1 = moe.moe_schedule_host(counts, H, I, sms, mode, wave_experts, lead)
-    nL1, nL2 = I // 128, H // 256
+    nL1, nL2 = -(-I // 128), -(-H // 256)          # the last tile of each may be partial
     mt = (np.asarray(counts) + 255) // 256          # units: pairs of 128-row m-tiles (one 2-CTA cluster)
     mtb = np.concatenate([[0], np.cumsum(mt)])
     total_mt = int(mtb[-1])
@@ -120,6 +129,18 @@ def test_schedule_permutation_and_order(lib, mode, dist):
         counts = np.zeros(E, np.int64)
         counts[E - 1] = 4096
     _check_schedule(counts, 512, 256, 20, mode, 0, 2 if mode == 1 else 1)
+
+
+@pytest.mark.parametrize("H,I", [(64, 64), (320, 192), (704, 320)])
+def test_schedule_partial_column_blocks(lib, H, I):
+    """Shapes whose I is not a multiple of 128 or H of 256 get ceil(I/128) Linear-1 and
+    ceil(H/256) Linear-2 tiles per unit (the last one partial)."""
+    counts = np.random.default_rng(3).multinomial(3000, np.ones(12) / 12)
+    for mode in (0, 1, 2):
+        tiles, n1 = _check_schedule(counts, H, I, 12, mode)
+        nb1 = {(t[0] >> 1) & 0x7FFF for t in tiles[:n1].tolist() if t[0] & 1 == 0}
+        nb2 = {(t[0] >> 1) & 0x7FFF for t in tiles.tolist() if t[0] & 1 == 1}
+        assert nb1 == set(range(-(-I // 128))) and nb2 == set(range(-(-H // 256)))
 
 
 def test_schedule_phased_is_l1_then_l2(lib):
