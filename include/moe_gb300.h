@@ -87,7 +87,8 @@ typedef enum {
 #define MOE_FLAG_ACT_BILINEAR (1u << 0) /* activation g*u instead of silu(g)*u (GLU "bilinear"
                                            variant, same paper as SwiGLU); used by exactness tests */
 #define MOE_FLAG_STAGE_TIMING (1u << 1) /* record CUDA events between stages (moe_stage_times)    */
-#define MOE_FLAG_TRACE (1u << 2)        /* grouped GEMM records per-CTA wait times (moe_trace_read) */
+#define MOE_FLAG_TRACE (1u << 2)        /* grouped GEMM records per-CTA wait times (moe_trace_read)
+                                           and per-tile SM ids and timestamps (moe_trace_tiles)    */
 /* Shared-memory split of the grouped GEMM (results are bit-identical).  Default: a 6-stage
  * operand ring with one output staging buffer (measured faster on every workload tried, from
  * weight streaming to 1k rows per expert).  MOE_FLAG_GEMM_COMPUTE selects a 5-stage ring with
@@ -223,6 +224,19 @@ MOE_API moe_status_t moe_stage_times(moe_plan_t plan, float* ms);
  * for a free accumulator, MMA issuer waiting for operands, epilogue waiting for an accumulator,
  * CTA lifetime} in nanoseconds, then {Linear-1 tiles, Linear-2 tiles}. */
 MOE_API moe_status_t moe_trace_read(moe_plan_t plan, uint64_t* host_buf, size_t cap, size_t* n);
+
+/* Per-tile trace of the last forward's grouped GEMM (the per-tile timing that the X-Stage
+ * paper's experimental setup takes with in-kernel timer instrumentation, and the SM-id probe of
+ * the TIDE paper's section 2.2, SM wave quantization: CTAs recording their SM id with entry and
+ * exit timestamps); needs MOE_FLAG_TRACE; synchronises the device.  Writes n = tiles x 2 x 4
+ * uint64 values to host_buf (cap = capacity in values; host_buf NULL: n only), tiles = the
+ * length of the tile list moe_debug_schedule returns, in that order; for tile i and CTA rank r
+ * of the 2-CTA cluster that ran it, values (2 i + r) * 4 .. + 3: {SM id, %globaltimer (ns)
+ * when the CTA's TMA producer started the tile, when its accumulator was complete in TMEM,
+ * when its epilogue finished (Linear-1: h rows written, before the unit's readiness count is
+ * raised; Linear-2: the last P stores issued)}.  A tile a timed-out forward never reached reads
+ * zeros.  MOE_ERR_INVALID_ARG without MOE_FLAG_TRACE or if cap < n. */
+MOE_API moe_status_t moe_trace_tiles(moe_plan_t plan, uint64_t* host_buf, size_t cap, size_t* n);
 
 /* The coefficient cH of the default router's error bound (the router used without
  * MOE_FLAG_EXACT_LOGITS; library numerics, no counterpart in the paper) for a forward

@@ -52,7 +52,7 @@ STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")
 EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_get_status",
             "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
-            "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read",
+            "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read", "moe_trace_tiles",
             "moe_router_bound", "moe_debug_schedule")
 
 
@@ -106,6 +106,7 @@ def load() -> ctypes.CDLL:
     L.moe_schedule_host.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, i64, P(i64)]
     L.moe_dispatch_static.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
     L.moe_trace_read.argtypes = [vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)]
+    L.moe_trace_tiles.argtypes = [vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)]
     for f in EXPORTED:
         if f != "moe_status_string":
             getattr(L, f).restype = ctypes.c_int
@@ -195,6 +196,25 @@ def moe_trace_read(plan: int) -> np.ndarray:
     if st != MOE_OK:
         raise MoEError(st, "moe_trace_read")
     return out.reshape(-1, len(TRACE_FIELDS))
+
+
+TILE_TRACE_FIELDS = ("sm_id", "start_ns", "acc_ready_ns", "end_ns")
+
+
+def moe_trace_tiles(plan: int) -> np.ndarray:
+    """Per-tile trace of the last forward's grouped GEMM: [tiles, 2 (CTA rank), 4] uint64 (fields
+    in TILE_TRACE_FIELDS), tiles in the order of moe_debug_schedule.  Needs MOE_FLAG_TRACE."""
+    n = ctypes.c_size_t(0)
+    L = load()
+    st = L.moe_trace_tiles(plan, None, 0, ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_trace_tiles")
+    out = np.zeros(n.value, dtype=np.uint64)
+    if n.value:
+        st = L.moe_trace_tiles(plan, out.ctypes.data, n.value, ctypes.byref(n))
+        if st != MOE_OK:
+            raise MoEError(st, "moe_trace_tiles")
+    return out.reshape(-1, 2, len(TILE_TRACE_FIELDS))
 
 
 def moe_plan_destroy(plan: int) -> int:

@@ -40,6 +40,7 @@ struct moe_plan_s {
   cudaEvent_t ev_range[4];
   int last_launches;
   unsigned long long* trace;   // [max(gemm_grid, fused_grid) + 1][TRACE_SLOTS] when MOE_FLAG_TRACE
+  unsigned long long* tile_trace;   // [max_tiles][PAIR][TILE_TRACE_SLOTS] when MOE_FLAG_TRACE
 };
 
 namespace {
@@ -59,6 +60,7 @@ void release(moe_plan_s* p) {
   if (p->base) cudaFree(p->base);
   if (p->bias) cudaFree(p->bias);
   if (p->trace) cudaFree(p->trace);
+  if (p->tile_trace) cudaFree(p->tile_trace);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -194,6 +196,15 @@ moe_status_t check_forward_args(moe_plan_t p, int32_t T, const void* x, const fl
 // CTA rows of the trace buffer (the larger grid of the two launch paths); one more row of
 // TRACE_SLOTS values follows them: the phase stamps of a single-launch forward.
 int trace_ctas(const moe_plan_s* p) { return p->gemm_grid > p->fused_grid ? p->gemm_grid : p->fused_grid; }
+size_t tile_trace_bytes(const moe_plan_s* p) {
+  return sizeof(unsigned long long) * PAIR * TILE_TRACE_SLOTS * (size_t)p->max_tiles;
+}
+// zero both trace buffers before a forward's grouped GEMM (MOE_FLAG_TRACE)
+cudaError_t clear_traces(const moe_plan_s* p, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->tile_trace, 0, tile_trace_bytes(p), st);
+  return e;
+}
 
 // Arguments of the grouped GEMM (both launch paths) other than the tile range.
 GemmArgs gemm_args(const moe_plan_s* p) {
@@ -209,6 +220,7 @@ GemmArgs gemm_args(const moe_plan_s* p) {
   ga.ready = p->ws.ready;
   ga.err = p->ws.err;
   ga.trace = p->trace;
+  ga.tile_trace = p->tile_trace;
   ga.range_sel = 2;
   ga.H = c.H;
   ga.I = c.I;
@@ -264,7 +276,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     }
     GemmArgs ga = gemm_args(p);
     if (p->trace)
-      MOE_CK(cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1), st));
+      MOE_CK(clear_traces(p, st));
     const int sched_mode = (c.schedule == MOE_SCHED_AUTO) ? MOE_SCHED_WAVE_SERIAL : c.schedule;
     const int sched_we = (c.schedule == MOE_SCHED_AUTO) ? E : c.wave_experts;
     MOE_CK(launch_fused_layer(tA1, tB1, tA2, tB2, tH, tP, p->ws, p->ws.gbar, static_cast<const uint16_t*>(x),
@@ -353,7 +365,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   }
   GemmArgs ga = gemm_args(p);
   if (p->trace)
-    MOE_CK(cudaMemsetAsync(p->trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1), st));
+    MOE_CK(clear_traces(p, st));
   const bool streaming = !(c.flags & MOE_FLAG_GEMM_COMPUTE);   // the deeper operand ring by default
   if (c.schedule == MOE_SCHED_PHASED) {
     ga.range_sel = 0;
@@ -488,6 +500,11 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
       p->trace = nullptr;
       return fail(MOE_ERR_OOM);
     }
+    if (cudaMalloc(&p->tile_trace, tile_trace_bytes(p)) != cudaSuccess) {
+      cudaGetLastError();
+      p->tile_trace = nullptr;
+      return fail(MOE_ERR_OOM);
+    }
   }
   p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
   if (p->timing)
@@ -593,6 +610,22 @@ moe_status_t moe_trace_read(moe_plan_t p, uint64_t* host_buf, size_t cap, size_t
   if (cap < cnt) return MOE_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(host_buf, p->trace, cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_trace_tiles(moe_plan_t p, uint64_t* host_buf, size_t cap, size_t* n) {
+  if (!p || !n || !p->tile_trace) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t sc[4] = {0, 0, 0, 0};
+  if (p->last_launches > 0 && cudaMemcpy(sc, p->ws.sched, sizeof(sc), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const size_t tiles = (sc[1] > 0 && sc[1] <= p->max_tiles) ? (size_t)sc[1] : 0;
+  const size_t cnt = tiles * PAIR * TILE_TRACE_SLOTS;
+  *n = cnt;
+  if (!host_buf || cnt == 0) return MOE_OK;
+  if (cap < cnt) return MOE_ERR_INVALID_ARG;
+  if (cudaMemcpy(host_buf, p->tile_trace, cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -121,6 +121,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
   const bool tracing = (args.flags & MOE_FLAG_TRACE) != 0;
+  const bool tile_tracing = tracing && args.tile_trace != nullptr;
   const uint64_t t_start = ptx::globaltimer();
   uint64_t tr_a = 0, tr_b = 0;     // this thread's two wait-time counters (role specific)
   uint64_t* trp_a = tracing ? &tr_a : nullptr;
@@ -144,6 +145,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
         const int4 tl = args.tiles[i];
         const int ph = tl.x & 1, nb = (tl.x >> 1) & 0x7FFF, e = tl.y, g = tl.w;
         const int row0 = g * UNIT_ROWS + rank * BM;     // this CTA's 128 padded rows of the unit
+        if (tile_tracing) args.tile_trace[((size_t)i * PAIR + rank) * TILE_TRACE_SLOTS + TT_START] = ptx::globaltimer();
         const int nk = (ph == 0 ? args.H : args.I) / BK;
         // a unit whose valid rows all lie in the even CTA's half: the odd CTA's A rows are
         // padding, whose accumulator rows are never stored, so they are not loaded at all
@@ -301,10 +303,16 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
       const int as = local & 1;
       const uint32_t aphase = (local >> 1) & 1;
       // one thread waits, the named barrier broadcasts its decision to all epilogue threads
+      unsigned long long* const ttr =
+          tile_tracing ? args.tile_trace + ((size_t)i * PAIR + rank) * TILE_TRACE_SLOTS : nullptr;
       if (ep_tid == 0) {
         const bool okw = ptx::mbar_wait(&ctl->tfull[as], aphase, tmo, abort_flag, trp_a);
         if (!okw) set_abort(ctl, args.err, ERR_TIMEOUT);
         *(volatile int*)&ctl->ep_ok[local & 1] = okw ? 1 : 0;
+        if (ttr && okw) {
+          ttr[TT_SMID] = ptx::smid();
+          ttr[TT_ACC] = ptx::globaltimer();
+        }
       }
       ptx::named_bar_sync(1, EPI_THREADS);
       if (!*(volatile int*)&ctl->ep_ok[local & 1]) break;
@@ -362,6 +370,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
           ptx::bulk_commit();
           ptx::bulk_wait<0>();                       // h rows written: publish them to Linear-2
           ptx::fence_proxy_async_global();
+          if (ttr) ttr[TT_END] = ptx::globaltimer();
           __threadfence();
           ptx::red_release_add_gpu(args.ready + g, 1);
         }
@@ -445,6 +454,7 @@ __device__ __forceinline__ void grouped_gemm_body(const CUtensorMap* tmA1, const
                                   nb * L2_COLS + P_SCALE_COLS + pass * 64, prow0 + gq * ST_ROWS);
             }
             ptx::bulk_commit();                      // one group per pass, possibly empty
+            if (ttr && pass == MMA_N / 128 - 1) ttr[TT_END] = ptx::globaltimer();
           }
           ++sb;
         }

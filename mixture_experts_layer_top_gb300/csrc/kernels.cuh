@@ -70,6 +70,12 @@ enum TraceSlot {
   TR_TILES_L2 = 7,         // Linear-2 tiles (count)
   TRACE_SLOTS = 8
 };
+// Per-tile records of the grouped GEMM under MOE_FLAG_TRACE: for tile i of the tile list
+// and CTA rank r of its cluster, 4 values at tile_trace[(2 i + r) * 4]: the SM id, then the
+// %globaltimer (ns) when the CTA's producer started the tile, when its accumulator was ready
+// for the epilogue, and when the epilogue finished it (Linear-1: its h rows written, just
+// before the unit's readiness count is raised; Linear-2: the last P stores issued).
+enum TileTraceSlot { TT_SMID = 0, TT_START = 1, TT_ACC = 2, TT_END = 3, TILE_TRACE_SLOTS = 4 };
 
 struct GemmArgs {
   const int4* tiles;
@@ -82,6 +88,7 @@ struct GemmArgs {
   int32_t* ready;
   uint32_t* err;
   unsigned long long* trace;
+  unsigned long long* tile_trace;   // [tiles][PAIR][TILE_TRACE_SLOTS] (MOE_FLAG_TRACE) or null
   int range_sel;  // 0: linear-1 tiles, 1: linear-2 tiles, 2: all, 3: none
   int H, I, E, R_pad, nL1, nL2;
   uint32_t flags;

@@ -20,6 +20,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 // Programmatic dependent launch: wait until the previous kernel of the stream has
 // completed and its memory is visible (returns at once when launched without the
 // programmatic-serialization attribute).

@@ -28,7 +28,7 @@ int main(void) {
   CHECK(bytes > (size_t)cfg.T_max * cfg.top_k * (size_t)(2 * cfg.I + 2 * cfg.H));
 
   moe_config_t bad = cfg;
-  bad.H = 500; /* not a multiple of 256 */
+  bad.H = 500; /* not a multiple of 64 */
   CHECK(moe_workspace_bytes(&bad, &bytes) == MOE_ERR_UNSUPPORTED);
   bad = cfg;
   bad.top_k = 0;

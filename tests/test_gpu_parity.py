@@ -737,3 +737,49 @@ def test_single_launch_phase_stamps_and_trace_layout():
             assert np.all(stamps == 0)
             assert tr[:-1, 5].max() > 0
         layer.close()
+
+
+@pytest.mark.parametrize("schedule,flags", [(moe.MOE_SCHED_AUTO, 0), (moe.MOE_SCHED_INTERLEAVED, 0),
+                                            (moe.MOE_SCHED_PHASED, 0), (moe.MOE_SCHED_AUTO, SINGLE)])
+def test_tile_trace_records_every_tile(schedule, flags):
+    """moe_trace_tiles: one record per tile of the tile list and CTA rank, for every launch form:
+    SM ids inside the GPU, the two CTAs of a tile on two SMs, each cluster's tiles on one SM
+    pair in ticket order, start <= accumulator ready <= end, and every Linear-2 tile's
+    accumulator complete no earlier than the last Linear-1 tile of its unit finished (the
+    readiness dependency); without MOE_FLAG_TRACE the call is refused."""
+    wl = synth.Workload("trace", 1500, 1024, 384, 24, 4)
+    d = synth.device_inputs(wl)
+    layer = _layer(wl, schedule, flags=flags | moe.MOE_FLAG_TRACE)
+    for _ in range(2):                                   # the second forward's records start from zero
+        layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    tiles, n1, workers = layer.schedule()
+    tr = moe.moe_trace_tiles(layer.plan).astype(np.int64)
+    assert tr.shape == (len(tiles), 2, 4)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sm, start, acc, end = tr[..., 0], tr[..., 1], tr[..., 2], tr[..., 3]
+    assert np.all(start > 0) and np.all(sm < sms) and np.all(sm[:, 0] != sm[:, 1])
+    assert np.all(start <= acc) and np.all(acc <= end)
+    # both CTAs' loads feed the pair MMA: each accumulator is complete after both producers started
+    assert np.all(acc.min(axis=1) >= start.max(axis=1))
+    phased = schedule == moe.MOE_SCHED_PHASED
+    idx = np.arange(len(tiles))
+    first = np.where(phased & (idx >= n1), n1, 0)        # the phased schedule's second launch starts at n1
+    group = (first > 0) * 10**6 + (idx - first) % workers     # (launch, cluster) of each tile
+    for gk in np.unique(group):
+        sel = idx[group == gk]
+        for r in range(2):
+            assert len(set(sm[sel, r].tolist())) == 1, "a persistent CTA stays on its SM"
+            assert np.all(np.diff(start[sel, r]) >= 0) and np.all(np.diff(end[sel, r]) >= 0)
+    l1_end = {}
+    for i, (ph_n, e, m, g) in enumerate(tiles.tolist()):
+        if ph_n & 1 == 0:
+            l1_end[g] = max(l1_end.get(g, 0), int(end[i].max()))
+    for i, (ph_n, e, m, g) in enumerate(tiles.tolist()):
+        if ph_n & 1 == 1:
+            assert acc[i].min() >= l1_end[g], (i, g)
+    layer.close()
+    plain = _layer(wl, schedule, flags=flags)
+    plain.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    with pytest.raises(moe.MoEError):
+        moe.moe_trace_tiles(plain.plan)
+    plain.close()
