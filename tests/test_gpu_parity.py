@@ -783,3 +783,42 @@ def test_tile_trace_records_every_tile(schedule, flags):
     with pytest.raises(moe.MoEError):
         moe.moe_trace_tiles(plain.plan)
     plain.close()
+
+
+@pytest.mark.parametrize("schedule,flags", [(moe.MOE_SCHED_AUTO, 0), (moe.MOE_SCHED_INTERLEAVED, 0),
+                                            (moe.MOE_SCHED_PHASED, 0), (moe.MOE_SCHED_AUTO, EXACT),
+                                            (moe.MOE_SCHED_AUTO, SINGLE)])
+def test_forward_captured_in_cuda_graph(schedule, flags):
+    """moe_forward is stream-ordered and never synchronises, so a forward can be captured in a
+    CUDA graph: replays on new inputs copied into the captured buffers give logits, routing and y
+    bitwise equal to eager forwards of the same inputs, and the device status stays clean."""
+    wl = synth.Workload("graph", 700, 512, 256, 16, 4)
+    layer = _layer(wl, schedule, flags=flags)
+    w = synth.device_inputs(wl)
+    xs = [synth.device_inputs(synth.Workload("graph", 700, 512, 256, 16, 4, seed=s))["x"] for s in (1, 2, 3)]
+    x = torch.empty_like(xs[0])
+    logits = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    x.copy_(xs[0])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                       # warm-up outside the capture
+        layer.forward(x, w["Wr"], w["W1"], w["W2"], logits=logits, y=y)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, w["Wr"], w["W1"], w["W2"], logits=logits, y=y)
+    for xi in xs:
+        x.copy_(xi)
+        g.replay()
+        torch.cuda.synchronize()
+        layer.check()
+        got = (y.view(torch.int16).clone(), logits.clone(), {kk: v.cpu() for kk, v in layer.routing(wl.T).items()})
+        y_e, lg_e = layer.forward(xi, w["Wr"], w["W1"], w["W2"], check=True)
+        assert torch.equal(got[0], y_e.view(torch.int16)), "y of the replay differs from the eager forward"
+        assert torch.equal(got[1], lg_e), "logits differ"
+        for kk, v in layer.routing(wl.T).items():
+            assert torch.equal(got[2][kk], v.cpu()), kk
+    del g
+    layer.close()
