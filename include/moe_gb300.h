@@ -105,7 +105,8 @@ typedef enum {
  * and the tensor-core estimate (+ bias) elsewhere, within
  *   d = cH * ||x_t||_2 * ||Wr[:,e]||_2 + 2^-20 (|estimate - bias| + |bias|) of the canonical value,
  *   cH from moe_router_bound (at most (H/16 + 1) 2^-17 + (H/32 + 8 + 64) 2^-22).
- * MOE_FLAG_EXACT_LOGITS evaluates every logit in the canonical order on the CUDA cores. */
+ * MOE_FLAG_EXACT_LOGITS evaluates every logit in the canonical order on the CUDA cores; so does
+ * the default for E <= 8 with T * H * E <= 2^23 (measured faster there; every logit canonical). */
 #define MOE_FLAG_EXACT_LOGITS (1u << 5)
 /* The whole layer as ONE kernel launch (after the per-forward memset of the expert counts):
  * the MegaMoE design of the X-Stage paper's introduction - one persistent kernel for routing,
