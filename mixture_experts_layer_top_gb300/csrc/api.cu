@@ -193,6 +193,27 @@ moe_status_t check_forward_args(moe_plan_t p, int32_t T, const void* x, const fl
   return MOE_OK;
 }
 
+// Router of a forward with W_router given.  ROUTER_TC: tensor-core estimates + certified
+// canonical selection; ROUTER_CANON_32: canonical logits, 32 tokens x 32 experts per CTA, then
+// top-k; ROUTER_CANON_TASKS: canonical logits by 32-token x 8-expert tasks over every SM (top-k
+// in the same kernel for E <= 8).  Routing is the same whichever runs; the canonical ones write
+// every logit canonical (MOE_FLAG_EXACT_LOGITS asks for one of them).  The rule follows a
+// same-box measurement of each router forced on every shape (router stage, us: tensor-core /
+// 32 x 32 / tasks): T=256 H=512 E=8 16.0 / 16.0 / 15.0 with the 32 x 32 kernel's step fastest
+// (38.1 vs 38.9 us), T=1024 E=8 16.1 / 14.9 / 15.1 (steps 42.8 / 39.5 / 41.2), T=4096 H=1024
+// E=8 21.5 / 23.1 / 19.1; H=2048 E=128: T=64 24.2 / 28.3 / 21.1, T=256 26.2 / 29.3 / 22.6,
+// T=512 26.6 / 29.3 / 28.0, T=1024 28.3 / 29.8 / 43.6; H=7168 E=256: T=32 48.8 / 71.5 / 44.0,
+// T=128 53.0 / 72.8 / 44.5, T=256 47.6 / 73.0 / 61.5, T=512 46.8 / 73.4 / 109.1.  So: the
+// 32 x 32 kernel for small layers with at most 8 experts, the tasks while there are at most as
+// many as SMs, the tensor-core router above (or the 32 x 32 kernel when all logits must be
+// canonical).
+enum { ROUTER_TC = 0, ROUTER_CANON_32 = 1, ROUTER_CANON_TASKS = 2 };
+int router_choice(uint32_t flags, int T, int H, int E, int sms) {
+  if (E <= 8 && (int64_t)T * H * E <= (1ll << 23)) return ROUTER_CANON_32;
+  if (router_tasks(T, E) <= sms) return ROUTER_CANON_TASKS;
+  return (flags & MOE_FLAG_EXACT_LOGITS) ? ROUTER_CANON_32 : ROUTER_TC;
+}
+
 // CTA rows of the trace buffer (the larger grid of the two launch paths); one more row of
 // TRACE_SLOTS values follows them: the phase stamps of a single-launch forward.
 int trace_ctas(const moe_plan_s* p) { return p->gemm_grid > p->fused_grid ? p->gemm_grid : p->fused_grid; }
@@ -290,12 +311,8 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     p->last_launches = nl;
     return MOE_OK;
   }
-  // the all-canonical CUDA-core router also serves small layers with at most 8 experts, where it
-  // measured faster than the estimate + certified-selection chain (same routing; every logit
-  // canonical): T=256 H=512 E=8 router 16.0 -> 14.7 us, step 40.9 -> 38.2 us; T=1024 step 43.0
-  // -> 40.2 us; with 128 experts or H = 7168 the tensor-core router stays faster at every T tried
-  const bool small_router = E <= 8 && (int64_t)T * H * E <= (1ll << 23);
-  const bool tc_router = W_router && !(c.flags & MOE_FLAG_EXACT_LOGITS) && !small_router;
+  const int rchoice = W_router ? router_choice(c.flags, T, H, E, p->num_sms) : ROUTER_CANON_32;
+  const bool tc_router = rchoice == ROUTER_TC;
   if (x_src && !tc_router) {   // whole copy first
     MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
     ++nl;
@@ -341,13 +358,20 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
       nl += 2;
     }
   } else {
-    if (W_router) {
+    bool topk_done = false;
+    if (W_router && rchoice == ROUTER_CANON_TASKS) {
+      MOE_CK(launch_router_tasks(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router), p->bias,
+                                 router_logits, p->ws, T, H, E, k, p->num_sms, &topk_done, st));
+      ++nl;
+    } else if (W_router) {
       MOE_CK(launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
                                   p->bias, router_logits, T, H, E, st));
       ++nl;
     }
-    MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->ws.chist, p->num_sms, st));
-    ++nl;
+    if (!topk_done) {
+      MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->ws.chist, p->num_sms, st));
+      ++nl;
+    }
   }
   rec(1);
   // schedule actually run: MOE_SCHED_AUTO resolves to wave-serial with one wave of all experts
@@ -497,7 +521,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
       return fail(MOE_ERR_CUDA);
   }
   if (gemm_prepare(device, &p->gemm_grid) != cudaSuccess || router_prepare() != cudaSuccess ||
-      router_tc_prepare() != cudaSuccess || fused_prepare(device, &p->fused_grid) != cudaSuccess)
+      router_tc_prepare() != cudaSuccess || router_tasks_prepare() != cudaSuccess ||
+      fused_prepare(device, &p->fused_grid) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   if (cfg->flags & MOE_FLAG_TRACE) {
     if (cudaMalloc(&p->trace, sizeof(unsigned long long) * TRACE_SLOTS * (trace_ctas(p) + 1)) != cudaSuccess) {

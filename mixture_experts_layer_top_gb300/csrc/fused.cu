@@ -231,6 +231,19 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
   }
 }
 
+// Phase A as a kernel of its own: the multi-launch path's canonical router for small token
+// counts, where its tasks (32 tokens x 8 experts, one CTA each) spread over every SM while the
+// tensor-core router's selection and the 32 x 32 canonical kernel leave most SMs idle.  With
+// E <= FR_EXP the CTA that wrote a task's logits also selects its tokens' experts.
+constexpr int FR_SMEM = FR_NS * FR_STAGE * 2 + FR_TOK * FR_EXP * 4;
+
+__global__ void __launch_bounds__(GEMM_THREADS)
+router_tasks_kernel(const FusedArgs a) {
+  extern __shared__ __align__(16) uint8_t rsm_raw[];
+  ptx::grid_dep_wait();   // the previous kernel's results are visible from here on
+  router_phase(a, reinterpret_cast<uint16_t*>(rsm_raw), threadIdx.x & 31, threadIdx.x >> 5, a.E <= FR_EXP);
+}
+
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fused_layer_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -307,6 +320,31 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
 }
 
 }  // namespace
+
+cudaError_t router_tasks_prepare() {
+  return cudaFuncSetAttribute(router_tasks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FR_SMEM);
+}
+
+int router_tasks(int T, int E) { return ((T + FR_TOK - 1) / FR_TOK) * ((E + FR_EXP - 1) / FR_EXP); }
+
+cudaError_t launch_router_tasks(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits,
+                                const Workspace& ws, int T, int H, int E, int k, int num_sms, bool* topk_done,
+                                cudaStream_t st) {
+  FusedArgs a = {};
+  a.x = x;
+  a.Wr = Wr;
+  a.bias = bias;
+  a.logits = logits;
+  a.ws = ws;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.k = k;
+  *topk_done = E <= FR_EXP;
+  const int tasks = router_tasks(T, E), cap = 2 * num_sms;   // two resident CTAs per SM
+  return launch_pdl(router_tasks_kernel, dim3((unsigned)(tasks < cap ? tasks : cap)), dim3(GEMM_THREADS),
+                    (size_t)FR_SMEM, st, a);
+}
 
 cudaError_t fused_prepare(int device, int* grid) {
   using L = Layout<6, 1>;

@@ -32,6 +32,19 @@ def _layer(wl, schedule=0, flags=0, T_max=None, timeout_ns=0, wave_experts=0, le
     return moe.MoELayer(cfg, 0, router_bias=bias)
 
 
+def _router_plan(T, H, E, exact=False):
+    """(router launches, every logit canonical) of a forward under the library's router rule:
+    the 32 x 32 canonical kernel + top-k for E <= 8 with T*H*E <= 2^23, the 32-token x 8-expert
+    task kernel (+ top-k unless E <= 8) while the tasks fit one per SM, else the tensor-core
+    estimate + transpose + certified selection (or the 32 x 32 kernel + top-k under EXACT)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if E <= 8 and T * H * E <= 2 ** 23:
+        return 2, True
+    if -(-T // 32) * -(-E // 8) <= sms:
+        return (1 if E <= 8 else 2), True
+    return (2, True) if exact else (3, False)
+
+
 def _bias(wl):
     return synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
 
@@ -282,23 +295,24 @@ def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
     transpose tiles, selection keys), one expert, k = E, the smallest H and I the layout allows
     (64), and H = 64, 128, 192 (mod 256) with I = 64 (mod 128) - partial last Linear-1 and
     Linear-2 tiles and P scale blocks, router rows not a multiple of 256 h: routing and y
-    against the full oracle, default and all-canonical routers.  With at most 8 experts the
-    default router is the all-canonical one up to T*H*E = 2^23 (every logit equals the oracle's)
-    and the tensor-core one above it (the last three shapes)."""
+    against the full oracle, default and all-canonical routers.  Which router runs follows the
+    library's rule (`_router_plan`): the canonical kernels' logits equal the oracle's, the
+    tensor-core router's estimates lie within the bound (the last three shapes take it with at
+    most 8 experts, above T*H*E = 2^23 and one task per SM)."""
     wl = synth.Workload("odd", T, H, I, E, k)
     h = synth.host_inputs(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
     layer = _layer(wl, flags=flags)
     d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
     y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
-    canonical = flags & EXACT or (E <= 8 and T * H * E <= 2 ** 23)
-    assert layer.launch_count() == (2 if canonical else 3) + 4      # router launches + 4 (schedule 0)
+    n_router, canonical = _router_plan(T, H, E, bool(flags & EXACT))
+    assert layer.launch_count() == n_router + 4      # router launches + Dispatch, gather, GEMM, Combine
     if canonical:
         assert np.array_equal(logits.cpu().numpy(), ref["logits"])
     else:
         st = check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T))
-        if E <= 8 and E > k:
-            assert st["exact_frac"] < 1.0, "tensor-core estimates expected above T*H*E = 2^23"
+        if E > k:
+            assert st["exact_frac"] < 1.0, "tensor-core estimates expected"
     routing_equal(layer.routing(T), ref, T)
     check_y(bits(y), ref)
 
@@ -421,8 +435,9 @@ def test_host_buffers_match_device_forward(mode, T, flags):
     buffer, a view starting 3 rows in) are read by copy kernels - in up to 4 ranges of whole
     128-token chunks, each routed as it lands, with the split plan of the whole batch - and
     Combine writes y in place; a page-locked view 8 bytes off alignment and pageable buffers
-    go through the copy engines (no extra launch).  The all-canonical router copies x whole."""
-    wl = synth.Workload("host", T, 1024, 256, 16, 4)
+    go through the copy engines (no extra launch).  The canonical routers (all-canonical, and
+    the task kernel the 100-token batch takes) copy x whole."""
+    wl = synth.Workload("host", T, 1024, 256, 64, 4)
     h = synth.host_inputs(wl)
     d = {k: from_bits(v) for k, v in h.items() if k != "bias"}
     layer = _layer(wl, flags=flags)
@@ -445,7 +460,8 @@ def test_host_buffers_match_device_forward(mode, T, flags):
         assert torch.equal(v.cpu(), r_dev[k_]), k_
     direct = mode in ("pinned", "pinned_view")
     ranges = min(4, -(-T // 128))
-    extra = 0 if not direct else (1 if flags & EXACT else ranges + 2 * (ranges - 1))
+    canonical = _router_plan(T, wl.H, wl.E, bool(flags & EXACT))[1]
+    extra = 0 if not direct else (1 if canonical else ranges + 2 * (ranges - 1))
     assert layer.launch_count() == n_dev + extra
     assert torch.isnan(yb[:off]).all() and torch.isnan(yb[off + n:]).all()   # nothing outside y_host
 
@@ -456,6 +472,7 @@ def test_router_certified_selection_on_ties_and_infinities():
     values break ties to the lower id); an infinite Wr entry makes one expert's logits
     non-finite, so every token falls back to canonical logits for all experts."""
     T, H, I, E, k = 1000, 512, 256, 64, 8
+    assert not _router_plan(T, H, E)[1]               # the tensor-core router runs
     rng = np.random.default_rng(5)
     x = oracle.f32_to_bf16(rng.integers(-1, 2, size=(T, H)).astype(np.float32))
     Wr = oracle.f32_to_bf16((rng.integers(-2, 3, size=(H, E)) * 0.0625).astype(np.float32))
@@ -517,7 +534,8 @@ def test_router_certificate_under_stress(mode):
     ("align") or to put the k-th place on exact ties and 1-2 unit gaps ("ladder"): routing
     bit-exact, selected logits canonical, every written estimate within the bound; the
     largest observed error/bound ratio is printed."""
-    T, H, I, E, k = 512, 1024, 256, 64, 8
+    T, H, I, E, k = 1024, 1024, 256, 64, 8        # 256 router tasks: the tensor-core router runs
+    assert not _router_plan(T, H, E)[1]
     xb, wb = _stress_router_inputs(T, H, E, k, mode)
     wl = synth.Workload("rstress", T, H, I, E, k)
     hw = synth.host_inputs(wl)
