@@ -258,13 +258,17 @@ def test_ragged_token_counts(T, flags):
 
 @pytest.mark.parametrize("schedule", [moe.MOE_SCHED_AUTO, moe.MOE_SCHED_INTERLEAVED, moe.MOE_SCHED_PHASED])
 def test_plan_reused_across_batches(schedule):
-    """One plan, five forwards with different token counts and different inputs (weights
-    included), one of them through the host-buffer entry point: each against the full
+    """One plan, six forwards with different token counts and different inputs (weights
+    included), two of them through the host-buffer entry point: each against the full
     oracle, so that nothing a forward leaves in the workspace (counts, chunk histograms,
-    readiness counters, padded rows, the staging buffers) reaches the next one."""
+    readiness counters, padded rows, the staging buffers, the router's split estimates) reaches
+    the next one.  With 64 experts the router changes between forwards: the tensor-core one for
+    1000 and 640 tokens, the canonical task kernel for the others."""
     layer = None
-    for T, seed, host in [(1000, 11, False), (37, 12, False), (513, 13, False), (200, 14, True), (1000, 15, False)]:
-        wl = synth.Workload("reuse", T, 512, 256, 16, 4, seed=seed)
+    plans = [(1000, 11, False), (37, 12, False), (513, 13, False), (200, 14, True), (1000, 15, False), (640, 16, True)]
+    assert [_router_plan(T, 512, 64)[1] for T, _, _ in plans] == [False, True, True, True, False, False]
+    for T, seed, host in plans:
+        wl = synth.Workload("reuse", T, 512, 256, 64, 4, seed=seed)
         if layer is None:
             layer = _layer(wl, schedule, T_max=1024)
         h = synth.host_inputs(wl)
