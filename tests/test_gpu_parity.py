@@ -338,7 +338,23 @@ def _random_cases(n: int, seed: int = 20261202):
     return out
 
 
-@pytest.mark.parametrize("c", _random_cases(24),
+def _random_cases_many_tokens(n: int, seed: int = 20261203):
+    """Seeded shapes with 300 to 2000 tokens and small H and I (multiples of 64 up to 512 / 256),
+    so that the tensor-core router, experts of several 256-row units and multi-wave schedules
+    meet ragged shapes while the full oracle stays cheap."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        E = int(rng.choice([int(rng.integers(2, 33)), int(rng.integers(33, 257))]))
+        out.append(dict(T=int(rng.integers(300, 2001)), H=64 * int(rng.integers(1, 9)), I=64 * int(rng.integers(1, 5)),
+                        E=E, k=int(rng.integers(1, min(8, E) + 1)), sched=int(rng.integers(0, 4)),
+                        extra=int(rng.integers(0, 300)),
+                        flags=[0, 0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE, moe.MOE_FLAG_SINGLE_LAUNCH][int(rng.integers(0, 5))],
+                        zipf=float(rng.choice([0.0, 1.2])), host=bool(rng.integers(0, 3) == 0)))
+    return out
+
+
+@pytest.mark.parametrize("c", _random_cases(24) + _random_cases_many_tokens(32),
                          ids=lambda c: "T{T}-H{H}-I{I}-E{E}-k{k}-s{sched}-f{flags}-z{zipf}-h{host:d}".format(**c))
 def test_random_shapes_full_oracle(c):
     """Routing (bit-exact) and y (stated tolerance) against the full oracle on seeded random
