@@ -863,3 +863,38 @@ def test_forward_captured_in_cuda_graph(schedule, flags):
             assert torch.equal(got[2][kk], v.cpu()), kk
     del g
     layer.close()
+
+
+@pytest.mark.parametrize("schedule,flags", [(moe.MOE_SCHED_AUTO, 0), (moe.MOE_SCHED_INTERLEAVED, 0),
+                                            (moe.MOE_SCHED_AUTO, SINGLE)])
+def test_plan_reuse_long_random_sequence(schedule, flags):
+    """Forty forwards of one plan with seeded random token counts (1 to 2048: every router the
+    rule picks, experts of one to several units, some through the host-buffer entry point), each
+    bitwise equal - logits, routing, y - to a fresh plan's forward of the same inputs: nothing a
+    forward leaves in the workspace changes a later one."""
+    H, I, E, k, T_max = 512, 256, 64, 4, 2048
+    rng = np.random.default_rng(77)
+    wl_max = synth.Workload("seq", T_max, H, I, E, k)
+    w = synth.device_inputs(wl_max)
+    xs = synth.device_inputs(synth.Workload("seq", T_max, H, I, E, k, seed=5))["x"]
+    layer = _layer(wl_max, schedule, flags=flags)
+    for step in range(40):
+        T = int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(65, 700)), int(rng.integers(700, T_max + 1))]))
+        off = int(rng.integers(0, T_max - T + 1))
+        x = xs[off:off + T].contiguous()
+        host = bool(rng.integers(0, 4) == 0)
+        if host:
+            y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+            lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+            layer.forward_host(x.cpu().pin_memory(), w["Wr"], w["W1"], w["W2"], lg, y, check=True)
+        else:
+            y, lg = layer.forward(x, w["Wr"], w["W1"], w["W2"], check=True)
+        r = {kk: v.cpu() for kk, v in layer.routing(T).items()}
+        fresh = _layer(synth.Workload("seq", T, H, I, E, k), schedule, flags=flags)
+        y_f, lg_f = fresh.forward(x, w["Wr"], w["W1"], w["W2"], check=True)
+        assert torch.equal(lg.cpu(), lg_f.cpu()), f"logits differ at step {step} (T={T})"
+        for kk, v in fresh.routing(T).items():
+            assert torch.equal(r[kk], v.cpu()), f"{kk} differs at step {step} (T={T})"
+        assert torch.equal(y.cpu().view(torch.int16), y_f.cpu().view(torch.int16)), f"y differs at step {step} (T={T})"
+        fresh.close()
+    layer.close()
