@@ -898,3 +898,28 @@ def test_plan_reuse_long_random_sequence(schedule, flags):
         assert torch.equal(y.cpu().view(torch.int16), y_f.cpu().view(torch.int16)), f"y differs at step {step} (T={T})"
         fresh.close()
     layer.close()
+
+
+@pytest.mark.parametrize("T,schedule,zipf", [(65536, moe.MOE_SCHED_AUTO, 0.0), (131072, moe.MOE_SCHED_AUTO, 1.2),
+                                             (65536, moe.MOE_SCHED_INTERLEAVED, 0.0)])
+def test_many_tokens_routing_and_sampled_y(T, schedule, zipf):
+    """Batches far above the five workloads (65536 and 131072 tokens: 512 and 1024 chunks of 128
+    tokens, half a million and a million routed rows, the skewed one with its hottest expert in
+    every token's top-k): routing of every token bit-exact against the oracle, y on 48 sampled
+    tokens within the stated tolerance."""
+    wl = synth.Workload("many", T, 1024, 256, 64, 8, zipf_s=zipf)
+    bias = _bias(wl)
+    d = synth.device_inputs(wl)
+    layer = _layer(wl, schedule, bias=bias)
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    h = synth.host_inputs(wl, weights=False)
+    lg_ref = oracle.router_logits(h["x"], h["Wr"], bias)
+    tok = sample_tokens(T, 48, seed=3)
+    ref = oracle.forward(h["x"], h["Wr"], bias, lambda e: _device_weights(d)("W1", e),
+                         lambda e: _device_weights(d)("W2", e), wl.k, tokens=tok, logits=lg_ref, bounds=True)
+    check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(T), bias)
+    routing_equal(layer.routing(T), ref, T)
+    check_y(bits(y)[tok], ref, what=f"T={T}")
+    del d
+    layer.close()
+    torch.cuda.empty_cache()
