@@ -292,14 +292,16 @@ def test_plan_reused_across_batches(schedule):
                                        (300, 256, 384, 3, 3), (33, 768, 256, 200, 8),
                                        (77, 64, 64, 5, 2), (200, 320, 192, 12, 3), (129, 384, 320, 40, 4),
                                        (300, 448, 128, 9, 4), (60, 2112, 832, 16, 8),
-                                       (2100, 1024, 128, 5, 2), (9000, 1024, 64, 1, 1), (1200, 2048, 128, 6, 3)])
+                                       (2100, 1024, 128, 5, 2), (9000, 1024, 64, 1, 1), (1200, 2048, 128, 6, 3),
+                                       (2048, 16384, 64, 64, 2), (100, 64, 8192, 8, 2)])
 @pytest.mark.parametrize("flags", [0, EXACT])
 def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
     """Expert counts that are not multiples of 8 / 16 / 32 (tensor-core router N padding,
     transpose tiles, selection keys), one expert, k = E, the smallest H and I the layout allows
     (64), and H = 64, 128, 192 (mod 256) with I = 64 (mod 128) - partial last Linear-1 and
-    Linear-2 tiles and P scale blocks, router rows not a multiple of 256 h: routing and y
-    against the full oracle, default and all-canonical routers.  Which router runs follows the
+    Linear-2 tiles and P scale blocks, router rows not a multiple of 256 h, a long hidden size
+    (H = 16384) and a wide intermediate (I = 8192): routing and y against the full oracle,
+    default and all-canonical routers.  Which router runs follows the
     library's rule (`_router_plan`): the canonical kernels' logits equal the oracle's, the
     tensor-core router's estimates lie within the bound (the last three shapes take it with at
     most 8 experts, above T*H*E = 2^23 and one task per SM)."""
