@@ -35,6 +35,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 256 << 20
 
 
+# idle time before each workload's warm-up: a latency-bound workload timed right after heavy
+# work (input generation, a weight-streaming workload) ran at a power-limited SM clock
+IDLE_BEFORE_S = 0.5
+
+
 def load_traffic(kernel: str, workload: str, schedule: int):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, only while
     the kernel's sources are unchanged since the capture (else None), and a note saying how the
@@ -346,6 +351,8 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     fwd = lambda: layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=logits, y=y)   # noqa: E731
 
+    torch.cuda.synchronize()
+    time.sleep(IDLE_BEFORE_S)                   # the power state the input generation left settles
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         fwd()
