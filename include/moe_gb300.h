@@ -106,8 +106,8 @@ typedef enum {
  *   d = cH * ||x_t||_2 * ||Wr[:,e]||_2 + 2^-20 (|estimate - bias| + |bias|) of the canonical value,
  *   cH from moe_router_bound (at most (H/16 + 1) 2^-17 + (H/32 + 8 + 64) 2^-22).
  * MOE_FLAG_EXACT_LOGITS evaluates every logit in the canonical order on the CUDA cores; so does
- * the default where that measured faster (every logit then canonical): E <= 8 with
- * T * H * E <= 2^23, and batches of at most (number of SMs) tasks of 32 tokens x 8 experts. */
+ * the default where that measured faster (every logit then canonical): batches of at most
+ * (number of SMs) tasks of 32 tokens x 8 experts, i.e. ceil(T/32) * ceil(E/8) <= SMs. */
 #define MOE_FLAG_EXACT_LOGITS (1u << 5)
 /* The whole layer as ONE kernel launch (after the per-forward memset of the expert counts):
  * the MegaMoE design of the X-Stage paper's introduction - one persistent kernel for routing,

@@ -195,21 +195,20 @@ moe_status_t check_forward_args(moe_plan_t p, int32_t T, const void* x, const fl
 
 // Router of a forward with W_router given.  ROUTER_TC: tensor-core estimates + certified
 // canonical selection; ROUTER_CANON_32: canonical logits, 32 tokens x 32 experts per CTA, then
-// top-k; ROUTER_CANON_TASKS: canonical logits by 32-token x 8-expert tasks over every SM (top-k
-// in the same kernel for E <= 8).  Routing is the same whichever runs; the canonical ones write
-// every logit canonical (MOE_FLAG_EXACT_LOGITS asks for one of them).  The rule follows a
-// same-box measurement of each router forced on every shape (router stage, us: tensor-core /
-// 32 x 32 / tasks): T=256 H=512 E=8 16.0 / 16.0 / 15.0 with the 32 x 32 kernel's step fastest
-// (38.1 vs 38.9 us), T=1024 E=8 16.1 / 14.9 / 15.1 (steps 42.8 / 39.5 / 41.2), T=4096 H=1024
-// E=8 21.5 / 23.1 / 19.1; H=2048 E=128: T=64 24.2 / 28.3 / 21.1, T=256 26.2 / 29.3 / 22.6,
-// T=512 26.6 / 29.3 / 28.0, T=1024 28.3 / 29.8 / 43.6; H=7168 E=256: T=32 48.8 / 71.5 / 44.0,
-// T=128 53.0 / 72.8 / 44.5, T=256 47.6 / 73.0 / 61.5, T=512 46.8 / 73.4 / 109.1.  So: the
-// 32 x 32 kernel for small layers with at most 8 experts, the tasks while there are at most as
-// many as SMs, the tensor-core router above (or the 32 x 32 kernel when all logits must be
-// canonical).
+// top-k; ROUTER_CANON_TASKS: canonical logits by tasks of 32, 16 or 8 tokens x 8 experts over
+// every SM (top-k in the same kernel for E <= 8).  Routing is the same whichever runs; the
+// canonical ones write every logit canonical (MOE_FLAG_EXACT_LOGITS asks for one of them).  The
+// rule follows a same-box measurement of each router forced on every shape (router stage, us:
+// tensor-core / 32 x 32 / tasks): T=256 H=512 E=8 16.0 / 14.0 / 11.7 (steps 40.2 / 37.9 / 34.2),
+// T=1024 E=8 16.1 / 16.0 / 13.7 (steps 42.8 / 40.2 / 37.7), T=4096 H=1024 E=8 21.5 / 22.1 / 17.9;
+// H=2048 E=128: T=64 24.2 / 29.5 / 19.9, T=256 26.2 / 29.5 / 22.4, T=512 26.6 / 29.3 / 28.0,
+// T=1024 28.3 / 29.8 / 43.6; H=7168 E=256: T=32 48.8 / 71.3 / 32.4, T=128 53.0 / 72.7 / 44.4,
+// T=256 47.6 / 73.0 / 61.5, T=512 46.8 / 73.4 / 109.1.  So: the tasks while 32-token tasks
+// would fit one per SM, the tensor-core router above (or the 32 x 32 kernel when all logits
+// must be canonical).
 enum { ROUTER_TC = 0, ROUTER_CANON_32 = 1, ROUTER_CANON_TASKS = 2 };
 int router_choice(uint32_t flags, int T, int H, int E, int sms) {
-  if (E <= 8 && (int64_t)T * H * E <= (1ll << 23)) return ROUTER_CANON_32;
+  (void)H;
   if (router_tasks(T, E) <= sms) return ROUTER_CANON_TASKS;
   return (flags & MOE_FLAG_EXACT_LOGITS) ? ROUTER_CANON_32 : ROUTER_TC;
 }

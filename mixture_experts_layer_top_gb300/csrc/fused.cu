@@ -55,6 +55,7 @@ struct FusedArgs {
   int workers, mode, wave_experts, lead, dead_row, test_bad_id;
   int64_t timeout_ns;
   int trace_ctas;   // CTAs whose counters precede the phase stamps in the trace buffer
+  int rtok;         // tokens per router task: 32, 16 or 8 (router_task_tokens)
   GemmArgs ga;
 };
 
@@ -135,21 +136,24 @@ __device__ __forceinline__ void fr_cp16(uint16_t* dst, const uint16_t* src, bool
 }
 
 // with_topk (one expert group, E <= FR_EXP): the CTA that wrote a task's logits - every expert
-// of its 32 tokens - selects those tokens' experts right away (a CTA barrier orders the writes).
+// of its tokens - selects those tokens' experts right away (a CTA barrier orders the writes).
+// A task holds a.rtok tokens (32, 16 or 8: fewer when the batch would leave SMs without a task),
+// one compute warp per 4 of them; every logit's fused multiply-adds are the same either way.
 __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int warp, bool with_topk) {
   float* lg = reinterpret_cast<float*>(rs + FR_NS * FR_STAGE);   // [FR_TOK][FR_EXP] logits (with_topk)
-  const int nT = (a.T + FR_TOK - 1) / FR_TOK, nE = (a.E + FR_EXP - 1) / FR_EXP;
+  const int rtok = a.rtok;
+  const int nT = (a.T + rtok - 1) / rtok, nE = (a.E + FR_EXP - 1) / FR_EXP;
   const bool wvec = (a.E % FR_EXP) == 0;     // 16-byte rows of W_router (else element copies)
   // the last chunk of an H that is not a multiple of FR_HC holds zeros past H (a fused
   // multiply-add of 0 * 0 leaves a partial sum unchanged: the canonical value is the same)
   const int nchunk = (a.H + FR_HC - 1) / FR_HC;
   for (int task = blockIdx.x; task < nT * nE; task += gridDim.x) {
-    const int t0 = (task / nE) * FR_TOK, e0 = (task % nE) * FR_EXP;
+    const int t0 = (task / nE) * rtok, e0 = (task % nE) * FR_EXP;
     auto issue = [&](int c) {
       uint16_t* xs = rs + (c % FR_NS) * FR_STAGE;
       uint16_t* ws = xs + FR_STAGE_X;
       const int h0 = c * FR_HC;
-      for (int q = threadIdx.x; q < FR_TOK * (FR_HC / 8); q += GEMM_THREADS) {   // x: 16-byte pieces
+      for (int q = threadIdx.x; q < rtok * (FR_HC / 8); q += GEMM_THREADS) {     // x: 16-byte pieces
         const int tok = q / (FR_HC / 8), pc = q % (FR_HC / 8);
         const bool ok = t0 + tok < a.T && h0 + pc * 8 < a.H;
         fr_cp16(xs + tok * FR_XROW + pc * 8, ok ? a.x + (size_t)(t0 + tok) * a.H + h0 + pc * 8 : a.x, ok);
@@ -180,7 +184,7 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
       asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group %0;" ::"n"(FR_NS - 1) : "memory");
       __syncthreads();
-      if (warp < FR_CWARPS) {
+      if (warp < rtok / 4) {
         const uint16_t* xs = rs + (c % FR_NS) * FR_STAGE + (warp * 4) * FR_XROW;
         const uint16_t* ws = rs + (c % FR_NS) * FR_STAGE + FR_STAGE_X;
 #pragma unroll
@@ -205,7 +209,7 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
       __syncthreads();                         // the stage is refilled next round
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (warp < FR_CWARPS) {
+    if (warp < rtok / 4) {
       float mine = 0.0f;
 #pragma unroll
       for (int ti = 0; ti < 4; ++ti)
@@ -225,7 +229,7 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
     }
     __syncthreads();                           // the ring is reused by the next task
     if (with_topk) {
-      for (int tt = warp; tt < FR_TOK && t0 + tt < a.T; tt += FZ_WARPS) topk_token(a, t0 + tt, lg + tt * FR_EXP, lane);
+      for (int tt = warp; tt < rtok && t0 + tt < a.T; tt += FZ_WARPS) topk_token(a, t0 + tt, lg + tt * FR_EXP, lane);
       __syncthreads();                         // lg is rewritten by the next task
     }
   }
@@ -327,6 +331,15 @@ cudaError_t router_tasks_prepare() {
 
 int router_tasks(int T, int E) { return ((T + FR_TOK - 1) / FR_TOK) * ((E + FR_EXP - 1) / FR_EXP); }
 
+// Tokens per router task: the largest of 32, 16, 8 that still gives `ctas` tasks (so that a
+// small batch spreads over the grid), else 8.
+int router_task_tokens(int T, int E, int ctas) {
+  const int nE = (E + FR_EXP - 1) / FR_EXP;
+  for (int tpt = FR_TOK; tpt > 8; tpt /= 2)
+    if ((int64_t)((T + tpt - 1) / tpt) * nE >= ctas) return tpt;
+  return 8;
+}
+
 cudaError_t launch_router_tasks(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits,
                                 const Workspace& ws, int T, int H, int E, int k, int num_sms, bool* topk_done,
                                 cudaStream_t st) {
@@ -341,7 +354,9 @@ cudaError_t launch_router_tasks(const uint16_t* x, const uint16_t* Wr, const flo
   a.E = E;
   a.k = k;
   *topk_done = E <= FR_EXP;
-  const int tasks = router_tasks(T, E), cap = 2 * num_sms;   // two resident CTAs per SM
+  a.rtok = router_task_tokens(T, E, num_sms);
+  const int tasks = ((T + a.rtok - 1) / a.rtok) * ((E + FR_EXP - 1) / FR_EXP);
+  const int cap = 2 * num_sms;   // two resident CTAs per SM
   return launch_pdl(router_tasks_kernel, dim3((unsigned)(tasks < cap ? tasks : cap)), dim3(GEMM_THREADS),
                     (size_t)FR_SMEM, st, a);
 }
@@ -399,6 +414,7 @@ cudaError_t launch_fused_layer(const CUtensorMap& tA1, const CUtensorMap& tB1, c
   a.test_bad_id = test_bad_id ? 1 : 0;
   a.timeout_ns = ga.timeout_ns;
   a.trace_ctas = trace_ctas;
+  a.rtok = router_task_tokens(T, E, grid);
   a.ga = ga;
   (void)I;
   using L = Layout<6, 1>;

@@ -150,9 +150,10 @@ cudaError_t gemm_prepare(int device, int* grid);   // grid: CTAs of the co-resid
 cudaError_t launch_grouped_gemm(const CUtensorMap& tA1, const CUtensorMap& tB1, const CUtensorMap& tA2,
                                 const CUtensorMap& tB2, const CUtensorMap& tH, const CUtensorMap& tP,
                                 const GemmArgs& a, int grid, bool streaming, cudaStream_t st);
-// Canonical router logits by tasks of 32 tokens x 8 experts, one CTA each (fused.cu, the single
-// launch's router phase as a kernel of its own); with E <= 8 the same CTAs also select the top-k
-// (*topk_done = true), else the caller runs launch_topk.
+// Canonical router logits by tasks of 32, 16 or 8 tokens x 8 experts, one CTA each (fused.cu,
+// the single launch's router phase as a kernel of its own); with E <= 8 the same CTAs also select
+// the top-k (*topk_done = true), else the caller runs launch_topk.  router_tasks: the number of
+// 32-token tasks (the router rule's measure of batch size).
 cudaError_t router_tasks_prepare();
 int router_tasks(int T, int E);
 cudaError_t launch_router_tasks(const uint16_t* x, const uint16_t* Wr, const float* bias, float* logits,

@@ -34,12 +34,10 @@ def _layer(wl, schedule=0, flags=0, T_max=None, timeout_ns=0, wave_experts=0, le
 
 def _router_plan(T, H, E, exact=False):
     """(router launches, every logit canonical) of a forward under the library's router rule:
-    the 32 x 32 canonical kernel + top-k for E <= 8 with T*H*E <= 2^23, the 32-token x 8-expert
-    task kernel (+ top-k unless E <= 8) while the tasks fit one per SM, else the tensor-core
-    estimate + transpose + certified selection (or the 32 x 32 kernel + top-k under EXACT)."""
+    the canonical task kernel (+ top-k unless E <= 8) while 32-token x 8-expert tasks fit one per
+    SM, else the tensor-core estimate + transpose + certified selection (or the 32 x 32
+    canonical kernel + top-k under EXACT)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if E <= 8 and T * H * E <= 2 ** 23:
-        return 2, True
     if -(-T // 32) * -(-E // 8) <= sms:
         return (1 if E <= 8 else 2), True
     return (2, True) if exact else (3, False)
@@ -60,8 +58,9 @@ def test_device_generator_matches_host():
 # --------------------------------------------------------------------------- tiny config
 @pytest.mark.parametrize("schedule,flags", [(0, 0), (1, 0), (2, 0), (0, EXACT), (2, EXACT)])
 def test_tiny_full_parity(schedule, flags):
-    """Whole layer on the 256-token config, every schedule.  With 8 experts the default router is
-    the all-canonical one (2 launches, as with MOE_FLAG_EXACT_LOGITS): logits bit-exact either way."""
+    """Whole layer on the 256-token config, every schedule.  The default router is the canonical
+    task kernel here, with the top-k in the same launch (as with MOE_FLAG_EXACT_LOGITS): logits
+    bit-exact either way."""
     wl = synth.WORKLOADS["tiny"]
     h = synth.host_inputs(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
@@ -71,7 +70,7 @@ def test_tiny_full_parity(schedule, flags):
     assert np.array_equal(logits.cpu().numpy(), ref["logits"]), "logits not bit-exact"
     routing_equal(layer.routing(wl.T), ref, wl.T)
     check_y(bits(y), ref)
-    assert layer.launch_count() == 2 + (5 if schedule == 2 else 4)
+    assert layer.launch_count() == _router_plan(wl.T, wl.H, wl.E, bool(flags & EXACT))[0] + (5 if schedule == 2 else 4)
 
 
 def test_bilinear_integer_exact():
@@ -292,7 +291,8 @@ def test_plan_reused_across_batches(schedule):
                                        (300, 256, 384, 3, 3), (33, 768, 256, 200, 8),
                                        (77, 64, 64, 5, 2), (200, 320, 192, 12, 3), (129, 384, 320, 40, 4),
                                        (300, 448, 128, 9, 4), (60, 2112, 832, 16, 8),
-                                       (2100, 1024, 128, 5, 2), (9000, 1024, 64, 1, 1), (1200, 2048, 128, 6, 3),
+                                       (5000, 256, 64, 5, 2), (9000, 1024, 64, 1, 1), (6000, 512, 64, 6, 3),
+                                       (1200, 2048, 128, 6, 3),
                                        (2048, 16384, 64, 64, 2), (100, 64, 8192, 8, 2)])
 @pytest.mark.parametrize("flags", [0, EXACT])
 def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
@@ -301,10 +301,10 @@ def test_odd_shapes_full_oracle(T, H, I, E, k, flags):
     (64), and H = 64, 128, 192 (mod 256) with I = 64 (mod 128) - partial last Linear-1 and
     Linear-2 tiles and P scale blocks, router rows not a multiple of 256 h, a long hidden size
     (H = 16384) and a wide intermediate (I = 8192): routing and y against the full oracle,
-    default and all-canonical routers.  Which router runs follows the
-    library's rule (`_router_plan`): the canonical kernels' logits equal the oracle's, the
-    tensor-core router's estimates lie within the bound (the last three shapes take it with at
-    most 8 experts, above T*H*E = 2^23 and one task per SM)."""
+    default and all-canonical routers.  Which router runs follows the library's rule
+    (`_router_plan`): the canonical kernels' logits equal the oracle's, the tensor-core
+    router's estimates lie within the bound (shapes with more 32 x 8 tasks than SMs, among them
+    ones with at most 8 experts)."""
     wl = synth.Workload("odd", T, H, I, E, k)
     h = synth.host_inputs(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], None, None, full_weights=(h["W1"], h["W2"]))
