@@ -207,8 +207,7 @@ moe_status_t check_forward_args(moe_plan_t p, int32_t T, const void* x, const fl
 // would fit one per SM, the tensor-core router above (or the 32 x 32 kernel when all logits
 // must be canonical).
 enum { ROUTER_TC = 0, ROUTER_CANON_32 = 1, ROUTER_CANON_TASKS = 2 };
-int router_choice(uint32_t flags, int T, int H, int E, int sms) {
-  (void)H;
+int router_choice(uint32_t flags, int T, int E, int sms) {
   if (router_tasks(T, E) <= sms) return ROUTER_CANON_TASKS;
   return (flags & MOE_FLAG_EXACT_LOGITS) ? ROUTER_CANON_32 : ROUTER_TC;
 }
@@ -310,7 +309,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     p->last_launches = nl;
     return MOE_OK;
   }
-  const int rchoice = W_router ? router_choice(c.flags, T, H, E, p->num_sms) : ROUTER_CANON_32;
+  const int rchoice = W_router ? router_choice(c.flags, T, E, p->num_sms) : ROUTER_CANON_32;
   const bool tc_router = rchoice == ROUTER_TC;
   if (x_src && !tc_router) {   // whole copy first
     MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
