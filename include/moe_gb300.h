@@ -179,9 +179,11 @@ MOE_API moe_status_t moe_forward(moe_plan_t plan, int32_t T, const void* x, floa
  * plan-owned device buffer, the layer runs, and y (bf16 [T, H]) lands in y_host, all enqueued
  * on `stream`.  A page-locked buffer that is mapped into the device's address space (any
  * cudaHostAlloc / cudaMallocHost buffer under unified addressing) at a 16-byte-aligned address
- * is reached by the kernels directly: a copy kernel reads x_host, and Combine stores y into
- * y_host in place.  Any other buffer goes through cudaMemcpyAsync and a plan-owned staging
- * buffer (synchronous for pageable memory).  router_logits, W_router, W1_gate_up and W2 are
+ * is copied into the plan's buffer by the copy engines in token ranges, each routed as it
+ * lands (the copy waits only for the previous host-buffer forward's last read of that buffer, so
+ * it can run beside that forward's later kernels), and Combine stores y into y_host in place.
+ * Any other buffer goes through cudaMemcpyAsync and plan-owned staging buffers (synchronous for
+ * pageable memory).  router_logits, W_router, W1_gate_up and W2 are
  * DEVICE pointers exactly as in moe_forward.  The caller must not touch y_host before the
  * stream reaches this point (e.g. cudaStreamSynchronize), and must not write x_host before then. */
 MOE_API moe_status_t moe_forward_host(moe_plan_t plan, int32_t T, const void* x_host, float* router_logits,

@@ -36,7 +36,7 @@ struct moe_plan_s {
   // moe_forward_host: x streams in from page-locked host memory on st_aux in HOST_RANGES
   // token ranges, each routed as soon as it has landed
   cudaStream_t st_aux;
-  cudaEvent_t ev_fork;
+  cudaEvent_t ev_xfree;   // recorded on st after the last kernel that reads x_stage (host-buffer forwards)
   cudaEvent_t ev_range[4];
   int last_launches;
   unsigned long long* trace;   // [max(gemm_grid, fused_grid) + 1][TRACE_SLOTS] when MOE_FLAG_TRACE
@@ -55,7 +55,7 @@ void release(moe_plan_s* p) {
       if (p->ev[i]) cudaEventDestroy(p->ev[i]);
   for (int r = 0; r < HOST_RANGES; ++r)
     if (p->ev_range[r]) cudaEventDestroy(p->ev_range[r]);
-  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_xfree) cudaEventDestroy(p->ev_xfree);
   if (p->st_aux) cudaStreamDestroy(p->st_aux);
   if (p->base) cudaFree(p->base);
   if (p->bias) cudaFree(p->bias);
@@ -254,8 +254,19 @@ GemmArgs gemm_args(const moe_plan_s* p) {
 
 // One forward, enqueued on st.  x_src, when not null, is page-locked host memory mapped into
 // the device's address space: the layer's input is copied from it into x (the plan's staging
-// buffer) inside this call, in HOST_RANGES token ranges on st_aux, and the tensor-core router
-// starts on each range as soon as it has landed.
+// buffer) inside this call by the copy engines, on st_aux - in HOST_RANGES token ranges when the
+// tensor-core router runs, which starts on each range as soon as it has landed, else whole.  A
+// copy into the staging buffer waits only for ev_xfree: the previous host-buffer forward's last
+// kernel that reads it (its gather, or its single launch), so it runs beside that forward's
+// later kernels (the copy engines need no SM; an SM copy kernel measured slower there).
+cudaError_t stage_whole_input(moe_plan_t p, const void* x_src, size_t bytes, cudaStream_t st) {
+  cudaError_t e = cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(p->x_stage, x_src, bytes, cudaMemcpyDefault, p->st_aux);
+  if (e == cudaSuccess) e = cudaEventRecord(p->ev_range[0], p->st_aux);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, p->ev_range[0], 0);
+  return e;
+}
+
 moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_src, float* router_logits,
                           const void* W_router, const void* W1, const void* W2, void* y, cudaStream_t st) {
   const moe_config_t& c = p->cfg;
@@ -278,10 +289,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   // grid-barrier word, counts and chist (one contiguous range)
   MOE_CK(cudaMemsetAsync(p->ws.gbar, 0, 16 + sizeof(int32_t) * E * (1 + chunks), st));
   if (c.flags & MOE_FLAG_SINGLE_LAUNCH) {
-    if (x_src) {   // the input lands whole before the one launch
-      MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
-      ++nl;
-    }
+    if (x_src) MOE_CK(stage_whole_input(p, x_src, (size_t)T * H * 2, st));   // the input lands whole first
     rec(1);
     rec(2);
     rec(3);
@@ -304,6 +312,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
                               c.lead_waves, (int)p->R_pad_max, (c.flags & MOE_FLAG_TEST_BAD_ID) != 0, ga,
                               trace_ctas(p), st));
     ++nl;
+    if (x == p->x_stage) MOE_CK(cudaEventRecord(p->ev_xfree, st));   // x_stage free for the next upload
     rec(4);
     rec(5);
     p->last_launches = nl;
@@ -311,10 +320,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   }
   const int rchoice = W_router ? router_choice(c.flags, T, E, p->num_sms) : ROUTER_CANON_32;
   const bool tc_router = rchoice == ROUTER_TC;
-  if (x_src && !tc_router) {   // whole copy first
-    MOE_CK(launch_stage_copy(x_src, p->x_stage, (size_t)T * H * 2, p->num_sms, st));
-    ++nl;
-  }
+  if (x_src && !tc_router) MOE_CK(stage_whole_input(p, x_src, (size_t)T * H * 2, st));   // whole copy first
   if (tc_router) {
     // split plan of the whole forward, whatever the ranges: the same logits either way
     const RouterSplit sp = router_split(T, H, E, p->num_sms);
@@ -328,14 +334,12 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     const int nr = x_src ? std::min(HOST_RANGES, chunks) : 1;
     const int per = ((chunks + nr - 1) / nr) * DS_CHUNK_TOK;
     if (x_src) {
-      MOE_CK(cudaEventRecord(p->ev_fork, st));   // the previous forward no longer reads x_stage
-      MOE_CK(cudaStreamWaitEvent(p->st_aux, p->ev_fork, 0));
+      MOE_CK(cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0));   // the previous forward's gather is done
       for (int r = 0; r * per < T; ++r) {
         const size_t off = (size_t)r * per * H * 2, n = (size_t)std::min(per, T - r * per) * H * 2;
-        MOE_CK(launch_stage_copy(static_cast<const char*>(x_src) + off, static_cast<char*>(p->x_stage) + off, n,
-                                 p->num_sms, p->st_aux));
+        MOE_CK(cudaMemcpyAsync(static_cast<char*>(p->x_stage) + off, static_cast<const char*>(x_src) + off, n,
+                               cudaMemcpyDefault, p->st_aux));
         MOE_CK(cudaEventRecord(p->ev_range[r], p->st_aux));
-        ++nl;
       }
     }
     MOE_CK(launch_router_prep(static_cast<const uint16_t*>(W_router), H, E, p->rw, st));
@@ -380,6 +384,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   ++nl;
   rec(2);
   MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.prow_of, T, H, k, p->ws.x_pad, st));
+  if (x == p->x_stage) MOE_CK(cudaEventRecord(p->ev_xfree, st));   // x_stage free for the next upload
   ++nl;
   rec(3);
   CUtensorMap tA1, tB1, tA2, tB2, tH, tP;
@@ -539,7 +544,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
     for (int i = 0; i <= MOE_NUM_STAGES; ++i)
       if (cudaEventCreate(&p->ev[i]) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&p->st_aux, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess)
+      cudaEventCreateWithFlags(&p->ev_xfree, cudaEventDisableTiming) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   for (int r = 0; r < HOST_RANGES; ++r)
     if (cudaEventCreateWithFlags(&p->ev_range[r], cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -558,9 +563,9 @@ moe_status_t moe_forward(moe_plan_t p, int32_t T, const void* x, float* router_l
 moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float* router_logits,
                               const void* W_router, const void* W1, const void* W2, void* y_host, void* stream) {
   if (!p || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
-  // Page-locked buffers are reached from the kernels directly: x streams in through copy
-  // kernels (overlapping the router), Combine writes y in place.  Pageable ones go through
-  // the copy engines and the staging buffers.
+  // Page-locked buffers: x streams in by the copy engines in token ranges (overlapping the
+  // router, and the previous forward's later kernels), Combine writes y in place.  Pageable
+  // ones go through the copy engines and the staging buffers whole.
   const void* x_dev = mapped_host(x_host);
   void* y_dev = mapped_host(y_host);
   void* y = y_dev ? y_dev : p->y_stage;
@@ -572,8 +577,12 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)T * p->cfg.H * 2;
-  if (!x_dev && cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (!x_dev) {   // pageable: the copy engines, on st_aux once x_stage is free (as stage_whole_input)
+    if (cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0) != cudaSuccess ||
+        cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, p->st_aux) != cudaSuccess ||
+        cudaEventRecord(p->ev_range[0], p->st_aux) != cudaSuccess || cudaStreamWaitEvent(st, p->ev_range[0], 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   const moe_status_t s = forward_impl(p, T, p->x_stage, x_dev, router_logits, W_router, W1, W2, y, st);
   if (s != MOE_OK) return s;
   if (!y_dev && cudaMemcpyAsync(y_host, p->y_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)

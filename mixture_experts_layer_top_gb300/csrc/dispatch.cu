@@ -70,38 +70,7 @@ compact_intermediates_kernel(const int32_t* __restrict__ row_pair, const int32_t
       P[(size_t)f * H + c] = __half2float(__ushort_as_half(P_pad[pr * H + c])) * S_pad[pr * p_scale_blocks(H) + c / P_SCALE_COLS];
 }
 
-// Token block from page-locked host memory (mapped into this device's address space)
-// into the device staging buffer, pulled by the SMs with 16-byte loads, four in flight
-// per thread.  The CPU-GPU link, not the SMs, is the limit: 16 blocks of 512 threads
-// reach its rate (measured 203 GB/s, as for 152 blocks), which leaves the other SMs
-// to the router running beside the copy.
-constexpr int SC_BLOCKS = 16;
-__global__ void __launch_bounds__(512)
-stage_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
-  ptx::grid_dep_wait();   // the previous forward no longer reads dst from here on
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n; i += 4 * stride) {
-    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
-    dst[i] = a;
-    dst[i + stride] = b;
-    dst[i + 2 * stride] = c;
-    dst[i + 3 * stride] = d;
-  }
-  for (; i < n; i += stride) dst[i] = src[i];
-}
-
 }  // namespace
-
-cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st) {
-  const int64_t n = (int64_t)(bytes / 16);
-  int64_t blocks = (n + 511) / 512;
-  const int64_t cap = num_sms < SC_BLOCKS ? num_sms : SC_BLOCKS;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return launch_pdl(stage_copy_kernel, dim3((unsigned)blocks), dim3(512), 0, st, static_cast<const uint4*>(src),
-                    static_cast<uint4*>(dst), n);
-}
 
 cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int I, int num_sms, int mode,
                             int wave_experts, int lead, int dead_row, bool test_bad_id, cudaStream_t st) {

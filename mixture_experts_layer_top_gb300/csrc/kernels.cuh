@@ -139,8 +139,6 @@ cudaError_t launch_dispatch(const Workspace& ws, int T, int E, int k, int H, int
                             int wave_experts, int lead, int dead_row, bool test_bad_id, cudaStream_t st);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* prow_of, int T, int H, int k, uint16_t* x_pad,
                           cudaStream_t st);
-// bytes a multiple of 16, both pointers 16-byte aligned; src may be mapped host memory.
-cudaError_t launch_stage_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st);
 cudaError_t launch_compact_intermediates(const int32_t* row_pair, const int32_t* prow_of, int R, int R_pad, int H,
                                          int I,
                                          const uint16_t* h_pad, const uint16_t* P_pad, const float* S_pad,
