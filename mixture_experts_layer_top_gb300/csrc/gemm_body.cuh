@@ -23,9 +23,8 @@ constexpr int STG_BOX_BYTES = BM * 128;                // 128 staged rows x 128 
 constexpr int ST_ROWS = 32;                            // rows per output store box (one TMEM quadrant)
 constexpr int ST_BOX_BYTES = ST_ROWS * 128;            // 4 KB
 constexpr int STG_BYTES = 2 * STG_BOX_BYTES;           // one staging buffer: two boxes (the two column halves)
-// mbarriers and flags (SmemCtl, 152 bytes); kept small so that with the 1 KB the GPU reserves per
-// block a 256-thread block without shared memory still fits beside a CTA on its SM (the next
-// host-buffer forward's input copy runs beside this kernel)
+// mbarriers and flags (SmemCtl, 152 bytes), with room to spare: with the 1 KB the GPU reserves
+// per block, a small block without shared memory still fits beside a CTA of this kernel
 constexpr int CTL_BYTES = 512;
 // Shared-memory layout of a <NST stages, NBUF staging buffers> instance.
 template <int NST, int NBUF>
