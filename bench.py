@@ -380,28 +380,34 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     ms_per_step = reduce_max(sum(a.elapsed_time(b) for a, b in ev), group) / args.steps
 
     # ---- e2e: the host-buffer C-ABI call, copies inside the timed region
+    # (MOE_FLAG_HOST_PIPELINE: x_host is written once, on the host, before the steps, so each
+    # step's upload may run beside the previous step's GEMM)
     e2e = None
     if with_e2e:
+        layer_h = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags | moe.MOE_FLAG_HOST_PIPELINE,
+                                             **cfg), local, router_bias=bias)
         x_host = d["x"].cpu().pin_memory()
         y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
         for _ in range(2):
             flush.zero_()
-            layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
+            layer_h.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
         torch.cuda.synchronize()
         eev = _events(args.steps)
         for i in range(args.steps):
             flush.zero_()
             eev[i][0].record()
-            layer.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
+            layer_h.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
             eev[i][1].record()
         torch.cuda.synchronize()
-        layer.check()
+        layer_h.check()
+        layer_h.close()
         if not torch.equal(y_host.view(torch.int16), y.cpu().view(torch.int16)):
             raise RuntimeError("host-buffer forward disagrees with the device-buffer forward")
         e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in eev), group) / args.steps
         e2e = {"value": ws * wl.useful_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
-               "ms_per_step": e_ms, "tokens_per_s": ws * wl.T / (e_ms * 1e-3)}
+               "ms_per_step": e_ms, "tokens_per_s": ws * wl.T / (e_ms * 1e-3),
+               "host_pipeline": True}
     layer.close()
     # ---- per-stage breakdown on a second plan whose library records events between stages
     # (those events serialise the stream, so the timed steps above run without them)

@@ -122,6 +122,14 @@ typedef enum {
  * ignored (the default ring split); with MOE_FLAG_STAGE_TIMING the whole launch is reported
  * as stage 3 (the grouped GEMM) and the other stages as 0. */
 #define MOE_FLAG_SINGLE_LAUNCH (1u << 6)
+/* moe_forward_host only (library plumbing: no counterpart in the paper).  Default: the input
+ * upload waits for all work enqueued on the stream before the call, like any stream-ordered
+ * operation.  With this flag it waits only until the previous moe_forward_host of this plan no
+ * longer reads the plan's input buffer (its gather), so back-to-back host forwards upload the
+ * next input while the previous one is still computing.  The caller then must have written
+ * x_host on the host before the call: a write of x_host by work enqueued on the stream between
+ * two such calls (a device-to-host copy, a host callback) is not waited for. */
+#define MOE_FLAG_HOST_PIPELINE (1u << 7)
 #define MOE_FLAG_TEST_BAD_ID (1u << 9)  /* test only: Dispatch sees the first (token, slot) pair's expert
                                           id out of range; the pair is dropped, no access leaves the
                                           workspace, and moe_get_status reports MOE_ERR_DEVICE_CHECK */

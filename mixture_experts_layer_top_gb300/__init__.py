@@ -41,6 +41,7 @@ MOE_FLAG_GEMM_STREAMING = 1 << 3
 MOE_FLAG_GEMM_COMPUTE = 1 << 4
 MOE_FLAG_EXACT_LOGITS = 1 << 5
 MOE_FLAG_SINGLE_LAUNCH = 1 << 6
+MOE_FLAG_HOST_PIPELINE = 1 << 7
 TRACE_FIELDS = ("prod_wait_empty_ns", "prod_wait_ready_ns", "mma_wait_tempty_ns", "mma_wait_full_ns",
                 "epi_wait_tfull_ns", "cta_ns", "tiles_l1", "tiles_l2")
 MOE_FLAG_TEST_STALL = 1 << 8

@@ -36,6 +36,7 @@ struct moe_plan_s {
   // moe_forward_host: x streams in from page-locked host memory on st_aux in HOST_RANGES
   // token ranges, each routed as soon as it has landed
   cudaStream_t st_aux;
+  cudaEvent_t ev_fork;    // recorded on st at the start of a host-buffer forward (strict stream order)
   cudaEvent_t ev_xfree;   // recorded on st after the last kernel that reads x_stage (host-buffer forwards)
   cudaEvent_t ev_range[4];
   int last_launches;
@@ -56,6 +57,7 @@ void release(moe_plan_s* p) {
   for (int r = 0; r < HOST_RANGES; ++r)
     if (p->ev_range[r]) cudaEventDestroy(p->ev_range[r]);
   if (p->ev_xfree) cudaEventDestroy(p->ev_xfree);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->st_aux) cudaStreamDestroy(p->st_aux);
   if (p->base) cudaFree(p->base);
   if (p->bias) cudaFree(p->bias);
@@ -256,11 +258,18 @@ GemmArgs gemm_args(const moe_plan_s* p) {
 // the device's address space: the layer's input is copied from it into x (the plan's staging
 // buffer) inside this call by the copy engines, on st_aux - in HOST_RANGES token ranges when the
 // tensor-core router runs, which starts on each range as soon as it has landed, else whole.  A
-// copy into the staging buffer waits only for ev_xfree: the previous host-buffer forward's last
-// kernel that reads it (its gather, or its single launch), so it runs beside that forward's
-// later kernels (the copy engines need no SM; an SM copy kernel measured slower there).
+// copy into the staging buffer waits for all work enqueued on st before the call, or with
+// MOE_FLAG_HOST_PIPELINE only for ev_xfree: the previous host-buffer forward's last kernel that
+// reads it (its gather, or its single launch), so it runs beside that forward's later kernels
+// (the copy engines need no SM; an SM copy kernel measured slower there).
+cudaError_t wait_staging_free(moe_plan_t p, cudaStream_t st) {
+  if (p->cfg.flags & MOE_FLAG_HOST_PIPELINE) return cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0);
+  cudaError_t e = cudaEventRecord(p->ev_fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->st_aux, p->ev_fork, 0);
+  return e;
+}
 cudaError_t stage_whole_input(moe_plan_t p, const void* x_src, size_t bytes, cudaStream_t st) {
-  cudaError_t e = cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0);
+  cudaError_t e = wait_staging_free(p, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->x_stage, x_src, bytes, cudaMemcpyDefault, p->st_aux);
   if (e == cudaSuccess) e = cudaEventRecord(p->ev_range[0], p->st_aux);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, p->ev_range[0], 0);
@@ -334,7 +343,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     const int nr = x_src ? std::min(HOST_RANGES, chunks) : 1;
     const int per = ((chunks + nr - 1) / nr) * DS_CHUNK_TOK;
     if (x_src) {
-      MOE_CK(cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0));   // the previous forward's gather is done
+      MOE_CK(wait_staging_free(p, st));
       for (int r = 0; r * per < T; ++r) {
         const size_t off = (size_t)r * per * H * 2, n = (size_t)std::min(per, T - r * per) * H * 2;
         MOE_CK(cudaMemcpyAsync(static_cast<char*>(p->x_stage) + off, static_cast<const char*>(x_src) + off, n,
@@ -544,7 +553,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
     for (int i = 0; i <= MOE_NUM_STAGES; ++i)
       if (cudaEventCreate(&p->ev[i]) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&p->st_aux, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&p->ev_xfree, cudaEventDisableTiming) != cudaSuccess)
+      cudaEventCreateWithFlags(&p->ev_xfree, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   for (int r = 0; r < HOST_RANGES; ++r)
     if (cudaEventCreateWithFlags(&p->ev_range[r], cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -578,7 +588,7 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)T * p->cfg.H * 2;
   if (!x_dev) {   // pageable: the copy engines, on st_aux once x_stage is free (as stage_whole_input)
-    if (cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0) != cudaSuccess ||
+    if (wait_staging_free(p, st) != cudaSuccess ||
         cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, p->st_aux) != cudaSuccess ||
         cudaEventRecord(p->ev_range[0], p->st_aux) != cudaSuccess || cudaStreamWaitEvent(st, p->ev_range[0], 0) != cudaSuccess)
       return MOE_ERR_CUDA;

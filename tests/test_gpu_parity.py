@@ -926,3 +926,47 @@ def test_many_tokens_routing_and_sampled_y(T, schedule, zipf):
     del d
     layer.close()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T,pin", [(1000, True), (100, True), (1000, False)])
+def test_host_forward_waits_for_stream_ordered_input(T, pin):
+    """By default moe_forward_host is stream-ordered like any other operation: an x_host written
+    by a device-to-host copy enqueued on the stream just before the call is the input the forward
+    sees (tensor-core router in ranges, the canonical task router, pageable staging)."""
+    wl = synth.Workload("strict", T, 1024, 256, 64, 4)
+    w = synth.device_inputs(wl)
+    xb = synth.device_inputs(synth.Workload("strict", T, 1024, 256, 64, 4, seed=9))["x"]
+    layer = _layer(wl)
+    y_a, _ = layer.forward(w["x"], w["Wr"], w["W1"], w["W2"], check=True)
+    y_b, _ = layer.forward(xb, w["Wr"], w["W1"], w["W2"], check=True)
+    x_host = torch.empty((T, wl.H), dtype=torch.bfloat16, pin_memory=pin)
+    y_host = torch.empty((T, wl.H), dtype=torch.bfloat16, pin_memory=pin)
+    lg = torch.empty((T, wl.E), dtype=torch.float32, device="cuda")
+    x_host.copy_(w["x"].cpu())
+    layer.forward_host(x_host, w["Wr"], w["W1"], w["W2"], lg, y_host)
+    x_host.copy_(xb, non_blocking=pin)          # stream-ordered write of the next input
+    layer.forward_host(x_host, w["Wr"], w["W1"], w["W2"], lg, y_host, check=True)
+    assert torch.equal(y_host.view(torch.int16), y_b.cpu().view(torch.int16)), "the forward read a stale x_host"
+    layer.close()
+
+
+def test_host_pipeline_back_to_back():
+    """MOE_FLAG_HOST_PIPELINE: back-to-back host forwards with no synchronisation between them,
+    alternating two page-locked inputs written on the host beforehand, each with its own output:
+    every y bitwise equal to the device forward of its input."""
+    wl = synth.Workload("pipe", 1000, 1024, 256, 64, 4)
+    w = synth.device_inputs(wl)
+    xs = [w["x"], synth.device_inputs(synth.Workload("pipe", 1000, 1024, 256, 64, 4, seed=4))["x"]]
+    ref = _layer(wl)
+    y_ref = [ref.forward(x, w["Wr"], w["W1"], w["W2"], check=True)[0].cpu() for x in xs]
+    ref.close()
+    layer = _layer(wl, flags=moe.MOE_FLAG_HOST_PIPELINE)
+    x_host = [x.cpu().pin_memory() for x in xs]
+    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    y_host = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+    for i in range(6):
+        layer.forward_host(x_host[i % 2], w["Wr"], w["W1"], w["W2"], lg, y_host[i])
+    layer.check()
+    for i in range(6):
+        assert torch.equal(y_host[i].view(torch.int16), y_ref[i % 2].view(torch.int16)), f"forward {i}"
+    layer.close()
