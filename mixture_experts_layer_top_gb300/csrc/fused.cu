@@ -8,7 +8,7 @@
 // grid-wide barriers:
 //
 //   A  router logits in the canonical fp32 order on the CUDA cores (W_router given), x and
-//      W_router staged in shared memory per 32-token x 8-expert task
+//      W_router staged in shared memory per task of 32, 16 or 8 tokens x 8 experts
 //   B  top-k, softmax weights, expert counts (one warp per token)
 //   C  Dispatch: counting sort, padded rows, tile list (dispatch_body, 320-thread blocks)
 //   D  gather of the x rows into the padded row space
@@ -236,7 +236,7 @@ __device__ void router_phase(const FusedArgs& a, uint16_t* rs, int lane, int war
 }
 
 // Phase A as a kernel of its own: the multi-launch path's canonical router for small token
-// counts, where its tasks (32 tokens x 8 experts, one CTA each) spread over every SM while the
+// counts, where its tasks (32, 16 or 8 tokens x 8 experts, one CTA each) spread over every SM while the
 // tensor-core router's selection and the 32 x 32 canonical kernel leave most SMs idle.  With
 // E <= FR_EXP the CTA that wrote a task's logits also selects its tokens' experts.
 constexpr int FR_SMEM = FR_NS * FR_STAGE * 2 + FR_TOK * FR_EXP * 4;
