@@ -9,7 +9,10 @@ One step = one moe_forward over the whole batch of T tokens, inputs and weights
 resident in HBM; L2 is flushed (256 MiB write) before every step, outside the
 timed events.  The headline is the large layer (T=4096, H=7168, I=2048, E=256,
 top-8); the fine-grained, skewed and 128-token workloads are timed in the same
-process the same way and reported under "workloads".  Rank 0 prints one JSON line.  With torchrun (N > 1) every rank
+process the same way and reported under "workloads".  "e2e" is the same metric through
+moe_forward_host: K back-to-back calls on page-locked host x and y, their copies pipelined
+beside the neighbouring steps' kernels, timed as one span up to the last y in host memory.
+Rank 0 prints one JSON line.  With torchrun (N > 1) every rank
 runs an independent replica on its own GPU (the layer is not sharded) and the
 time is the maximum over ranks.
 """
@@ -379,35 +382,54 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     clocks = sampler.summary(t0, t1) if sampler else None
     ms_per_step = reduce_max(sum(a.elapsed_time(b) for a, b in ev), group) / args.steps
 
-    # ---- e2e: the host-buffer C-ABI call, copies inside the timed region
-    # (MOE_FLAG_HOST_PIPELINE: x_host is written once, on the host, before the steps, so each
-    # step's upload may run beside the previous step's GEMM)
+    # ---- e2e: back-to-back host-buffer C-ABI calls, every copy inside the timed region.
+    # MOE_FLAG_HOST_PIPELINE: x_host is written once, on the host, before the steps; each step's
+    # upload runs beside the previous step's GEMM and its y copy beside the next step, so the
+    # region is one span from the first step's start to the last y landing in host memory
+    # (moe_host_wait).  L2: the steps stream the expert weights, several times L2 on every
+    # workload but the tiny one; that one is flushed between steps, the flushes' own time
+    # (events around each) taken out of the span.
     e2e = None
     if with_e2e:
         layer_h = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags | moe.MOE_FLAG_HOST_PIPELINE,
                                              **cfg), local, router_bias=bias)
         x_host = d["x"].cpu().pin_memory()
         y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+        weight_bytes = 3 * wl.E * wl.H * wl.I * 2
+        l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush_steps = weight_bytes < 4 * l2_bytes   # weights not well beyond L2: flush between steps
         for _ in range(2):
-            flush.zero_()
             layer_h.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
+        layer_h.host_wait()
+        flush.zero_()
         torch.cuda.synchronize()
-        eev = _events(args.steps)
+        fev = _events(args.steps)
+        span = _events(1)[0]
+        span[0].record()
         for i in range(args.steps):
-            flush.zero_()
-            eev[i][0].record()
+            if flush_steps and i:
+                fev[i][0].record()
+                flush.zero_()
+                fev[i][1].record()
             layer_h.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
-            eev[i][1].record()
+        layer_h.host_wait()
+        span[1].record()
         torch.cuda.synchronize()
         layer_h.check()
         layer_h.close()
         if not torch.equal(y_host.view(torch.int16), y.cpu().view(torch.int16)):
             raise RuntimeError("host-buffer forward disagrees with the device-buffer forward")
-        e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in eev), group) / args.steps
+        flush_ms = sum(fev[i][0].elapsed_time(fev[i][1]) for i in range(1, args.steps)) if flush_steps else 0.0
+        e_ms = reduce_max(span[0].elapsed_time(span[1]) - flush_ms, group) / args.steps
         e2e = {"value": ws * wl.useful_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2,
                "ms_per_step": e_ms, "tokens_per_s": ws * wl.T / (e_ms * 1e-3),
-               "host_pipeline": True}
+               "host_pipeline": True,
+               "timing": "one span over the back-to-back steps, first step's start to the last y in host memory",
+               "l2": (f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write), flush time taken out"
+                      if flush_steps else
+                      f"not flushed: the {weight_bytes / 2**30:.2f} GiB of expert weights exceed L2 "
+                      f"({l2_bytes >> 20} MiB)")}
     layer.close()
     # ---- per-stage breakdown on a second plan whose library records events between stages
     # (those events serialise the stream, so the timed steps above run without them)

@@ -122,13 +122,20 @@ typedef enum {
  * ignored (the default ring split); with MOE_FLAG_STAGE_TIMING the whole launch is reported
  * as stage 3 (the grouped GEMM) and the other stages as 0. */
 #define MOE_FLAG_SINGLE_LAUNCH (1u << 6)
-/* moe_forward_host only (library plumbing: no counterpart in the paper).  Default: the input
- * upload waits for all work enqueued on the stream before the call, like any stream-ordered
- * operation.  With this flag it waits only until the previous moe_forward_host of this plan no
- * longer reads the plan's input buffer (its gather), so back-to-back host forwards upload the
- * next input while the previous one is still computing.  The caller then must have written
- * x_host on the host before the call: a write of x_host by work enqueued on the stream between
- * two such calls (a device-to-host copy, a host callback) is not waited for. */
+/* moe_forward_host only (library plumbing: no counterpart in the paper): pipelined host
+ * forwards, whose copies run beside the neighbouring forwards' kernels.  Default: the input
+ * upload waits for all work enqueued on the stream before the call, and y is in y_host when
+ * the stream reaches the end of the forward, like any stream-ordered operation.  With this flag
+ *  - the upload waits only until the previous moe_forward_host of this plan no longer reads
+ *    the plan's input buffer (its gather), so back-to-back host forwards upload the next input
+ *    while the previous one is still computing.  The caller must have written x_host on the
+ *    host before the call: a write of x_host by work enqueued on the stream between two such
+ *    calls (a device-to-host copy, a host callback) is not waited for;
+ *  - a page-locked y_host is filled by the copy engines on a stream of the plan's own, from one
+ *    of two plan-owned staging buffers that Combine writes in turn, and `stream` does not wait
+ *    for that copy: y_host is complete once moe_host_wait has made a stream wait for it (or
+ *    moe_get_status has returned).  Each staging buffer is reused by the forward after next,
+ *    whose Combine waits for its copy; the plan's workspace holds the second buffer. */
 #define MOE_FLAG_HOST_PIPELINE (1u << 7)
 #define MOE_FLAG_TEST_BAD_ID (1u << 9)  /* test only: Dispatch sees the first (token, slot) pair's expert
                                           id out of range; the pair is dropped, no access leaves the
@@ -188,8 +195,8 @@ MOE_API moe_status_t moe_forward(moe_plan_t plan, int32_t T, const void* x, floa
  * on `stream`.  A page-locked buffer that is mapped into the device's address space (any
  * cudaHostAlloc / cudaMallocHost buffer under unified addressing) at a 16-byte-aligned address
  * is copied into the plan's buffer by the copy engines in token ranges, each routed as it
- * lands (the copy waits only for the previous host-buffer forward's last read of that buffer, so
- * it can run beside that forward's later kernels), and Combine stores y into y_host in place.
+ * lands, and Combine stores y into y_host in place (with MOE_FLAG_HOST_PIPELINE the copies
+ * run beside the neighbouring forwards instead: see there).
  * Any other buffer goes through cudaMemcpyAsync and plan-owned staging buffers (synchronous for
  * pageable memory).  router_logits, W_router, W1_gate_up and W2 are
  * DEVICE pointers exactly as in moe_forward.  The caller must not touch y_host before the
@@ -198,8 +205,14 @@ MOE_API moe_status_t moe_forward_host(moe_plan_t plan, int32_t T, const void* x_
                               const void* W_router, const void* W1_gate_up, const void* W2, void* y_host,
                               void* stream);
 
-/* Synchronise `stream`, then read and clear the plan's device error word (library plumbing:
- * no counterpart in the paper).
+/* Make `stream` wait (without blocking the host) until every output copy of the plan's pipelined
+ * host forwards (MOE_FLAG_HOST_PIPELINE) enqueued so far has landed in its y_host; a no-op
+ * wait when there is none (library plumbing: no counterpart in the paper).
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG (null plan) or MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_host_wait(moe_plan_t plan, void* stream);
+
+/* Synchronise `stream` and the plan's pending output copies (MOE_FLAG_HOST_PIPELINE), then read
+ * and clear the plan's device error word (library plumbing: no counterpart in the paper).
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or MOE_ERR_CUDA. */
 MOE_API moe_status_t moe_get_status(moe_plan_t plan, void* stream);
 

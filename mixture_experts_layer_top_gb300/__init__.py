@@ -50,7 +50,7 @@ MOE_FLAG_TEST_BAD_ID = 1 << 9
 MOE_NUM_STAGES = 5
 STAGE_NAMES = ("router_topk", "dispatch", "gather", "grouped_gemm", "combine")
 
-EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_get_status",
+EXPORTED = ("moe_plan", "moe_workspace_bytes", "moe_forward", "moe_forward_host", "moe_host_wait", "moe_get_status",
             "moe_debug_routing",
             "moe_debug_intermediates", "moe_stage_times", "moe_last_launch_count", "moe_plan_destroy",
             "moe_status_string", "moe_schedule_host", "moe_dispatch_static", "moe_trace_read", "moe_trace_tiles",
@@ -95,6 +95,7 @@ def load() -> ctypes.CDLL:
     L.moe_forward.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     L.moe_forward_host.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     L.moe_get_status.argtypes = [vp, vp]
+    L.moe_host_wait.argtypes = [vp, vp]
     L.moe_debug_routing.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     L.moe_debug_intermediates.argtypes = [vp, i32, vp, vp, vp]
     L.moe_stage_times.argtypes = [vp, P(ctypes.c_float)]
@@ -149,6 +150,10 @@ def moe_forward_host(plan: int, T: int, x_host: int, router_logits: int, W_route
 
 def moe_get_status(plan: int, stream: int) -> int:
     return load().moe_get_status(plan, stream)
+
+
+def moe_host_wait(plan: int, stream: int) -> int:
+    return load().moe_host_wait(plan, stream)
 
 
 def moe_debug_routing(plan: int, T: int, ids, w, counts, offsets, row_pair, row_of, stream: int) -> int:
@@ -335,6 +340,13 @@ class MoELayer:
         if check:
             self.check()
         return y_host, logits
+
+    def host_wait(self):
+        """Make the current stream wait for the output copies of the pipelined host forwards
+        (MOE_FLAG_HOST_PIPELINE) enqueued so far."""
+        st = moe_host_wait(self.plan, self._stream())
+        if st != MOE_OK:
+            raise MoEError(st, "moe_host_wait")
 
     def check(self):
         st = moe_get_status(self.plan, self._stream())

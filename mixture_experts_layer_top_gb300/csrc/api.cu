@@ -27,7 +27,7 @@ struct moe_plan_s {
   void* base;
   size_t bytes;
   void* x_stage;
-  void* y_stage;
+  void* y_stage[2];   // [1]: MOE_FLAG_HOST_PIPELINE only
   float* bias;
   Workspace ws;
   RouterWs rw;
@@ -39,6 +39,13 @@ struct moe_plan_s {
   cudaEvent_t ev_fork;    // recorded on st at the start of a host-buffer forward (strict stream order)
   cudaEvent_t ev_xfree;   // recorded on st after the last kernel that reads x_stage (host-buffer forwards)
   cudaEvent_t ev_range[4];
+  // MOE_FLAG_HOST_PIPELINE with page-locked y_host: Combine writes y_stage[y_slot] (alternating),
+  // whose copy to y_host runs on st_out beside the next forward
+  cudaStream_t st_out;
+  cudaEvent_t ev_ydone;      // recorded on st after the forward's Combine
+  cudaEvent_t ev_yfree[2];   // recorded on st_out after the copy out of y_stage[s]
+  cudaEvent_t ev_ylast;      // moe_host_wait: every output copy enqueued so far
+  int y_slot;
   int last_launches;
   unsigned long long* trace;   // [max(gemm_grid, fused_grid) + 1][TRACE_SLOTS] when MOE_FLAG_TRACE
   unsigned long long* tile_trace;   // [max_tiles][PAIR][TILE_TRACE_SLOTS] when MOE_FLAG_TRACE
@@ -59,6 +66,11 @@ void release(moe_plan_s* p) {
   if (p->ev_xfree) cudaEventDestroy(p->ev_xfree);
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->st_aux) cudaStreamDestroy(p->st_aux);
+  for (int s = 0; s < 2; ++s)
+    if (p->ev_yfree[s]) cudaEventDestroy(p->ev_yfree[s]);
+  if (p->ev_ydone) cudaEventDestroy(p->ev_ydone);
+  if (p->ev_ylast) cudaEventDestroy(p->ev_ylast);
+  if (p->st_out) cudaStreamDestroy(p->st_out);
   if (p->base) cudaFree(p->base);
   if (p->bias) cudaFree(p->bias);
   if (p->trace) cudaFree(p->trace);
@@ -161,7 +173,7 @@ Layout layout_of(const moe_config_t& c, int64_t R, int64_t max_mt, int64_t max_t
   sizes[B_READY] = (size_t)max_mt * 4;
   sizes[B_ERR] = 16;
   sizes[B_X_STAGE] = (size_t)c.T_max * c.H * 2;          // moe_forward_host staging
-  sizes[B_Y_STAGE] = (size_t)c.T_max * c.H * 2;
+  sizes[B_Y_STAGE] = (size_t)c.T_max * c.H * 2 * ((c.flags & MOE_FLAG_HOST_PIPELINE) ? 2 : 1);
   sizes[B_WRT] = (size_t)c.E * c.H * 2;                  // router: Wr transposed
   sizes[B_NW] = (size_t)c.E * 4;                         // router: column norm bounds
   sizes[B_PART] = (size_t)router_part_rows(c.T_max) * c.E * 4;   // router: split-K partial estimates
@@ -339,8 +351,9 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
       p->last_launches = nl;
       return MOE_ERR_CUDA;
     }
-    // token ranges of whole 128-token chunks: one, or up to HOST_RANGES while x streams in
-    const int nr = x_src ? std::min(HOST_RANGES, chunks) : 1;
+    // token ranges of whole 128-token chunks: up to HOST_RANGES while x streams in, else one
+    // (with MOE_FLAG_HOST_PIPELINE the upload ran beside the previous forward: no range waits)
+    const int nr = (x_src && !(c.flags & MOE_FLAG_HOST_PIPELINE)) ? std::min(HOST_RANGES, chunks) : 1;
     const int per = ((chunks + nr - 1) / nr) * DS_CHUNK_TOK;
     if (x_src) {
       MOE_CK(wait_staging_free(p, st));
@@ -512,7 +525,8 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   p->ws.ready = reinterpret_cast<int32_t*>(at(B_READY));
   p->ws.err = reinterpret_cast<uint32_t*>(at(B_ERR));
   p->x_stage = at(B_X_STAGE);
-  p->y_stage = at(B_Y_STAGE);
+  p->y_stage[0] = at(B_Y_STAGE);
+  p->y_stage[1] = (cfg->flags & MOE_FLAG_HOST_PIPELINE) ? at(B_Y_STAGE) + (size_t)cfg->T_max * cfg->H * 2 : nullptr;
   p->rw.WrT = reinterpret_cast<uint16_t*>(at(B_WRT));
   p->rw.nw = reinterpret_cast<float*>(at(B_NW));
   p->rw.part = reinterpret_cast<float*>(at(B_PART));
@@ -554,7 +568,12 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
       if (cudaEventCreate(&p->ev[i]) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&p->st_aux, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_xfree, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess)
+      cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&p->st_out, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_ydone, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_ylast, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_yfree[0], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_yfree[1], cudaEventDisableTiming) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   for (int r = 0; r < HOST_RANGES; ++r)
     if (cudaEventCreateWithFlags(&p->ev_range[r], cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -574,11 +593,16 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
                               const void* W_router, const void* W1, const void* W2, void* y_host, void* stream) {
   if (!p || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
   // Page-locked buffers: x streams in by the copy engines in token ranges (overlapping the
-  // router, and the previous forward's later kernels), Combine writes y in place.  Pageable
-  // ones go through the copy engines and the staging buffers whole.
+  // router, and the previous forward's later kernels), Combine writes y in place - or, with
+  // MOE_FLAG_HOST_PIPELINE, into the alternating staging buffers that the copy engines drain
+  // on st_out beside the next forward.  Pageable ones go through the copy engines and the
+  // staging buffers whole.
+  const bool pipe = (p->cfg.flags & MOE_FLAG_HOST_PIPELINE) != 0;
   const void* x_dev = mapped_host(x_host);
   void* y_dev = mapped_host(y_host);
-  void* y = y_dev ? y_dev : p->y_stage;
+  const bool y_out = pipe && y_dev;   // y leaves on st_out
+  const int slot = y_out ? p->y_slot : 0;
+  void* y = (y_dev && !y_out) ? y_dev : p->y_stage[slot];
   const moe_status_t v = check_forward_args(p, T, p->x_stage, router_logits, W_router, W1, W2, y);
   if (v != MOE_OK) return v;
   if (T == 0) {
@@ -587,6 +611,8 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)T * p->cfg.H * 2;
+  // the staging buffer Combine writes has been copied out (a no-op until a first copy)
+  if (pipe && cudaStreamWaitEvent(st, p->ev_yfree[slot], 0) != cudaSuccess) return MOE_ERR_CUDA;
   if (!x_dev) {   // pageable: the copy engines, on st_aux once x_stage is free (as stage_whole_input)
     if (wait_staging_free(p, st) != cudaSuccess ||
         cudaMemcpyAsync(p->x_stage, x_host, bytes, cudaMemcpyHostToDevice, p->st_aux) != cudaSuccess ||
@@ -595,7 +621,24 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
   }
   const moe_status_t s = forward_impl(p, T, p->x_stage, x_dev, router_logits, W_router, W1, W2, y, st);
   if (s != MOE_OK) return s;
-  if (!y_dev && cudaMemcpyAsync(y_host, p->y_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  if (y_out) {
+    if (cudaEventRecord(p->ev_ydone, st) != cudaSuccess || cudaStreamWaitEvent(p->st_out, p->ev_ydone, 0) != cudaSuccess ||
+        cudaMemcpyAsync(y_host, y, bytes, cudaMemcpyDeviceToHost, p->st_out) != cudaSuccess ||
+        cudaEventRecord(p->ev_yfree[slot], p->st_out) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    p->y_slot ^= 1;
+    return MOE_OK;
+  }
+  if (!y_dev && cudaMemcpyAsync(y_host, p->y_stage[0], bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (pipe && cudaEventRecord(p->ev_yfree[0], st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_host_wait(moe_plan_t p, void* stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (cudaEventRecord(p->ev_ylast, p->st_out) != cudaSuccess ||
+      cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), p->ev_ylast, 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -603,7 +646,7 @@ moe_status_t moe_forward_host(moe_plan_t p, int32_t T, const void* x_host, float
 moe_status_t moe_get_status(moe_plan_t p, void* stream) {
   if (!p) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess || cudaStreamSynchronize(p->st_out) != cudaSuccess) return MOE_ERR_CUDA;
   uint32_t e = 0;
   if (cudaMemcpy(&e, p->ws.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (e != 0 && cudaMemset(p->ws.err, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;

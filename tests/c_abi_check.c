@@ -37,6 +37,7 @@ int main(void) {
 
   CHECK(moe_status_string(MOE_OK) != NULL && strlen(moe_status_string(MOE_OK)) > 0);
   CHECK(moe_status_string(MOE_ERR_TIMEOUT) != NULL);
+  CHECK(moe_host_wait(NULL, NULL) == MOE_ERR_INVALID_ARG);   /* rejected before any CUDA call */
 
   /* host evaluation of the tile schedule: 3 experts with 300, 0 and 40 rows */
   int32_t counts[3] = {300, 0, 40};

@@ -970,3 +970,36 @@ def test_host_pipeline_back_to_back():
     for i in range(6):
         assert torch.equal(y_host[i].view(torch.int16), y_ref[i % 2].view(torch.int16)), f"forward {i}"
     layer.close()
+
+
+def test_host_pipeline_output_copies():
+    """MOE_FLAG_HOST_PIPELINE output side: y leaves through the plan's alternating staging buffers
+    on its own stream; after moe_host_wait on the caller's stream (no moe_get_status) every
+    y_host of a back-to-back run holds its forward's y - with token counts below T_max and a
+    pageable y_host mixed in (that one stream-ordered, through the first staging buffer)."""
+    wl = synth.Workload("pipe", 1000, 1024, 256, 64, 4)
+    w = synth.device_inputs(wl)
+    xs = [w["x"], synth.device_inputs(synth.Workload("pipe", 1000, 1024, 256, 64, 4, seed=5))["x"]]
+    ref = _layer(wl)
+    runs = [(0, 1000, True), (1, 1000, True), (0, 300, True), (1, 1000, False), (1, 700, True), (0, 1000, True),
+            (1, 1000, True)]
+    y_ref = {}
+    for xi, T, _ in runs:
+        if (xi, T) not in y_ref:
+            y_ref[(xi, T)] = ref.forward(xs[xi][:T], w["Wr"], w["W1"], w["W2"], check=True)[0].cpu()
+    ref.close()
+    layer = _layer(wl, flags=moe.MOE_FLAG_HOST_PIPELINE)
+    x_host = [x.cpu().pin_memory() for x in xs]
+    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    y_host = []
+    for _, T, pin in runs:
+        yh = torch.full((T, wl.H), -1, dtype=torch.int16)
+        y_host.append((yh.pin_memory() if pin else yh).view(torch.bfloat16))
+    for (xi, T, _), yh in zip(runs, y_host):
+        layer.forward_host(x_host[xi][:T], w["Wr"], w["W1"], w["W2"], lg[:T], yh)
+    layer.host_wait()
+    torch.cuda.current_stream().synchronize()
+    for i, ((xi, T, _), yh) in enumerate(zip(runs, y_host)):
+        assert torch.equal(yh.view(torch.int16), y_ref[(xi, T)].view(torch.int16)), f"forward {i} (T={T})"
+    layer.check()
+    layer.close()
