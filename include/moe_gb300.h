@@ -135,7 +135,7 @@ typedef enum {
  *    of two plan-owned staging buffers that Combine writes in turn, and `stream` does not wait
  *    for that copy: y_host is complete once moe_host_wait has made a stream wait for it (or
  *    moe_get_status has returned).  Each staging buffer is reused by the forward after next,
- *    whose Combine waits for its copy; the plan's workspace holds the second buffer. */
+ *    whose kernels start once that copy is done; the plan's workspace holds the second buffer. */
 #define MOE_FLAG_HOST_PIPELINE (1u << 7)
 #define MOE_FLAG_TEST_BAD_ID (1u << 9)  /* test only: Dispatch sees the first (token, slot) pair's expert
                                           id out of range; the pair is dropped, no access leaves the
