@@ -38,8 +38,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 256 << 20
 
 
-# idle time before each workload's warm-up: a latency-bound workload timed right after heavy
-# work (input generation, a weight-streaming workload) ran at a power-limited SM clock
+# idle time before each workload's warm-up and before its e2e steps: a latency-bound workload
+# timed right after heavy work (input generation, a weight-streaming workload) ran at a
+# power-limited SM clock, and the weight-streaming layer's steps slow as a run goes on
 IDLE_BEFORE_S = 0.5
 
 
@@ -398,6 +399,8 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
         weight_bytes = 3 * wl.E * wl.H * wl.I * 2
         l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
         flush_steps = weight_bytes < 4 * l2_bytes   # weights not well beyond L2: flush between steps
+        torch.cuda.synchronize()
+        time.sleep(IDLE_BEFORE_S)               # the same idle start as the device-buffer steps
         for _ in range(2):
             layer_h.forward_host(x_host, d["Wr"], d["W1"], d["W2"], logits, y_host)
         layer_h.host_wait()
