@@ -361,12 +361,14 @@ def _random_cases_many_tokens(n: int, seed: int = 20261203):
 def test_random_shapes_full_oracle(c):
     """Routing (bit-exact) and y (stated tolerance) against the full oracle on seeded random
     shapes, schedules and kernel variants, with the plan sized above the batch; a third of
-    the cases through the host-buffer entry point (page-locked x and y)."""
+    the cases through the host-buffer entry point (page-locked x and y), half of those as
+    pipelined host forwards (MOE_FLAG_HOST_PIPELINE: y copied out on the plan's own stream)."""
     wl = synth.Workload("rand", c["T"], c["H"], c["I"], c["E"], c["k"], zipf_s=c["zipf"])
     h = synth.host_inputs(wl)
     bias = _bias(wl)
     ref = oracle_for(wl, h["x"], h["Wr"], bias, None, full_weights=(h["W1"], h["W2"]), want_intermediates=True)
-    layer = _layer(wl, c["sched"], flags=c["flags"], T_max=c["T"] + c["extra"], bias=bias)
+    pipe = moe.MOE_FLAG_HOST_PIPELINE if c["host"] and c["extra"] % 2 else 0
+    layer = _layer(wl, c["sched"], flags=c["flags"] | pipe, T_max=c["T"] + c["extra"], bias=bias)
     d = {kk: from_bits(v) for kk, v in h.items() if kk != "bias"}
     if c["host"]:
         x_host = d["x"].cpu().pin_memory()
@@ -972,11 +974,13 @@ def test_host_pipeline_back_to_back():
     layer.close()
 
 
-def test_host_pipeline_output_copies():
+@pytest.mark.parametrize("extra", [0, moe.MOE_FLAG_SINGLE_LAUNCH])
+def test_host_pipeline_output_copies(extra):
     """MOE_FLAG_HOST_PIPELINE output side: y leaves through the plan's alternating staging buffers
     on its own stream; after moe_host_wait on the caller's stream (no moe_get_status) every
-    y_host of a back-to-back run holds its forward's y - with token counts below T_max and a
-    pageable y_host mixed in (that one stream-ordered, through the first staging buffer)."""
+    y_host of a back-to-back run holds its forward's y - with token counts below T_max (the
+    tensor-core and the canonical task router), a pageable y_host mixed in (that one
+    stream-ordered, through the first staging buffer), multi-launch and single launch."""
     wl = synth.Workload("pipe", 1000, 1024, 256, 64, 4)
     w = synth.device_inputs(wl)
     xs = [w["x"], synth.device_inputs(synth.Workload("pipe", 1000, 1024, 256, 64, 4, seed=5))["x"]]
@@ -988,7 +992,7 @@ def test_host_pipeline_output_copies():
         if (xi, T) not in y_ref:
             y_ref[(xi, T)] = ref.forward(xs[xi][:T], w["Wr"], w["W1"], w["W2"], check=True)[0].cpu()
     ref.close()
-    layer = _layer(wl, flags=moe.MOE_FLAG_HOST_PIPELINE)
+    layer = _layer(wl, flags=moe.MOE_FLAG_HOST_PIPELINE | extra)
     x_host = [x.cpu().pin_memory() for x in xs]
     lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
     y_host = []
