@@ -6,7 +6,9 @@
  * result (absolute 2e-2 RMS everywhere, relative 3e-2 where |y_ref| > 0.1 RMS, measured from
  * the oracle's interval of y before rounding, the GPU's value standing for anything within
  * half a bf16 spacing of it), then a second forward on the same plan bitwise equal to the
- * first.  Prints "ok ..." and exits 0 on success; prints the failed check otherwise. */
+ * first, then two back-to-back pipelined host forwards (MOE_FLAG_HOST_PIPELINE,
+ * cudaMallocHost buffers, moe_forward_host + moe_host_wait) bitwise equal to it too.
+ * Prints "ok ..." and exits 0 on success; prints the failed check otherwise. */
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -139,6 +141,28 @@ int main(int argc, char** argv) {
   CHECK(moe_get_status(plan, (void*)st) == MOE_OK);
   CHECK(memcmp(y, y2, nx * 2) == 0);
   CHECK(moe_plan_destroy(plan) == MOE_OK);
+
+  /* pipelined host forwards: page-locked x in, two outputs, the copies waited for by moe_host_wait */
+  cfg.flags = MOE_FLAG_HOST_PIPELINE;
+  moe_plan_t hplan = NULL;
+  CHECK(moe_plan(&cfg, 0, &hplan) == MOE_OK && hplan != NULL);
+  void *hx = NULL, *hy0 = NULL, *hy1 = NULL;
+  CHECK(cudaMallocHost(&hx, nx * 2) == cudaSuccess && cudaMallocHost(&hy0, nx * 2) == cudaSuccess &&
+        cudaMallocHost(&hy1, nx * 2) == cudaSuccess);
+  memcpy(hx, x, nx * 2);
+  memset(hy0, 0xFF, nx * 2);
+  memset(hy1, 0xFF, nx * 2);
+  CHECK(moe_forward_host(hplan, T, hx, (float*)dlogits, dWr, dW1, dW2, hy0, (void*)st) == MOE_OK);
+  CHECK(moe_forward_host(hplan, T, hx, (float*)dlogits, dWr, dW1, dW2, hy1, (void*)st) == MOE_OK);
+  CHECK(moe_host_wait(hplan, (void*)st) == MOE_OK);
+  CHECK(cudaStreamSynchronize(st) == cudaSuccess);
+  CHECK(memcmp(y, hy0, nx * 2) == 0);
+  CHECK(memcmp(y, hy1, nx * 2) == 0);
+  CHECK(moe_get_status(hplan, (void*)st) == MOE_OK);
+  CHECK(moe_plan_destroy(hplan) == MOE_OK);
+  cudaFreeHost(hx);
+  cudaFreeHost(hy0);
+  cudaFreeHost(hy1);
   cudaFree(dx);
   cudaFree(dWr);
   cudaFree(dW1);

@@ -36,8 +36,9 @@ def test_plain_c_caller_compiles_links_and_runs(lib_dir, tmp_path):
 @pytest.mark.gpu
 def test_plain_c_caller_runs_the_layer_on_the_gpu(lib_dir, tmp_path):
     """tests/c_abi_gpu.c, a C99 program with cudaMalloc'd buffers, plans and runs the tiny layer
-    through moe_plan / moe_forward / moe_get_status / moe_debug_routing; its inputs and the
-    oracle's expectations come from tests/golden/make_c_abi_case.py (oracle and synth only)."""
+    through moe_plan / moe_forward / moe_get_status / moe_debug_routing, then as pipelined host
+    forwards (moe_forward_host / moe_host_wait); its inputs and the oracle's expectations come
+    from tests/golden/make_c_abi_case.py (oracle and synth only)."""
     import sys
     sys.path.insert(0, os.path.join(ROOT, "tests", "golden"))
     import make_c_abi_case
