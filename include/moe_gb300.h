@@ -123,14 +123,20 @@ typedef enum {
  * as stage 3 (the grouped GEMM) and the other stages as 0. */
 #define MOE_FLAG_SINGLE_LAUNCH (1u << 6)
 /* moe_forward_host only (library plumbing: no counterpart in the paper): pipelined host
- * forwards, whose copies run beside the neighbouring forwards' kernels.  Default: the input
- * upload waits for all work enqueued on the stream before the call, and y is in y_host when
- * the stream reaches the end of the forward, like any stream-ordered operation.  With this flag
- *  - the upload waits only until the previous moe_forward_host of this plan no longer reads
- *    the plan's input buffer (its gather), so back-to-back host forwards upload the next input
- *    while the previous one is still computing.  The caller must have written x_host on the
- *    host before the call: a write of x_host by work enqueued on the stream between two such
- *    calls (a device-to-host copy, a host callback) is not waited for;
+ * forwards, whose copies and routing run beside the neighbouring forwards' kernels.  Default:
+ * the input upload waits for all work enqueued on the stream before the call, and y is in
+ * y_host when the stream reaches the end of the forward, like any stream-ordered operation.
+ * With this flag
+ *  - the upload waits only until the previous forward of this plan no longer reads the plan's
+ *    input buffer or its routing (its gather), so back-to-back host forwards upload the next
+ *    input while the previous one is still computing; with a page-locked x_host the routing
+ *    (router and top-k) follows the upload on a stream of the plan's own, beside the previous
+ *    forward's last kernels, and the stream joins it before Dispatch.  The caller must have
+ *    written x_host on the host, and W_router (router_logits when it is the input) on the
+ *    device, before the call: a write by work enqueued on the stream between two such calls
+ *    (a copy, a kernel, a host callback) is not waited for.  A forward's routing outputs
+ *    (router_logits, and what moe_debug_routing reads) may be overwritten as soon as the next
+ *    pipelined host forward of the plan has been called;
  *  - a page-locked y_host is filled by the copy engines on a stream of the plan's own, from one
  *    of two plan-owned staging buffers that Combine writes in turn, and `stream` does not wait
  *    for that copy: y_host is complete once moe_host_wait has made a stream wait for it (or

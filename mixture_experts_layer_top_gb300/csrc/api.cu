@@ -37,7 +37,9 @@ struct moe_plan_s {
   // token ranges, each routed as soon as it has landed
   cudaStream_t st_aux;
   cudaEvent_t ev_fork;    // recorded on st at the start of a host-buffer forward (strict stream order)
-  cudaEvent_t ev_xfree;   // recorded on st after the last kernel that reads x_stage (host-buffer forwards)
+  cudaEvent_t ev_xfree;   // MOE_FLAG_HOST_PIPELINE: recorded on st after each forward's gather (or single
+                          // launch): x_stage and the routing buffers (last read by Dispatch) are free
+  cudaEvent_t ev_routed;  // recorded on st_aux after a pipelined host forward's routing
   cudaEvent_t ev_range[4];
   // MOE_FLAG_HOST_PIPELINE with page-locked y_host: Combine writes y_stage[y_slot] (alternating),
   // whose copy to y_host runs on st_out beside the next forward
@@ -64,6 +66,7 @@ void release(moe_plan_s* p) {
   for (int r = 0; r < HOST_RANGES; ++r)
     if (p->ev_range[r]) cudaEventDestroy(p->ev_range[r]);
   if (p->ev_xfree) cudaEventDestroy(p->ev_xfree);
+  if (p->ev_routed) cudaEventDestroy(p->ev_routed);
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->st_aux) cudaStreamDestroy(p->st_aux);
   for (int s = 0; s < 2; ++s)
@@ -271,9 +274,10 @@ GemmArgs gemm_args(const moe_plan_s* p) {
 // buffer) inside this call by the copy engines, on st_aux - in HOST_RANGES token ranges when the
 // tensor-core router runs, which starts on each range as soon as it has landed, else whole.  A
 // copy into the staging buffer waits for all work enqueued on st before the call, or with
-// MOE_FLAG_HOST_PIPELINE only for ev_xfree: the previous host-buffer forward's last kernel that
-// reads it (its gather, or its single launch), so it runs beside that forward's later kernels
-// (the copy engines need no SM; an SM copy kernel measured slower there).
+// MOE_FLAG_HOST_PIPELINE only for ev_xfree: the previous forward's gather (or single launch), the
+// last kernel that reads x_stage, so it runs beside that forward's later kernels (the copy
+// engines need no SM; an SM copy kernel measured slower there) - and the routing follows it
+// there (see forward_impl).
 cudaError_t wait_staging_free(moe_plan_t p, cudaStream_t st) {
   if (p->cfg.flags & MOE_FLAG_HOST_PIPELINE) return cudaStreamWaitEvent(p->st_aux, p->ev_xfree, 0);
   cudaError_t e = cudaEventRecord(p->ev_fork, st);
@@ -307,9 +311,10 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   } while (0)
   rec(0);
   const int chunks = (T + DS_CHUNK_TOK - 1) / DS_CHUNK_TOK;
-  // grid-barrier word, counts and chist (one contiguous range)
-  MOE_CK(cudaMemsetAsync(p->ws.gbar, 0, 16 + sizeof(int32_t) * E * (1 + chunks), st));
+  // grid-barrier word, counts and chist (one contiguous range), zeroed before each forward's routing
+  const size_t zero_bytes = 16 + sizeof(int32_t) * E * (1 + chunks);
   if (c.flags & MOE_FLAG_SINGLE_LAUNCH) {
+    MOE_CK(cudaMemsetAsync(p->ws.gbar, 0, zero_bytes, st));
     if (x_src) MOE_CK(stage_whole_input(p, x_src, (size_t)T * H * 2, st));   // the input lands whole first
     rec(1);
     rec(2);
@@ -333,7 +338,8 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
                               c.lead_waves, (int)p->R_pad_max, (c.flags & MOE_FLAG_TEST_BAD_ID) != 0, ga,
                               trace_ctas(p), st));
     ++nl;
-    if (x == p->x_stage) MOE_CK(cudaEventRecord(p->ev_xfree, st));   // x_stage free for the next upload
+    if (c.flags & MOE_FLAG_HOST_PIPELINE)   // x_stage and the routing buffers free for the next forward
+      MOE_CK(cudaEventRecord(p->ev_xfree, st));
     rec(4);
     rec(5);
     p->last_launches = nl;
@@ -341,7 +347,20 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   }
   const int rchoice = W_router ? router_choice(c.flags, T, E, p->num_sms) : ROUTER_CANON_32;
   const bool tc_router = rchoice == ROUTER_TC;
-  if (x_src && !tc_router) MOE_CK(stage_whole_input(p, x_src, (size_t)T * H * 2, st));   // whole copy first
+  // Stream of the routing: with MOE_FLAG_HOST_PIPELINE and a page-locked host input (stage timing
+  // off), the plan's copy stream, right behind the input's upload there - both wait only until the
+  // previous forward's gather is done (so its Dispatch, the last reader of the routing buffers),
+  // and the routing then runs beside that forward's GEMM tail and Combine; st joins it before
+  // Dispatch.  Otherwise st, the input copied in ranges (tensor-core router) or whole.
+  const bool aside = x_src && (c.flags & MOE_FLAG_HOST_PIPELINE) && !p->timing;
+  cudaStream_t sr = aside ? p->st_aux : st;
+  if (aside) {
+    MOE_CK(wait_staging_free(p, st));
+    MOE_CK(cudaMemcpyAsync(p->x_stage, x_src, (size_t)T * H * 2, cudaMemcpyDefault, sr));
+  } else if (x_src && !tc_router) {
+    MOE_CK(stage_whole_input(p, x_src, (size_t)T * H * 2, st));   // whole copy first
+  }
+  MOE_CK(cudaMemsetAsync(p->ws.gbar, 0, zero_bytes, sr));
   if (tc_router) {
     // split plan of the whole forward, whatever the ranges: the same logits either way
     const RouterSplit sp = router_split(T, H, E, p->num_sms);
@@ -355,7 +374,7 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
     // (with MOE_FLAG_HOST_PIPELINE the upload ran beside the previous forward: no range waits)
     const int nr = (x_src && !(c.flags & MOE_FLAG_HOST_PIPELINE)) ? std::min(HOST_RANGES, chunks) : 1;
     const int per = ((chunks + nr - 1) / nr) * DS_CHUNK_TOK;
-    if (x_src) {
+    if (x_src && !aside) {
       MOE_CK(wait_staging_free(p, st));
       for (int r = 0; r * per < T; ++r) {
         const size_t off = (size_t)r * per * H * 2, n = (size_t)std::min(per, T - r * per) * H * 2;
@@ -364,11 +383,11 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
         MOE_CK(cudaEventRecord(p->ev_range[r], p->st_aux));
       }
     }
-    MOE_CK(launch_router_prep(static_cast<const uint16_t*>(W_router), H, E, p->rw, st));
+    MOE_CK(launch_router_prep(static_cast<const uint16_t*>(W_router), H, E, p->rw, sr));
     ++nl;
     for (int r = 0; r * per < T; ++r) {
       const int t0 = r * per, tn = std::min(per, T - t0);
-      if (x_src) MOE_CK(cudaStreamWaitEvent(st, p->ev_range[r], 0));
+      if (x_src && !aside) MOE_CK(cudaStreamWaitEvent(st, p->ev_range[r], 0));
       const uint16_t* xr = static_cast<const uint16_t*>(x) + (size_t)t0 * H;
       CUtensorMap tX;
       if (!make_tmap(&tX, xr, H, (uint64_t)tn, 128)) {
@@ -378,24 +397,28 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
       MOE_CK(launch_router_tc(tX, tW, xr, p->bias, p->rw, sp, tn, H, E, k, p->num_sms,
                               router_logits + (size_t)t0 * E, p->ws.ids + (size_t)t0 * k, p->ws.w + (size_t)t0 * k,
                               p->ws.counts, p->ws.chist + (size_t)(t0 / DS_CHUNK_TOK) * E, p->ws.err, c.timeout_ns,
-                              st));
+                              sr));
       nl += 2;
     }
   } else {
     bool topk_done = false;
     if (W_router && rchoice == ROUTER_CANON_TASKS) {
       MOE_CK(launch_router_tasks(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router), p->bias,
-                                 router_logits, p->ws, T, H, E, k, p->num_sms, &topk_done, st));
+                                 router_logits, p->ws, T, H, E, k, p->num_sms, &topk_done, sr));
       ++nl;
     } else if (W_router) {
       MOE_CK(launch_router_logits(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(W_router),
-                                  p->bias, router_logits, T, H, E, st));
+                                  p->bias, router_logits, T, H, E, sr));
       ++nl;
     }
     if (!topk_done) {
-      MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->ws.chist, p->num_sms, st));
+      MOE_CK(launch_topk(router_logits, T, E, k, p->ws.ids, p->ws.w, p->ws.counts, p->ws.chist, p->num_sms, sr));
       ++nl;
     }
+  }
+  if (aside) {
+    MOE_CK(cudaEventRecord(p->ev_routed, sr));
+    MOE_CK(cudaStreamWaitEvent(st, p->ev_routed, 0));
   }
   rec(1);
   // schedule actually run: MOE_SCHED_AUTO resolves to wave-serial with one wave of all experts
@@ -406,7 +429,8 @@ moe_status_t forward_impl(moe_plan_t p, int32_t T, const void* x, const void* x_
   ++nl;
   rec(2);
   MOE_CK(launch_gather(static_cast<const uint16_t*>(x), p->ws.prow_of, T, H, k, p->ws.x_pad, st));
-  if (x == p->x_stage) MOE_CK(cudaEventRecord(p->ev_xfree, st));   // x_stage free for the next upload
+  if (c.flags & MOE_FLAG_HOST_PIPELINE)   // x_stage and the routing buffers free for the next forward
+    MOE_CK(cudaEventRecord(p->ev_xfree, st));
   ++nl;
   rec(3);
   CUtensorMap tA1, tB1, tA2, tB2, tH, tP;
@@ -569,6 +593,7 @@ moe_status_t moe_plan(const moe_config_t* cfg, int device, moe_plan_t* out) {
   if (cudaStreamCreateWithFlags(&p->st_aux, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_xfree, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ev_routed, cudaEventDisableTiming) != cudaSuccess ||
       cudaStreamCreateWithFlags(&p->st_out, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_ydone, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->ev_ylast, cudaEventDisableTiming) != cudaSuccess ||
@@ -646,7 +671,9 @@ moe_status_t moe_host_wait(moe_plan_t p, void* stream) {
 moe_status_t moe_get_status(moe_plan_t p, void* stream) {
   if (!p) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(st) != cudaSuccess || cudaStreamSynchronize(p->st_out) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess || cudaStreamSynchronize(p->st_aux) != cudaSuccess ||
+      cudaStreamSynchronize(p->st_out) != cudaSuccess)
+    return MOE_ERR_CUDA;
   uint32_t e = 0;
   if (cudaMemcpy(&e, p->ws.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (e != 0 && cudaMemset(p->ws.err, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;

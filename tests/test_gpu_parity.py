@@ -974,6 +974,36 @@ def test_host_pipeline_back_to_back():
     layer.close()
 
 
+def test_host_pipeline_mixed_with_device_forwards():
+    """A plan with MOE_FLAG_HOST_PIPELINE serving device-buffer and pipelined host-buffer
+    forwards in turn: a host forward's routing, which runs on the plan's own stream, must still
+    wait for the previous device forward's Dispatch (the last reader of the routing buffers).
+    Every y bitwise equal to a plain plan's forward of the same input."""
+    wl = synth.Workload("pipe", 1000, 1024, 256, 64, 4)
+    w = synth.device_inputs(wl)
+    xs = [w["x"], synth.device_inputs(synth.Workload("pipe", 1000, 1024, 256, 64, 4, seed=6))["x"]]
+    ref = _layer(wl)
+    y_ref = [ref.forward(x, w["Wr"], w["W1"], w["W2"], check=True)[0].cpu() for x in xs]
+    ref.close()
+    layer = _layer(wl, flags=moe.MOE_FLAG_HOST_PIPELINE)
+    x_host = [x.cpu().pin_memory() for x in xs]
+    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    outs = []
+    for i, (xi, host) in enumerate([(0, False), (1, True), (1, False), (0, True), (0, False), (1, True)]):
+        if host:
+            yh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+            layer.forward_host(x_host[xi], w["Wr"], w["W1"], w["W2"], lg, yh)
+            outs.append((xi, yh))
+        else:
+            outs.append((xi, layer.forward(xs[xi], w["Wr"], w["W1"], w["W2"])[0]))
+    layer.host_wait()
+    torch.cuda.current_stream().synchronize()
+    for i, (xi, y) in enumerate(outs):
+        assert torch.equal(y.cpu().view(torch.int16), y_ref[xi].view(torch.int16)), f"forward {i}"
+    layer.check()
+    layer.close()
+
+
 @pytest.mark.parametrize("extra", [0, moe.MOE_FLAG_SINGLE_LAUNCH])
 def test_host_pipeline_output_copies(extra):
     """MOE_FLAG_HOST_PIPELINE output side: y leaves through the plan's alternating staging buffers
