@@ -429,6 +429,8 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
                "ms_per_step": e_ms, "tokens_per_s": ws * wl.T / (e_ms * 1e-3),
                "host_pipeline": True,
                "timing": "one span over the back-to-back steps, first step's start to the last y in host memory",
+               "overlap": ("each forward's upload and routing run beside the previous forward's last kernels, "
+                           "its output copy beside the next forward; the first upload and the last copy are exposed"),
                "l2": (f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write), flush time taken out"
                       if flush_steps else
                       f"not flushed: the {weight_bytes / 2**30:.2f} GiB of expert weights exceed L2 "
