@@ -356,7 +356,7 @@ def _random_cases_many_tokens(n: int, seed: int = 20261203):
     return out
 
 
-@pytest.mark.parametrize("c", _random_cases(24) + _random_cases_many_tokens(32),
+@pytest.mark.parametrize("c", _random_cases(48) + _random_cases_many_tokens(64),
                          ids=lambda c: "T{T}-H{H}-I{I}-E{E}-k{k}-s{sched}-f{flags}-z{zipf}-h{host:d}".format(**c))
 def test_random_shapes_full_oracle(c):
     """Routing (bit-exact) and y (stated tolerance) against the full oracle on seeded random
