@@ -905,6 +905,50 @@ def test_plan_reuse_long_random_sequence(schedule, flags):
     layer.close()
 
 
+def _random_mid_cases(n: int, seed: int = 20261204):
+    """Seeded mid-size layers: 1000 to 6000 tokens, H up to 3072 and I up to 1536 (multiples of
+    64), up to 256 experts (T*H*E <= 3e9, so that the oracle's logits stay cheap), with every
+    schedule and kernel variant and a Zipf router bias on some."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        T, H, I = int(rng.integers(1000, 6001)), 64 * int(rng.integers(8, 49)), 64 * int(rng.integers(4, 25))
+        E = int(rng.integers(8, 257))
+        k = int(rng.integers(1, min(8, E) + 1))
+        if T * H * E > 3e9:
+            continue
+        out.append(dict(T=T, H=H, I=I, E=E, k=k, zipf=float(rng.choice([0.0, 1.2])), sched=int(rng.integers(0, 4)),
+                        flags=[0, 0, EXACT, moe.MOE_FLAG_GEMM_COMPUTE, moe.MOE_FLAG_SINGLE_LAUNCH][int(rng.integers(0, 5))]))
+    return out
+
+
+@pytest.mark.parametrize("c", _random_mid_cases(16),
+                         ids=lambda c: "T{T}-H{H}-I{I}-E{E}-k{k}-s{sched}-f{flags}-z{zipf}".format(**c))
+def test_random_mid_shapes_sampled(c):
+    """Seeded mid-size shapes (experts of several 256-row units, H and I well past one tile):
+    logits and routing of every token against the oracle, y on 24 sampled tokens within the
+    stated tolerance."""
+    wl = synth.Workload("mid", c["T"], c["H"], c["I"], c["E"], c["k"], zipf_s=c["zipf"])
+    bias = _bias(wl)
+    d = synth.device_inputs(wl)
+    layer = _layer(wl, c["sched"], flags=c["flags"], bias=bias)
+    y, logits = layer.forward(d["x"], d["Wr"], d["W1"], d["W2"], check=True)
+    h = synth.host_inputs(wl, weights=False)
+    lg_ref = oracle.router_logits(h["x"], h["Wr"], bias)
+    tok = sample_tokens(c["T"], 24, seed=c["T"])
+    ref = oracle.forward(h["x"], h["Wr"], bias, lambda e: _device_weights(d)("W1", e),
+                         lambda e: _device_weights(d)("W2", e), wl.k, tokens=tok, logits=lg_ref, bounds=True)
+    if c["flags"] & (EXACT | moe.MOE_FLAG_SINGLE_LAUNCH):     # all logits canonical
+        assert np.array_equal(logits.cpu().numpy(), lg_ref)
+    else:
+        check_logits(logits.cpu().numpy(), ref, h["x"], h["Wr"], layer.router_bound(c["T"]), bias)
+    routing_equal(layer.routing(c["T"]), ref, c["T"])
+    check_y(bits(y)[tok], ref, what=f"T={c['T']}")
+    del d
+    layer.close()
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("T,schedule,zipf", [(65536, moe.MOE_SCHED_AUTO, 0.0), (131072, moe.MOE_SCHED_AUTO, 1.2),
                                              (65536, moe.MOE_SCHED_INTERLEAVED, 0.0)])
 def test_many_tokens_routing_and_sampled_y(T, schedule, zipf):
