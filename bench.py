@@ -661,6 +661,56 @@ def run_schedule_sweep(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- single-launch phases
+PHASE_NAMES = ("router_logits", "topk", "dispatch", "gather", "grouped_gemm", "combine")
+
+
+def run_phase_trace(args, wl):
+    """The single-launch layer (MOE_FLAG_SINGLE_LAUNCH with MOE_FLAG_TRACE) on wl: the time of
+    each phase inside the launch from the kernel's own %globaltimer stamps at the phase boundaries
+    (CTA 0; the last row of moe_trace_read), beside the multi-launch path's stage times (CUDA
+    events between the stages); `--steps` forwards of each after `--warmup`, alternating, L2
+    flushed before each; medians.  One JSON line."""
+    import numpy as np
+    import torch
+    import mixture_experts_layer_top_gb300 as moe
+    moe.build()
+    torch.cuda.set_device(0)
+    d = synth.device_inputs(wl, device="cuda")
+    bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    single = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k,
+                                        flags=moe.MOE_FLAG_SINGLE_LAUNCH | moe.MOE_FLAG_TRACE), 0, router_bias=bias)
+    multi = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=moe.MOE_FLAG_STAGE_TIMING), 0,
+                         router_bias=bias)
+    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    phases, stages = [], []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        single.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=lg, y=y)
+        stamps = moe.moe_trace_read(single.plan)[-1][:len(PHASE_NAMES) + 1].astype(np.int64)
+        flush.zero_()
+        multi.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=lg, y=y)
+        st = multi.stage_times()
+        if i >= args.warmup:
+            phases.append(np.diff(stamps) / 1e3)
+            stages.append(st)
+    single.check()
+    multi.check()
+    single.close()
+    multi.close()
+    ph = np.median(np.array(phases), axis=0)
+    print(json.dumps({"workload": f"{wl.name}: {wl.description}", "forwards": args.steps,
+                      "single_launch_phases_us": {n: round(float(v), 2) for n, v in zip(PHASE_NAMES, ph)},
+                      "single_launch_total_us": round(float(ph.sum()), 2),
+                      "multi_launch_stages_us": {n: round(1e3 * statistics.median(s[n] for s in stages), 2)
+                                                 for n in stages[0]},
+                      "note": "phases: %globaltimer stamps of CTA 0 inside the one launch; stages: CUDA events "
+                              "between the multi-launch path's kernels (they serialise its launches)"}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -688,6 +738,8 @@ def main(argv=None):
                     help="run the headline (and --also) workloads with the whole layer in one launch")
     ap.add_argument("--schedule-sweep", action="store_true",
                     help="time every tile schedule over a sweep of routing skew and token counts (JSON lines)")
+    ap.add_argument("--phase-trace", action="store_true",
+                    help="time the phases inside the single-launch layer on --workload (one JSON line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -704,6 +756,8 @@ def main(argv=None):
                             description=f"custom T={T} H={H} I={I} E={E} top-{k}" + (f" Zipf({z})" if z else ""))
     if args.schedule_sweep:
         return run_schedule_sweep(args)
+    if args.phase_trace:
+        return run_phase_trace(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
