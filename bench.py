@@ -323,12 +323,15 @@ def config_of(wl, args, single=None):
     sched = {0: "wave-serial", 1: "interleaved", 2: "phased (L1 launch, L2 launch)",
              3: "auto (wave-serial, one wave of all experts)"}[args.schedule]
     split = "streaming" if args.gemm_split == "auto" else args.gemm_split
-    return {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-            "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
-            "wave_experts": args.wave_experts, "lead_waves": args.lead_waves,
-            "launch": "single (MOE_FLAG_SINGLE_LAUNCH)" if single else "multi",
-            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
-            "parallelism": f"replicas x{args.gpus} (no sharding)"}
+    cfg = {"workload": f"{wl.name}: {wl.description}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+           "top_k": wl.k, "zipf_s": wl.zipf_s, "schedule": sched, "gemm_split": split,
+           "wave_experts": args.wave_experts, "lead_waves": args.lead_waves,
+           "launch": "single (MOE_FLAG_SINGLE_LAUNCH)" if single else "multi",
+           "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+           "parallelism": f"replicas x{args.gpus} (no sharding)"}
+    if getattr(args, "exact_logits", False):
+        cfg["router"] = "all logits canonical (MOE_FLAG_EXACT_LOGITS)"
+    return cfg
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -347,6 +350,8 @@ def measure(wl, d, args, dev, local, peaks, peak_src, group, ws, sampler, with_e
     bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
     flags = {"auto": 0, "streaming": moe.MOE_FLAG_GEMM_STREAMING, "compute": moe.MOE_FLAG_GEMM_COMPUTE}[args.gemm_split]
     flags |= extra_flags
+    if getattr(args, "exact_logits", False):
+        flags |= moe.MOE_FLAG_EXACT_LOGITS
     single = bool(flags & moe.MOE_FLAG_SINGLE_LAUNCH)
     cfg = dict(schedule=args.schedule, wave_experts=args.wave_experts, lead_waves=args.lead_waves)
     layer = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=flags, **cfg), local, router_bias=bias)
@@ -661,6 +666,56 @@ def run_schedule_sweep(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- grouped-GEMM wait trace
+def run_gemm_trace(args, wl):
+    """The grouped GEMM's per-role wait times on wl with the chosen schedule (MOE_FLAG_TRACE,
+    moe_trace_read): per CTA the nanoseconds each role spent blocked - producer on a free stage,
+    producer on Linear-1 readiness, MMA issuer on a free accumulator, MMA issuer on operands,
+    epilogue on an accumulator - summed over the CTAs and divided by their summed lifetimes;
+    median over `--steps` forwards after `--warmup`, L2 flushed before each, beside the GEMM
+    launch time of a second plan (its stage events).  One JSON line."""
+    import numpy as np
+    import torch
+    import mixture_experts_layer_top_gb300 as moe
+    moe.build()
+    torch.cuda.set_device(0)
+    d = synth.device_inputs(wl, device="cuda")
+    bias = synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    cfg = dict(schedule=args.schedule, wave_experts=args.wave_experts, lead_waves=args.lead_waves)
+    traced = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=moe.MOE_FLAG_TRACE, **cfg), 0,
+                          router_bias=bias)
+    timed = moe.MoELayer(moe.MoEConfig(wl.T, wl.H, wl.I, wl.E, wl.k, flags=moe.MOE_FLAG_STAGE_TIMING, **cfg), 0,
+                         router_bias=bias)
+    lg = torch.empty((wl.T, wl.E), dtype=torch.float32, device="cuda")
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    fracs, gemm = [], []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        traced.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=lg, y=y)
+        tr = moe.moe_trace_read(traced.plan)[:-1].astype(np.float64)   # the last row: single-launch stamps
+        live = tr[:, 5] > 0
+        flush.zero_()
+        timed.forward(d["x"], d["Wr"], d["W1"], d["W2"], logits=lg, y=y)
+        g = timed.stage_times()["grouped_gemm"]
+        if i >= args.warmup:
+            fracs.append(tr[live, :5].sum(axis=0) / tr[live, 5].sum())
+            gemm.append(g)
+    traced.check()
+    timed.check()
+    traced.close()
+    timed.close()
+    med = np.median(np.array(fracs), axis=0)
+    names = ("producer_free_stage", "producer_l1_readiness", "mma_free_accumulator", "mma_operands",
+             "epilogue_accumulator")
+    print(json.dumps({"workload": f"{wl.name}: {wl.description}", "schedule": config_of(wl, args)["schedule"],
+                      "forwards": args.steps, "gemm_ms": round(statistics.median(gemm), 4),
+                      "wait_fraction_of_cta_lifetime": {n: round(float(v), 3) for n, v in zip(names, med)},
+                      "note": "a wait is clocked from its first failed barrier probe: waits that end inside "
+                              "that probe are not counted"}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- single-launch phases
 PHASE_NAMES = ("router_logits", "topk", "dispatch", "gather", "grouped_gemm", "combine")
 
@@ -738,6 +793,10 @@ def main(argv=None):
                     help="run the headline (and --also) workloads with the whole layer in one launch")
     ap.add_argument("--schedule-sweep", action="store_true",
                     help="time every tile schedule over a sweep of routing skew and token counts (JSON lines)")
+    ap.add_argument("--exact-logits", action="store_true",
+                    help="every router logit in the canonical order on the CUDA cores (MOE_FLAG_EXACT_LOGITS)")
+    ap.add_argument("--gemm-trace", action="store_true",
+                    help="per-role wait times of the grouped GEMM on --workload with --schedule (one JSON line)")
     ap.add_argument("--phase-trace", action="store_true",
                     help="time the phases inside the single-launch layer on --workload (one JSON line)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -758,6 +817,8 @@ def main(argv=None):
         return run_schedule_sweep(args)
     if args.phase_trace:
         return run_phase_trace(args, wl)
+    if args.gemm_trace:
+        return run_gemm_trace(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
