@@ -905,6 +905,51 @@ def test_plan_reuse_long_random_sequence(schedule, flags):
     layer.close()
 
 
+@pytest.mark.parametrize("flags", [0, moe.MOE_FLAG_SINGLE_LAUNCH])
+def test_host_pipeline_long_random_sequence(flags):
+    """Forty forwards of one MOE_FLAG_HOST_PIPELINE plan enqueued back to back with no
+    synchronisation: seeded random token counts (1 to 2048, every router the rule picks),
+    pipelined host forwards (routing on the plan's copy stream, y copied out beside the next
+    forward) mixed with device-buffer forwards, each with its own output and logits buffers.
+    After moe_host_wait every y and every logits row bitwise equal to a plain plan's forward of
+    the same input."""
+    H, I, E, k, T_max = 512, 256, 64, 4, 2048
+    rng = np.random.default_rng(78)
+    wl_max = synth.Workload("seq", T_max, H, I, E, k)
+    w = synth.device_inputs(wl_max)
+    xs = synth.device_inputs(synth.Workload("seq", T_max, H, I, E, k, seed=7))["x"]
+    steps = []
+    for _ in range(40):
+        T = int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(65, 700)), int(rng.integers(700, T_max + 1))]))
+        off = int(rng.integers(0, T_max - T + 1))
+        steps.append((T, off, bool(rng.integers(0, 3) != 0)))
+    plain = _layer(wl_max, flags=flags)
+    ref = []
+    for T, off, _ in steps:
+        y_r, lg_r = plain.forward(xs[off:off + T].contiguous(), w["Wr"], w["W1"], w["W2"], check=True)
+        ref.append((y_r.cpu(), lg_r.cpu()))
+    plain.close()
+    layer = _layer(wl_max, flags=flags | moe.MOE_FLAG_HOST_PIPELINE)
+    x_host = xs.cpu().pin_memory()       # written on the host before any pipelined forward
+    outs = []
+    torch.cuda.synchronize()
+    for T, off, host in steps:
+        lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        if host:
+            y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+            layer.forward_host(x_host[off:off + T], w["Wr"], w["W1"], w["W2"], lg, y)
+        else:
+            y, _ = layer.forward(xs[off:off + T].contiguous(), w["Wr"], w["W1"], w["W2"], logits=lg)
+        outs.append((y, lg))
+    layer.host_wait()
+    torch.cuda.current_stream().synchronize()
+    for i, ((T, off, host), (y, lg), (y_r, lg_r)) in enumerate(zip(steps, outs, ref)):
+        assert torch.equal(lg.cpu(), lg_r), f"logits differ at step {i} (T={T}, host={host})"
+        assert torch.equal(y.cpu().view(torch.int16), y_r.view(torch.int16)), f"y differs at step {i} (T={T}, host={host})"
+    layer.check()
+    layer.close()
+
+
 def _random_mid_cases(n: int, seed: int = 20261204):
     """Seeded mid-size layers: 1000 to 6000 tokens, H up to 3072 and I up to 1536 (multiples of
     64), up to 256 experts (T*H*E <= 3e9, so that the oracle's logits stay cheap), with every
